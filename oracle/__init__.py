@@ -1,0 +1,173 @@
+"""fp64 CPU oracle for sink attention -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product (the CUDA library and its
+Python binding) never imports it and has no CPU fallback.
+
+The arithmetic lives in ``sinkattn_oracle.c`` (plain C, double precision);
+this module compiles it with gcc into ``oracle/_build/`` and wraps it for
+numpy arrays.  The method it states is the one described in the "GPT-OSS on
+day 0" blog post, section "Kernels for GPT-OSS / Sink Attention": a per-head
+learned sink logit that enters the softmax normaliser and has no value row.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from pathlib import Path
+
+import numpy as np
+
+_HERE = Path(__file__).resolve().parent
+_SRC = _HERE / "sinkattn_oracle.c"
+_BUILD = _HERE / "_build"
+_LIB_PATH = _BUILD / "libsinkattn_oracle.so"
+_lib = None
+
+
+def build(force: bool = False) -> Path:
+    """Compile the oracle shared library (gcc, OpenMP when available)."""
+    if _LIB_PATH.exists() and not force and _LIB_PATH.stat().st_mtime >= _SRC.stat().st_mtime:
+        return _LIB_PATH
+    _BUILD.mkdir(exist_ok=True)
+    tmp = _LIB_PATH.with_suffix(f".{os.getpid()}.tmp")
+    base = ["gcc", "-O2", "-std=c11", "-shared", "-fPIC", str(_SRC), "-o", str(tmp), "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        _lib = ctypes.CDLL(str(build()))
+        P = ctypes.c_void_p
+        i = ctypes.c_int
+        f = ctypes.c_float
+        _lib.oracle_decode.argtypes = [i, i, i, i, i, i, i, P, P, P, P, P, P, f, i, P, P, P]
+        _lib.oracle_prefill.argtypes = [i, P, i, i, i, i, P, P, P, P, f, i, i, P, P, P]
+        _lib.oracle_decode_partials.argtypes = [i, i, i, i, i, i, i, P, P, P, P, P, P, f, i, i, i, P, P]
+        _lib.oracle_merge.argtypes = [i, i, i, i, P, P, P, P, P]
+        for fn in ("oracle_decode", "oracle_prefill", "oracle_decode_partials", "oracle_merge",
+                   "oracle_num_threads"):
+            getattr(_lib, fn).restype = ctypes.c_int
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _bf16_bits(a) -> np.ndarray:
+    """Accept a uint16 array of bf16 bit patterns or a torch bf16 tensor."""
+    if hasattr(a, "dtype") and str(a.dtype) == "torch.bfloat16":
+        import torch
+
+        a = a.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint16:
+        raise TypeError("bf16 inputs must be uint16 bit patterns or torch.bfloat16")
+    return a
+
+
+def _np(a, dtype):
+    if hasattr(a, "detach"):
+        a = a.detach().cpu().numpy()
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _check(rc: int, what: str):
+    if rc == -2:
+        raise IndexError(f"{what}: page id out of range")
+    if rc != 0:
+        raise ValueError(f"{what}: bad arguments (code {rc})")
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def decode(q, k_pages, v_pages, page_table, kv_lens, sinks, scale, rows=None):
+    """Sink-attention decode by definition.
+
+    q [B,Hq,D] bf16; k_pages/v_pages [P,Hkv,PS,D] bf16; page_table [B,maxpg]
+    int32; kv_lens [B] int32; sinks [Hq] f32.  rows: optional int array of
+    (b, h) pairs.  Returns (out float64 [B,Hq,D] or [n,D], lse float64).
+    """
+    q, kp, vp = _bf16_bits(q), _bf16_bits(k_pages), _bf16_bits(v_pages)
+    pt, kl, sk = _np(page_table, np.int32), _np(kv_lens, np.int32), _np(sinks, np.float32)
+    B, Hq, D = q.shape
+    P, Hkv, PS, _ = kp.shape
+    if rows is not None:
+        rows = _np(rows, np.int32).reshape(-1, 2)
+        n = rows.shape[0]
+        out, lse = np.empty((n, D)), np.empty(n)
+    else:
+        n = B * Hq
+        out, lse = np.empty((B, Hq, D)), np.empty((B, Hq))
+    rc = _load().oracle_decode(B, Hq, Hkv, D, PS, pt.shape[1], P, _ptr(q), _ptr(kp), _ptr(vp),
+                               _ptr(pt), _ptr(kl), _ptr(sk), float(scale), n, _ptr(rows),
+                               _ptr(out), _ptr(lse))
+    _check(rc, "oracle.decode")
+    return out, lse
+
+
+def prefill(q, k, v, cu_seqlens, sinks, scale, causal=True, rows=None):
+    """Sink-attention prefill by definition over packed varlen sequences.
+
+    q [T,Hq,D], k/v [T,Hkv,D] bf16; cu_seqlens [N+1] int32.  rows: optional
+    (t, h) pairs.  Returns (out float64, lse float64).
+    """
+    q, k, v = _bf16_bits(q), _bf16_bits(k), _bf16_bits(v)
+    cu, sk = _np(cu_seqlens, np.int32), _np(sinks, np.float32)
+    T, Hq, D = q.shape
+    Hkv = k.shape[1]
+    if rows is not None:
+        rows = _np(rows, np.int32).reshape(-1, 2)
+        n = rows.shape[0]
+        out, lse = np.empty((n, D)), np.empty(n)
+    else:
+        n = T * Hq
+        out, lse = np.empty((T, Hq, D)), np.empty((T, Hq))
+    rc = _load().oracle_prefill(len(cu) - 1, _ptr(cu), T, Hq, Hkv, D, _ptr(q), _ptr(k), _ptr(v),
+                                _ptr(sk), float(scale), int(bool(causal)), n, _ptr(rows),
+                                _ptr(out), _ptr(lse))
+    _check(rc, "oracle.prefill")
+    return out, lse
+
+
+SINK_IN_FIRST_CHUNK = 0
+SINK_IN_NO_CHUNK = 1
+SINK_IN_EVERY_CHUNK = 2  # the wrong rule; exists only for a negative test
+
+
+def decode_partials(q, k_pages, v_pages, page_table, kv_lens, sinks, scale, num_chunks,
+                    chunk_tokens, sink_mode=SINK_IN_FIRST_CHUNK):
+    """Per-chunk partial results (o_c, lse_c) of decode, by definition."""
+    q, kp, vp = _bf16_bits(q), _bf16_bits(k_pages), _bf16_bits(v_pages)
+    pt, kl, sk = _np(page_table, np.int32), _np(kv_lens, np.int32), _np(sinks, np.float32)
+    B, Hq, D = q.shape
+    P, Hkv, PS, _ = kp.shape
+    po = np.empty((num_chunks, B, Hq, D))
+    pl = np.empty((num_chunks, B, Hq))
+    rc = _load().oracle_decode_partials(B, Hq, Hkv, D, PS, pt.shape[1], P, _ptr(q), _ptr(kp),
+                                        _ptr(vp), _ptr(pt), _ptr(kl), _ptr(sk), float(scale),
+                                        num_chunks, chunk_tokens, sink_mode, _ptr(po), _ptr(pl))
+    _check(rc, "oracle.decode_partials")
+    return po, pl
+
+
+def merge(partial_o, partial_lse, sinks=None):
+    """Log-sum-exp merge of partials [S,R,H,D] / [S,R,H]; sinks [H] adds the sink once."""
+    po = _np(partial_o, np.float64)
+    pl = _np(partial_lse, np.float64)
+    S, R, H, D = po.shape
+    sk = None if sinks is None else _np(sinks, np.float32)
+    out, lse = np.empty((R, H, D)), np.empty((R, H))
+    rc = _load().oracle_merge(S, R, H, D, _ptr(po), _ptr(pl), _ptr(sk), _ptr(out), _ptr(lse))
+    _check(rc, "oracle.merge")
+    return out, lse

@@ -1,0 +1,329 @@
+"""Pins of the fp64 oracle to facts that do not come from the oracle itself.
+
+The blog posts that define the method ("GPT-OSS on day 0", section "Kernels
+for GPT-OSS / Sink Attention") print no worked example: their equations were
+lost.  What they fix in prose -- a per-head sink logit inside the softmax
+normaliser with no value row, the online state seeded from the sink, and the
+sink held by the first chunk only when the sequence is split -- is pinned
+here through library routines, closed forms, invariants and special cases:
+
+* sink = -inf reduces to ordinary attention: torch's fp64 SDPA;
+* any sink equals SDPA over the keys plus one zero key whose logit is the
+  sink (additive mask) and whose value row is zero;
+* a single key has the closed form e^s / (e^s + e^sink) * v;
+* a huge sink drives out to 0 and lse to the sink;
+* constant V gives out = c * (1 - e^(sink - lse));
+* one-hot V exposes the weights: ratios e^(s_j - s_k), mass 1 with the sink;
+* split + merge equals unsplit for both sink routes, and the wrong rule
+  (every chunk seeded) is caught;
+* permuting the page pool with the page table changes nothing;
+* prefill row i equals decode over keys 0..i; GQA equals explicit head repeat.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+from gqa_attention_learned_head_gb300 import workloads as W
+
+TOL = 1e-12
+
+
+def bf16(x):
+    return torch.as_tensor(x, dtype=torch.float32).to(torch.bfloat16)
+
+
+def gather_kv(inp, b, kvh):
+    """Contiguous K, V rows [len, D] (float64) of request b, KV head kvh."""
+    L = int(inp.kv_lens[b])
+    t = torch.arange(L)
+    pages = inp.page_table[b, t // W.PAGE_SIZE].long()
+    k = inp.k_pages[pages, kvh, t % W.PAGE_SIZE].double()
+    v = inp.v_pages[pages, kvh, t % W.PAGE_SIZE].double()
+    return k, v
+
+
+def sdpa_with_sink(q, k, v, sink, scale, causal=False):
+    """torch SDPA (fp64) with the sink modelled as an extra zero key of logit `sink` and zero value.
+
+    q [H, Lq, D], k/v [H, Lk, D]; sink [H].  causal aligns query i with key i.
+    """
+    H, Lq, D = q.shape
+    Lk = k.shape[1]
+    k1 = torch.cat([k, torch.zeros(H, 1, D, dtype=k.dtype)], 1)
+    v1 = torch.cat([v, torch.zeros(H, 1, D, dtype=v.dtype)], 1)
+    mask = torch.zeros(H, Lq, Lk + 1, dtype=torch.float64)
+    if causal:
+        mask[:, :, :Lk] = torch.triu(torch.full((Lq, Lk), float("-inf"), dtype=torch.float64), 1)
+    mask[:, :, Lk] = torch.as_tensor(sink, dtype=torch.float64)[:, None]
+    return F.scaled_dot_product_attention(q[None], k1[None], v1[None], attn_mask=mask[None],
+                                          scale=scale)[0]
+
+
+# ----------------------------------------------------------------------------------------
+# decode against library SDPA
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(4, 1), (8, 2), (16, 2)])
+def test_decode_minus_inf_sink_is_plain_attention(Hq, Hkv):
+    inp = W.make_decode(3, Hq, Hkv, [1, 37, 64], seed=1)
+    inp.sinks[:] = float("-inf")
+    out, lse = oracle.decode(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens,
+                             inp.sinks, inp.scale)
+    G = Hq // Hkv
+    for b in range(3):
+        for kvh in range(Hkv):
+            k, v = gather_kv(inp, b, kvh)
+            q = inp.q[b, kvh * G:(kvh + 1) * G].double()[:, None]  # [G,1,D]
+            ref = F.scaled_dot_product_attention(q, k.expand(G, -1, -1), v.expand(G, -1, -1),
+                                                 scale=inp.scale)[:, 0]
+            np.testing.assert_allclose(out[b, kvh * G:(kvh + 1) * G], ref.numpy(), rtol=0, atol=TOL)
+            # lse of plain attention: log-sum-exp of the scaled scores (torch routine)
+            s = inp.scale * (q[:, 0] @ k.T)
+            np.testing.assert_allclose(lse[b, kvh * G:(kvh + 1) * G],
+                                       torch.logsumexp(s, -1).numpy(), rtol=0, atol=TOL)
+
+
+@pytest.mark.parametrize("sink_std", [0.5, 3.0])
+def test_decode_sink_equals_sdpa_with_zero_value_key(sink_std):
+    inp = W.make_decode(4, 8, 2, [5, 16, 17, 90], seed=2, sink_std=sink_std)
+    out, _ = oracle.decode(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens,
+                           inp.sinks, inp.scale)
+    for b in range(4):
+        for kvh in range(2):
+            k, v = gather_kv(inp, b, kvh)
+            q = inp.q[b, kvh * 4:(kvh + 1) * 4].double()[:, None]
+            ref = sdpa_with_sink(q, k.expand(4, -1, -1), v.expand(4, -1, -1),
+                                 inp.sinks[kvh * 4:(kvh + 1) * 4], inp.scale)[:, 0]
+            np.testing.assert_allclose(out[b, kvh * 4:(kvh + 1) * 4], ref.numpy(), rtol=0, atol=TOL)
+
+
+# ----------------------------------------------------------------------------------------
+# closed forms and limits
+
+
+def test_single_key_closed_form():
+    inp = W.make_decode(1, 4, 1, [1], seed=3)
+    out, lse = oracle.decode(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens,
+                             inp.sinks, inp.scale)
+    k, v = gather_kv(inp, 0, 0)
+    for h in range(4):
+        s = inp.scale * float(inp.q[0, h].double() @ k[0])
+        sig = float(inp.sinks[h])
+        w = math.exp(s) / (math.exp(s) + math.exp(sig))
+        np.testing.assert_allclose(out[0, h], w * v[0].numpy(), rtol=0, atol=TOL)
+        assert abs(lse[0, h] - math.log(math.exp(s) + math.exp(sig))) < TOL
+
+
+def test_huge_sink_takes_all_mass():
+    inp = W.make_decode(2, 4, 1, [3, 40], seed=4)
+    inp.sinks[:] = 1.0e4
+    out, lse = oracle.decode(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens,
+                             inp.sinks, inp.scale)
+    assert np.all(out == 0.0)
+    assert np.all(lse == 1.0e4)
+
+
+def test_growing_sink_shrinks_output():
+    inp = W.make_decode(1, 4, 1, [50], seed=5)
+    norms = []
+    for sig in [-5.0, 0.0, 5.0, 10.0, 20.0, 40.0]:
+        inp.sinks[:] = sig
+        out, _ = oracle.decode(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens,
+                               inp.sinks, inp.scale)
+        norms.append(np.abs(out).max())
+    assert all(a > b for a, b in zip(norms, norms[1:]))
+    assert norms[-1] < 1e-12
+
+
+def test_empty_cache_puts_all_mass_on_sink():
+    inp = W.make_decode(2, 4, 1, [0, 0], seed=6)
+    inp.sinks[2] = float("-inf")
+    out, lse = oracle.decode(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens,
+                             inp.sinks, inp.scale)
+    assert np.all(out == 0.0)
+    for h in range(4):
+        assert lse[0, h] == float(inp.sinks[h])
+    assert lse[1, 2] == float("-inf")
+
+
+def test_constant_values():
+    inp = W.make_decode(2, 8, 2, [7, 33], seed=7)
+    c = 1.5
+    inp.v_pages[:] = c
+    out, lse = oracle.decode(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens,
+                             inp.sinks, inp.scale)
+    mass = 1.0 - np.exp(inp.sinks.double().numpy()[None, :] - lse)  # [B, Hq]
+    np.testing.assert_allclose(out, c * mass[..., None] * np.ones(64), rtol=0, atol=TOL)
+
+
+def test_one_hot_values_expose_weights():
+    L = 48
+    inp = W.make_decode(1, 4, 1, [L], seed=8, contiguous=True)
+    pages = inp.page_table[0, :3].long()
+    eye = torch.eye(64)[:L].reshape(3, W.PAGE_SIZE, 64)
+    inp.v_pages[pages, 0] = eye.to(torch.bfloat16)
+    out, lse = oracle.decode(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens,
+                             inp.sinks, inp.scale)
+    k, _ = gather_kv(inp, 0, 0)
+    for h in range(4):
+        s = inp.scale * (k @ inp.q[0, h].double()).numpy()
+        w = out[0, h, :L]
+        assert np.all(out[0, h, L:] == 0)
+        # weights are the exponentials of the scores (ratio e^(s_j - s_0)) ...
+        np.testing.assert_allclose(w / w[0], np.exp(s - s[0]), rtol=1e-12)
+        # ... and, together with the sink's share, sum to one
+        assert abs(w.sum() + math.exp(float(inp.sinks[h]) - lse[0, h]) - 1.0) < 1e-12
+
+
+# ----------------------------------------------------------------------------------------
+# split-KV + merge
+
+
+@pytest.mark.parametrize("S", [1, 2, 7, 32])
+def test_split_then_merge_equals_unsplit(S):
+    lens = [0, 1, 15, 16, 17, 300, 511]
+    inp = W.make_decode(len(lens), 8, 2, lens, seed=9)
+    chunk = max(1, -(-max(lens) // S))
+    ref_o, ref_l = oracle.decode(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens,
+                                 inp.sinks, inp.scale)
+    args = (inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens, inp.sinks, inp.scale,
+            S, chunk)
+    # the page's rule: the first chunk holds the sink, the merge does not add it
+    po, pl = oracle.decode_partials(*args, sink_mode=oracle.SINK_IN_FIRST_CHUNK)
+    o, l = oracle.merge(po, pl)
+    np.testing.assert_allclose(o, ref_o, rtol=0, atol=TOL)
+    np.testing.assert_allclose(l, ref_l, rtol=0, atol=TOL)
+    # the equivalent route: no chunk holds it, the merge adds it once
+    po, pl = oracle.decode_partials(*args, sink_mode=oracle.SINK_IN_NO_CHUNK)
+    o, l = oracle.merge(po, pl, inp.sinks)
+    np.testing.assert_allclose(o, ref_o, rtol=0, atol=TOL)
+    np.testing.assert_allclose(l, ref_l, rtol=0, atol=TOL)
+
+
+def test_seeding_every_chunk_is_detected():
+    """Planting the wrong rule (sink in every chunk) must break split == unsplit."""
+    inp = W.make_decode(2, 4, 1, [100, 64], seed=10)
+    ref_o, ref_l = oracle.decode(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens,
+                                 inp.sinks, inp.scale)
+    po, pl = oracle.decode_partials(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens,
+                                    inp.sinks, inp.scale, 4, 25,
+                                    sink_mode=oracle.SINK_IN_EVERY_CHUNK)
+    o, l = oracle.merge(po, pl)
+    assert np.abs(l - ref_l).max() > 1e-3
+    assert np.abs(o - ref_o).max() > 1e-3
+
+
+def test_merge_edge_rows():
+    po = np.zeros((3, 2, 1, 4))
+    pl = np.full((3, 2, 1), -np.inf)
+    po[1, 1, 0] = [1, 2, 3, 4]
+    pl[1, 1, 0] = 0.25
+    o, l = oracle.merge(po, pl)
+    assert np.all(o[0] == 0) and l[0, 0] == -np.inf          # nothing at all
+    np.testing.assert_array_equal(o[1, 0], [1, 2, 3, 4])      # one live partial passes through
+    assert l[1, 0] == 0.25
+    o, l = oracle.merge(po, pl, np.array([0.25], np.float32))  # sink equal to the live lse
+    np.testing.assert_allclose(o[1, 0], [0.5, 1, 1.5, 2], rtol=0, atol=TOL)
+    assert abs(l[1, 0] - (0.25 + math.log(2))) < TOL
+    assert np.all(o[0] == 0) and l[0, 0] == 0.25
+
+
+# ----------------------------------------------------------------------------------------
+# paging, GQA, prefill
+
+
+def test_page_permutation_invariance():
+    inp = W.make_decode(3, 8, 2, [40, 17, 64], seed=11)
+    out, lse = oracle.decode(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens,
+                             inp.sinks, inp.scale)
+    P = inp.k_pages.shape[0]
+    perm = torch.randperm(P, generator=torch.Generator().manual_seed(5))
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(P)
+    pt = inp.page_table.clone()
+    pt[pt >= 0] = inv[pt[pt >= 0].long()].int()
+    out2, lse2 = oracle.decode(inp.q, inp.k_pages[perm], inp.v_pages[perm], pt, inp.kv_lens,
+                               inp.sinks, inp.scale)
+    np.testing.assert_array_equal(out, out2)
+    np.testing.assert_array_equal(lse, lse2)
+
+
+def test_bad_page_id_is_reported():
+    inp = W.make_decode(1, 4, 1, [20], seed=12)
+    inp.page_table[0, 1] = 99
+    with pytest.raises(IndexError):
+        oracle.decode(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens, inp.sinks,
+                      inp.scale)
+
+
+def test_gqa_equals_explicit_head_repeat():
+    inp = W.make_decode(2, 8, 2, [30, 45], seed=13)
+    out, lse = oracle.decode(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens,
+                             inp.sinks, inp.scale)
+    rep = W.DecodeInputs(inp.q, inp.k_pages.repeat_interleave(4, 1),
+                         inp.v_pages.repeat_interleave(4, 1), inp.page_table, inp.kv_lens,
+                         inp.sinks, inp.scale)
+    out2, lse2 = oracle.decode(rep.q, rep.k_pages, rep.v_pages, rep.page_table, rep.kv_lens,
+                               rep.sinks, rep.scale)
+    np.testing.assert_array_equal(out, out2)
+    np.testing.assert_array_equal(lse, lse2)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_prefill_against_sdpa(causal):
+    inp = W.make_prefill(8, 2, [1, 37, 130], seed=14, causal=causal)
+    out, lse = oracle.prefill(inp.q, inp.k, inp.v, inp.cu_seqlens, inp.sinks, inp.scale, causal)
+    cu = inp.cu_seqlens.tolist()
+    for n in range(3):
+        a, b = cu[n], cu[n + 1]
+        q = inp.q[a:b].double().transpose(0, 1)                       # [Hq, L, D]
+        k = inp.k[a:b].double().transpose(0, 1).repeat_interleave(4, 0)
+        v = inp.v[a:b].double().transpose(0, 1).repeat_interleave(4, 0)
+        ref = sdpa_with_sink(q, k, v, inp.sinks, inp.scale, causal).transpose(0, 1)
+        np.testing.assert_allclose(out[a:b], ref.numpy(), rtol=0, atol=TOL)
+
+
+def test_prefill_rows_equal_decode_over_prefix():
+    L = 70
+    inp = W.make_prefill(4, 1, [L], seed=15)
+    out, lse = oracle.prefill(inp.q, inp.k, inp.v, inp.cu_seqlens, inp.sinks, inp.scale, True)
+    # the same keys as a contiguous paged cache
+    npg = -(-L // W.PAGE_SIZE)
+    kp = torch.zeros(npg * W.PAGE_SIZE, 1, 64, dtype=torch.bfloat16)
+    vp = torch.zeros_like(kp)
+    kp[:L], vp[:L] = inp.k, inp.v
+    kp = kp.view(npg, W.PAGE_SIZE, 1, 64).transpose(1, 2).contiguous()
+    vp = vp.view(npg, W.PAGE_SIZE, 1, 64).transpose(1, 2).contiguous()
+    pt = torch.arange(npg, dtype=torch.int32)[None].repeat(L, 1)
+    lens = torch.arange(1, L + 1, dtype=torch.int32)
+    dout, dlse = oracle.decode(inp.q, kp, vp, pt, lens, inp.sinks, inp.scale)
+    np.testing.assert_array_equal(out, dout)
+    np.testing.assert_array_equal(lse, dlse)
+    # row 0 of a sequence is the single-key closed form
+    for h in range(4):
+        s = inp.scale * float(inp.q[0, h].double() @ inp.k[0, 0].double())
+        w = math.exp(s) / (math.exp(s) + math.exp(float(inp.sinks[h])))
+        np.testing.assert_allclose(out[0, h], w * inp.v[0, 0].double().numpy(), rtol=0, atol=TOL)
+
+
+def test_row_selection_matches_full_result():
+    inp = W.make_decode(3, 8, 2, [10, 0, 33], seed=16)
+    out, lse = oracle.decode(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens,
+                             inp.sinks, inp.scale)
+    rows = np.array([[2, 7], [0, 0], [1, 3]], np.int32)
+    o, l = oracle.decode(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens,
+                         inp.sinks, inp.scale, rows=rows)
+    for i, (b, h) in enumerate(rows):
+        np.testing.assert_array_equal(o[i], out[b, h])
+        assert l[i] == lse[b, h]
+    pin = W.make_prefill(4, 2, [9, 20], seed=17)
+    out, lse = oracle.prefill(pin.q, pin.k, pin.v, pin.cu_seqlens, pin.sinks, pin.scale)
+    rows = np.array([[28, 1], [0, 3], [9, 0]], np.int32)
+    o, l = oracle.prefill(pin.q, pin.k, pin.v, pin.cu_seqlens, pin.sinks, pin.scale, rows=rows)
+    for i, (t, h) in enumerate(rows):
+        np.testing.assert_array_equal(o[i], out[t, h])
+        assert l[i] == lse[t, h]
