@@ -1,0 +1,555 @@
+#!/usr/bin/env python3
+"""Benchmark of libsinkattn (sink attention, GQA, paged split-KV decode + causal prefill).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload batched_paged_decode|long_context_decode|causal_prefill]
+
+Headline: decode KV GB/s on the batched paged decode workload (batch 32,
+64 q / 8 KV heads, head_dim 64, kv_len uniform in [512, 4096], 16-token pages
+randomly permuted in the pool).  One step = one sinkattn_decode call (split
+pass + merge), i.e. the whole decode hot path, on inputs resident in HBM.
+The L2 is flushed (256 MiB write) before every timed step.  Secondary lines
+for the long-context split-KV decode, the causal prefill and the mixed
+serving batch ride in the same JSON object under "secondary".
+
+Prints ONE JSON line on rank 0.  Under torchrun every rank runs its own
+independent batch (weak scaling, no collective on the data path); the
+barrier / max-over-ranks reduction only brackets the timing.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from pathlib import Path
+
+import torch
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+METRIC = "decode KV GB/s (% of HBM peak); prefill TFLOP/s (% of bf16 TC peak)"
+HBM_FALLBACK_GBS = 6800.0
+BF16_FALLBACK_TFLOPS = 1900.0
+L2_FLUSH_BYTES = 256 << 20
+
+WORKLOAD_TEXT = {
+    "tiny_decode": "tiny decode: batch 1, 4 q / 1 KV head, head_dim 64, kv_len 128, contiguous pages",
+    "batched_paged_decode": "batched paged decode: batch 32, 64 q / 8 KV heads, head_dim 64, kv_len U[512,4096], "
+                            "16-token pages randomly permuted in the pool",
+    "long_context_decode": "long-context split-KV decode: batch 4, 64 q / 8 KV heads, head_dim 64, kv_len 131072, "
+                           "32 chunks per request merged by LSE",
+    "causal_prefill": "causal prefill: 2 x 8192 tokens (varlen), 64 q / 8 KV heads, head_dim 64",
+    "mixed_serving": "mixed serving batch: 8 causal prefills L~U[256,4096] + 256 paged decodes kv_len~U[1024,32768], "
+                     "64 q / 8 KV heads, two streams",
+}
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        try:
+            d = json.loads(p.read_text())
+            return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+        except Exception:
+            pass
+    return HBM_FALLBACK_GBS, BF16_FALLBACK_TFLOPS, 1700.0, "fallback"
+
+
+def kernel_source_hash(names):
+    h = hashlib.sha256()
+    for n in names:
+        h.update((ROOT / "gqa_attention_learned_head_gb300" / "csrc" / n).read_bytes())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel, workload, sources):
+    """DRAM bytes per launch from a committed ncu summary, if taken on the current kernel source."""
+    p = ROOT / "profiles" / f"{kernel}.{workload}.txt"
+    if not p.exists():
+        return None
+    kv = {}
+    for line in p.read_text().splitlines():
+        if "=" in line and not line.startswith("#"):
+            k, v = line.split("=", 1)
+            kv[k.strip()] = v.strip()
+    if kv.get("source_hash") != kernel_source_hash(sources):
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch_full"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+
+    def summary(self, t0, t1):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ts, line in self.lines:
+            if not (t0 <= ts <= t1):
+                continue
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def timed_steps(step, K, warmup, flush, stream):
+    """W warm-up steps, then K steps each preceded by an L2 flush; device ms per step (events on `stream`)."""
+    for _ in range(warmup):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for i in range(K):
+        flush()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+# ----------------------------------------------------------------------------- workloads
+
+def decode_bytes(kv_lens, Hkv, D=64):
+    return int(kv_lens.to(torch.int64).sum()) * Hkv * D * 2 * 2
+
+
+def bench_decode(S, W, name, rank, K, warmup, flush, stream, num_workers=0):
+    gen = getattr(W, name)
+    inp = gen(device="cuda", seed=rank)
+    B, Hq, D = inp.q.shape
+    Hkv = inp.k_pages.shape[1]
+    ws = torch.empty(S.sinkattn_decode_workspace_size(inp.q, inp.k_pages, inp.page_table, num_workers),
+                     dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(inp.q)
+    lse = torch.empty(B, Hq, dtype=torch.float32, device="cuda")
+
+    def step():
+        S.sinkattn_decode(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens, inp.sinks, inp.scale,
+                          out=out, lse=lse, workspace=ws, num_workers=num_workers, stream=stream)
+
+    with torch.cuda.stream(stream):
+        times = timed_steps(step, K, warmup, flush, stream)
+    err = S.sinkattn_get_error(stream)
+    if err:
+        raise RuntimeError(f"device error {S.status_string(err)}")
+    return inp, step, times, decode_bytes(inp.kv_lens, Hkv, D)
+
+
+def bench_prefill(S, W, name, rank, K, warmup, flush, stream):
+    inp = (W.mixed_serving_prefill if name == "mixed_serving" else W.causal_prefill)(device="cuda", seed=rank)
+    out = torch.empty_like(inp.q)
+    lse = torch.empty(inp.q.shape[0], inp.q.shape[1], dtype=torch.float32, device="cuda")
+
+    def step():
+        S.sinkattn_prefill(inp.q, inp.k, inp.v, inp.cu_seqlens, inp.sinks, inp.scale, True,
+                           max_seqlen=inp.max_seqlen, out=out, lse=lse, stream=stream)
+
+    with torch.cuda.stream(stream):
+        times = timed_steps(step, K, warmup, flush, stream)
+    err = S.sinkattn_get_error(stream)
+    if err:
+        raise RuntimeError(f"device error {S.status_string(err)}")
+    flops = 4 * 64 * inp.q.shape[1] * inp.visible_pairs()
+    return inp, step, times, flops
+
+
+def cpu_baseline_decode(inp, budget_s=12.0):
+    """The fp64 oracle on the host cores, on whole requests of the same workload, ~budget_s of CPU work."""
+    import oracle
+
+    q, kp, vp = inp.q.cpu(), inp.k_pages.cpu(), inp.v_pages.cpu()
+    pt, kl, sk = inp.page_table.cpu(), inp.kv_lens.cpu(), inp.sinks.cpu()
+    B, Hq, _ = q.shape
+    Hkv = kp.shape[1]
+    done_bytes, reqs = 0, 0
+    t0 = time.perf_counter()
+    b = 0
+    while time.perf_counter() - t0 < budget_s and reqs < 4 * B:
+        rows = torch.stack([torch.full((Hq,), b % B, dtype=torch.int32), torch.arange(Hq, dtype=torch.int32)], 1)
+        oracle.decode(q, kp, vp, pt, kl, sk, inp.scale, rows=rows.numpy())
+        done_bytes += int(kl[b % B]) * Hkv * 64 * 4
+        reqs += 1
+        b += 1
+    dt = time.perf_counter() - t0
+    return {"value": done_bytes / dt / 1e9, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{reqs} whole requests (all {Hq} heads) of the same workload, fp64, {dt:.1f} s"}
+
+
+def cpu_baseline_prefill(inp, budget_s=8.0):
+    import numpy as np
+
+    import oracle
+
+    q, k, v, cu, sk = inp.q.cpu(), inp.k.cpu(), inp.v.cpu(), inp.cu_seqlens.cpu(), inp.sinks.cpu()
+    T, Hq, _ = q.shape
+    rng = np.random.default_rng(0)
+    cul = cu.tolist()
+    pairs, n = 0, 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < budget_s:
+        t = int(rng.integers(0, T))
+        rows = np.stack([np.full(Hq, t), np.arange(Hq)], 1).astype(np.int32)
+        oracle.prefill(q, k, v, cu, sk, inp.scale, True, rows=rows)
+        s = max(i for i in range(len(cul) - 1) if cul[i] <= t)
+        pairs += (t - cul[s] + 1) * Hq
+        n += 1
+    dt = time.perf_counter() - t0
+    return {"value": 4 * 64 * pairs / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{n} random query rows (all {Hq} heads) of the workload, fp64, {dt:.1f} s"}
+
+
+# ----------------------------------------------------------------------------- arms
+
+def run_reference(args):
+    """Reference arm: the fp64 oracle, as it stands, on the host cores (rank 0 only)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from gqa_attention_learned_head_gb300 import workloads as W
+    import oracle
+
+    inp = W.batched_paged_decode(device="cpu", seed=0)
+    B, Hq, _ = inp.q.shape
+    Hkv = inp.k_pages.shape[1]
+    per_step = 2  # requests per step: a bounded sample (~1 s of CPU each)
+
+    def step(i):
+        bs = [(i * per_step + j) % B for j in range(per_step)]
+        rows = torch.tensor([[b, h] for b in bs for h in range(Hq)], dtype=torch.int32).numpy()
+        oracle.decode(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens, inp.sinks, inp.scale, rows=rows)
+        return sum(int(inp.kv_lens[b]) for b in bs) * Hkv * 64 * 4
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    nbytes = sum(step(args.warmup + i) for i in range(args.steps))
+    dt = time.perf_counter() - t0
+    value = nbytes / dt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD_TEXT["batched_paged_decode"],
+                       "step": f"{per_step} whole requests x {Hq} heads through the fp64 CPU oracle"},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": f"{per_step} requests per step, {args.steps} steps"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    rank, world, local = dist_setup(args)
+    from gqa_attention_learned_head_gb300 import sinkattn as S
+    from gqa_attention_learned_head_gb300 import workloads as W
+
+    hbm_peak, tc_peak, tc_sustained, peak_src = peaks()
+    stream = torch.cuda.Stream()
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    def flush():
+        flush_buf.fill_(rank & 0x7f)
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+
+    K, Wu = args.steps, args.warmup
+    name = args.workload
+    barrier(world)
+    torch.cuda.synchronize()
+    t_load0 = time.time()
+    if name in ("batched_paged_decode", "long_context_decode", "tiny_decode"):
+        workers = 0
+        inp, step, times, nbytes = bench_decode(S, W, name, rank, K, Wu, flush, stream, workers)
+        ms = statistics.mean(times)
+        torch.cuda.synchronize()
+        barrier(world)
+        ms_max = max_over_ranks(ms, world)
+        total_bytes = sum_over_ranks(float(nbytes), world)
+        value = total_bytes / (ms_max * 1e-3) / 1e9
+        unit = "GB/s"
+        achieved = nbytes / (ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "kernel": "decode_split_kernel + merge_pieces_kernel (one sinkattn_decode call)",
+                "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+                "peak_source": f"{peak_src} hbm_gbs",
+                "traffic": profiled_traffic("decode_split_kernel", name, ["decode.cu", "ptx.cuh", "kernels.h"])}
+        launches = 2 * K
+        cfg_extra = {"kv_tokens": int(inp.kv_lens.sum()), "kv_bytes_per_step": nbytes}
+    else:
+        inp, step, times, flops = bench_prefill(S, W, name, rank, K, Wu, flush, stream)
+        total_flops = sum_over_ranks(float(flops), world)
+        ms = statistics.mean(times)
+        torch.cuda.synchronize()
+        barrier(world)
+        ms_max = max_over_ranks(ms, world)
+        value = total_flops / (ms_max * 1e-3) / 1e12
+        unit = "TFLOP/s"
+        achieved = flops / (ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "kernel": "prefill kernel (one sinkattn_prefill call)", "achieved": achieved,
+                "peak": tc_peak, "unit": "TFLOP/s", "frac": achieved / tc_peak, "peak_source": f"{peak_src} bf16_tflops",
+                "traffic": None}
+        launches = K
+        cfg_extra = {"tokens": int(inp.q.shape[0]), "flops_per_step": flops}
+    # keep the GPU under the same load for >= 1.5 s of clock samples (not timed)
+    while time.time() - t_load0 < 1.5:
+        with torch.cuda.stream(stream):
+            for _ in range(50):
+                flush()
+                step()
+        torch.cuda.synchronize()
+    t_load1 = time.time()
+
+    # ---- end to end through the public API: per-step inputs from pinned host memory, result read back
+    if name == "causal_prefill":
+        h_in = [t.cpu().pin_memory() for t in (inp.q, inp.k, inp.v, inp.cu_seqlens)]
+        d_in = [torch.empty_like(t) for t in (inp.q, inp.k, inp.v, inp.cu_seqlens)]
+        h_out = torch.empty(inp.q.shape, dtype=torch.bfloat16).pin_memory()
+        h_lse = torch.empty(inp.q.shape[:2], dtype=torch.float32).pin_memory()
+        d_out = torch.empty_like(inp.q)
+        d_lse = torch.empty(inp.q.shape[:2], dtype=torch.float32, device="cuda")
+
+        def e2e_step():
+            for h, d in zip(h_in, d_in):
+                d.copy_(h, non_blocking=True)
+            S.sinkattn_prefill(d_in[0], d_in[1], d_in[2], d_in[3], inp.sinks, inp.scale, True,
+                               max_seqlen=inp.max_seqlen, out=d_out, lse=d_lse, stream=stream)
+            h_out.copy_(d_out, non_blocking=True)
+            h_lse.copy_(d_lse, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            et = timed_steps(e2e_step, K, Wu, flush, stream)
+        e_ms = max_over_ranks(statistics.mean(et), world)
+        e2e = {"value": total_flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e_ms,
+               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in h_in),
+               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in (h_out, h_lse))}
+    else:
+        h_q = inp.q.cpu().pin_memory()
+        h_pt = inp.page_table.cpu().pin_memory()
+        h_kl = inp.kv_lens.cpu().pin_memory()
+        h_out = torch.empty(inp.q.shape, dtype=torch.bfloat16).pin_memory()
+        h_lse = torch.empty(inp.q.shape[:2], dtype=torch.float32).pin_memory()
+        d_q, d_pt, d_kl = torch.empty_like(inp.q), torch.empty_like(inp.page_table), torch.empty_like(inp.kv_lens)
+        ws = torch.empty(S.sinkattn_decode_workspace_size(inp.q, inp.k_pages, inp.page_table), dtype=torch.uint8,
+                         device="cuda")
+        d_out = torch.empty_like(inp.q)
+        d_lse = torch.empty(inp.q.shape[:2], dtype=torch.float32, device="cuda")
+
+        def e2e_step():
+            d_q.copy_(h_q, non_blocking=True)
+            d_pt.copy_(h_pt, non_blocking=True)
+            d_kl.copy_(h_kl, non_blocking=True)
+            S.sinkattn_decode(d_q, inp.k_pages, inp.v_pages, d_pt, d_kl, inp.sinks, inp.scale, out=d_out, lse=d_lse,
+                              workspace=ws, stream=stream)
+            h_out.copy_(d_out, non_blocking=True)
+            h_lse.copy_(d_lse, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            et = timed_steps(e2e_step, K, Wu, flush, stream)
+        e_ms = max_over_ranks(statistics.mean(et), world)
+        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_pt, h_kl))
+        d2h = sum(t.numel() * t.element_size() for t in (h_out, h_lse))
+        e2e = {"value": total_bytes / (e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e_ms,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "note": "KV pool stays resident in HBM (it is the cache); q, page table and lengths come from "
+                       "pinned host memory every step and the output + lse are read back"}
+
+    # ---- secondary workloads (rank 0 reports its own numbers)
+    secondary = []
+    if not args.no_secondary:
+        Ks = max(3, min(K, 20))
+        try:
+            li, _, lt, lb = bench_decode(S, W, "long_context_decode", rank, Ks, Wu, flush, stream,
+                                         num_workers=4 * 8 * W.LONG_CONTEXT_CHUNKS)
+            lms = statistics.mean(lt)
+            secondary.append({"workload": WORKLOAD_TEXT["long_context_decode"], "value": lb / (lms * 1e-3) / 1e9,
+                              "unit": "GB/s", "ms_per_step": lms, "frac_of_hbm_peak": lb / (lms * 1e-3) / 1e9 / hbm_peak})
+            del li
+            pi, _, pt_, pf = bench_prefill(S, W, "causal_prefill", rank, Ks, Wu, flush, stream)
+            pms = statistics.mean(pt_)
+            secondary.append({"workload": WORKLOAD_TEXT["causal_prefill"], "value": pf / (pms * 1e-3) / 1e12,
+                              "unit": "TFLOP/s", "ms_per_step": pms,
+                              "frac_of_bf16_peak": pf / (pms * 1e-3) / 1e12 / tc_peak})
+            del pi
+            secondary.append(bench_mixed(S, W, rank, Ks, Wu, flush, hbm_peak, tc_peak))
+        except Exception as e:  # report, never hide
+            secondary.append({"error": f"{type(e).__name__}: {e}"})
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_decode(inp) if unit == "GB/s" else cpu_baseline_prefill(inp)
+
+    clocks = None
+    if sampler:
+        sampler.stop()
+        clocks = sampler.summary(t_load0, t_load1)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": K, "warmup": Wu,
+                "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16", "data": "synthetic (seeded, drawn on the device; seed = rank)",
+                "config": {"workload": WORKLOAD_TEXT[name], "l2": "flushed before every timed step (256 MiB write)",
+                           **cfg_extra},
+                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
+                "secondary": secondary}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+def bench_mixed(S, W, rank, K, Wu, flush, hbm_peak, tc_peak):
+    """Prefill and decode halves of the mixed batch on two streams; time vs t* = bytes/BW + flops/peak."""
+    pre = W.mixed_serving_prefill(device="cuda", seed=rank)
+    dec = W.mixed_serving_decode(device="cuda", seed=rank)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    ws = torch.empty(S.sinkattn_decode_workspace_size(dec.q, dec.k_pages, dec.page_table), dtype=torch.uint8,
+                     device="cuda")
+    po, dout = torch.empty_like(pre.q), torch.empty_like(dec.q)
+    main = torch.cuda.current_stream()
+
+    def step():
+        s1.wait_stream(main)
+        s2.wait_stream(main)
+        S.sinkattn_prefill(pre.q, pre.k, pre.v, pre.cu_seqlens, pre.sinks, pre.scale, True,
+                           max_seqlen=pre.max_seqlen, out=po, return_lse=False, stream=s1)
+        S.sinkattn_decode(dec.q, dec.k_pages, dec.v_pages, dec.page_table, dec.kv_lens, dec.sinks, dec.scale,
+                          out=dout, return_lse=False, workspace=ws, stream=s2)
+        main.wait_stream(s1)
+        main.wait_stream(s2)
+
+    times = timed_steps(step, K, Wu, flush, main)
+    if S.sinkattn_get_error(main):
+        raise RuntimeError("device error in mixed batch")
+    ms = statistics.mean(times)
+    nbytes = decode_bytes(dec.kv_lens, 8)
+    flops = 4 * 64 * 64 * pre.visible_pairs()
+    t_star = nbytes / (hbm_peak * 1e9) + flops / (tc_peak * 1e12)
+    return {"workload": WORKLOAD_TEXT["mixed_serving"], "value": ms, "unit": "ms", "higher_is_better": False,
+            "t_star_ms": t_star * 1e3, "frac_of_t_star": t_star * 1e3 / ms, "decode_bytes": nbytes,
+            "prefill_flops": flops}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="batched_paged_decode",
+                    choices=["batched_paged_decode", "long_context_decode", "tiny_decode", "causal_prefill"])
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,253 @@
+// api.cu -- the C ABI of libsinkattn (declared in include/sinkattn.h):
+// host-side validation, TMA descriptor encoding, launch, and the per-device
+// error word that kernels report into instead of trapping.
+#include <sinkattn.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "kernels.h"
+
+namespace sinkattn {
+namespace {
+
+// One word per device (each device holds its own copy of a __device__ variable).
+__device__ unsigned g_error_word = 0;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool ready = false;
+    unsigned* err = nullptr;  // device address of g_error_word
+};
+DeviceState g_dev[kMaxDevices];
+std::mutex g_mu;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+sinkattn_status_t device_state(DeviceState** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SINKATTN_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState& s = g_dev[dev];
+    if (!s.ready) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return SINKATTN_ERR_CUDA;
+        s.err = static_cast<unsigned*>(p);
+        if (!g_encode) {
+            cudaDriverEntryPointQueryResult q;
+            void* fn = nullptr;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                    cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || !fn)
+                return SINKATTN_ERR_CUDA;
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+        }
+        s.ready = true;
+    }
+    *out = &s;
+    return SINKATTN_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// 2-D bf16 tensor map over rows of 64 elements (128 B), box = box_rows x 64, 128-byte swizzle.
+bool encode_rows(CUtensorMap* map, const void* base, unsigned long long rows, unsigned long long row_stride_bytes,
+                 unsigned box_rows) {
+    cuuint64_t dims[2] = {64, rows};
+    cuuint64_t strides[1] = {row_stride_bytes};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t estride[2] = {1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estride,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D bf16 tensor map over [T, H, 64] (token-major), box = box_rows tokens x 1 head x 64.
+bool encode_thd(CUtensorMap* map, const void* base, int T, int H, unsigned box_rows) {
+    cuuint64_t dims[3] = {64, (cuuint64_t)H, (cuuint64_t)T};
+    cuuint64_t strides[2] = {128, (cuuint64_t)H * 128};
+    cuuint32_t box[3] = {64, 1, box_rows};
+    cuuint32_t estride[3] = {1, 1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estride,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+sinkattn_status_t check_decode_dims(const sinkattn_decode_dims_t* d) {
+    if (!d) return SINKATTN_ERR_INVALID_ARG;
+    if (d->batch < 0 || d->batch > 32768 || d->num_q_heads <= 0 || d->num_kv_heads <= 0 || d->num_pages < 0 ||
+        d->max_pages < 1 || d->num_workers < 0 || d->num_workers > (1 << 22))
+        return SINKATTN_ERR_INVALID_ARG;
+    if (d->num_q_heads % d->num_kv_heads) return SINKATTN_ERR_INVALID_ARG;
+    if (d->head_dim != kHeadDim || d->page_size != kPageSize) return SINKATTN_ERR_UNSUPPORTED;
+    if (d->num_q_heads / d->num_kv_heads > 16) return SINKATTN_ERR_UNSUPPORTED;
+    // TMA row coordinates are 32-bit: pages * Hkv * 16 rows must fit; so must the token cap.
+    if ((long long)d->num_pages * d->num_kv_heads * kPageSize >= (1ll << 31)) return SINKATTN_ERR_UNSUPPORTED;
+    if ((long long)d->max_pages * kPageSize >= (1ll << 31)) return SINKATTN_ERR_UNSUPPORTED;
+    return SINKATTN_OK;
+}
+
+}  // namespace
+}  // namespace sinkattn
+
+using namespace sinkattn;
+
+extern "C" {
+
+int32_t sinkattn_version(void) { return 10000; }
+
+const char* sinkattn_status_string(sinkattn_status_t s) {
+    switch (s) {
+        case SINKATTN_OK: return "ok";
+        case SINKATTN_ERR_INVALID_ARG: return "invalid argument";
+        case SINKATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+        case SINKATTN_ERR_WORKSPACE: return "workspace missing or too small";
+        case SINKATTN_ERR_BAD_PAGE: return "page id out of range";
+        case SINKATTN_ERR_TIMEOUT: return "device pipeline wait timed out";
+        case SINKATTN_ERR_CUDA: return "CUDA runtime error";
+        case SINKATTN_ERR_BAD_LENGTH: return "sequence length out of range";
+    }
+    return "unknown status";
+}
+
+size_t sinkattn_decode_workspace_size(const sinkattn_decode_dims_t* dims) {
+    if (check_decode_dims(dims) != SINKATTN_OK) return 0;
+    DecodePlan plan;
+    if (decode_plan(dims->batch, dims->num_q_heads, dims->num_kv_heads, dims->num_workers, &plan) != cudaSuccess)
+        return 0;
+    return plan.ws_bytes;
+}
+
+sinkattn_status_t sinkattn_decode(const void* q, const void* k_pages, const void* v_pages, const int32_t* page_table,
+                                  const int32_t* kv_lens, const float* sinks, float scale, void* out, float* lse,
+                                  const sinkattn_decode_dims_t* dims, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
+    sinkattn_status_t st = check_decode_dims(dims);
+    if (st != SINKATTN_OK) return st;
+    if (dims->batch == 0) return SINKATTN_OK;
+    if (!q || !k_pages || !v_pages || !page_table || !kv_lens || !sinks || !out) return SINKATTN_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(out, 16) ||
+        !aligned(page_table, 4) || !aligned(kv_lens, 4) || !aligned(sinks, 4) || (lse && !aligned(lse, 4)))
+        return SINKATTN_ERR_INVALID_ARG;
+    if (!(scale == scale)) return SINKATTN_ERR_INVALID_ARG;
+    DeviceState* ds = nullptr;
+    if ((st = device_state(&ds)) != SINKATTN_OK) return st;
+    DecodePlan plan;
+    if (decode_plan(dims->batch, dims->num_q_heads, dims->num_kv_heads, dims->num_workers, &plan) != cudaSuccess)
+        return SINKATTN_ERR_CUDA;
+    if (!workspace || workspace_bytes < plan.ws_bytes || !aligned(workspace, 256)) return SINKATTN_ERR_WORKSPACE;
+
+    const int Hkv = dims->num_kv_heads, G = dims->num_q_heads / Hkv;
+    CUtensorMap tk, tv;
+    const unsigned long long rows = (unsigned long long)(dims->num_pages > 0 ? dims->num_pages : 1) * Hkv * kPageSize;
+    if (!encode_rows(&tk, k_pages, rows, 128, kPageSize) || !encode_rows(&tv, v_pages, rows, 128, kPageSize))
+        return SINKATTN_ERR_INVALID_ARG;
+
+    DecodeArgs a;
+    a.q = static_cast<const __nv_bfloat16*>(q);
+    a.page_table = page_table;
+    a.kv_lens = kv_lens;
+    a.sinks = sinks;
+    a.out = static_cast<__nv_bfloat16*>(out);
+    a.lse = lse;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    a.part_o = reinterpret_cast<float*>(ws);
+    a.part_lse = a.part_o + plan.slots * G * kHeadDim;
+    size_t meta_off = (plan.slots * G * kHeadDim * 4 + plan.slots * G * 4 + 255) & ~size_t(255);
+    a.seg_meta = reinterpret_cast<int2*>(ws + meta_off);
+    a.err = ds->err;
+    a.B = dims->batch;
+    a.Hq = dims->num_q_heads;
+    a.Hkv = Hkv;
+    a.G = G;
+    a.num_pages = dims->num_pages;
+    a.max_pages = dims->max_pages;
+    a.workers = plan.workers;
+    a.min_pages_per_worker = 8;
+    a.fixed_workers = dims->num_workers > 0 ? 1 : 0;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    return decode_launch(a, plan, tk, tv, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SINKATTN_OK
+                                                                                            : SINKATTN_ERR_CUDA;
+}
+
+sinkattn_status_t sinkattn_prefill(const void* q, const void* k, const void* v, const int32_t* cu_seqlens,
+                                   const float* sinks, float scale, int32_t causal, void* out, float* lse,
+                                   const sinkattn_prefill_dims_t* dims, void* stream) {
+    if (!dims) return SINKATTN_ERR_INVALID_ARG;
+    const sinkattn_prefill_dims_t& d = *dims;
+    if (d.num_seqs < 0 || d.total_tokens < 0 || d.max_seqlen < 0 || d.num_q_heads <= 0 || d.num_kv_heads <= 0 ||
+        d.num_q_heads % d.num_kv_heads)
+        return SINKATTN_ERR_INVALID_ARG;
+    if (d.head_dim != kHeadDim) return SINKATTN_ERR_UNSUPPORTED;
+    if (d.num_seqs > 16384 || d.max_seqlen > (1 << 20)) return SINKATTN_ERR_UNSUPPORTED;
+    if (d.num_seqs == 0 || d.total_tokens == 0 || d.max_seqlen == 0) return SINKATTN_OK;
+    if (!q || !k || !v || !cu_seqlens || !sinks || !out) return SINKATTN_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(cu_seqlens, 4) ||
+        !aligned(sinks, 4) || (lse && !aligned(lse, 4)))
+        return SINKATTN_ERR_INVALID_ARG;
+    if (!(scale == scale)) return SINKATTN_ERR_INVALID_ARG;
+    sinkattn_status_t st;
+    DeviceState* ds = nullptr;
+    if ((st = device_state(&ds)) != SINKATTN_OK) return st;
+    PrefillArgs a;
+    a.q = static_cast<const __nv_bfloat16*>(q);
+    a.k = static_cast<const __nv_bfloat16*>(k);
+    a.v = static_cast<const __nv_bfloat16*>(v);
+    a.cu_seqlens = cu_seqlens;
+    a.sinks = sinks;
+    a.out = static_cast<__nv_bfloat16*>(out);
+    a.lse = lse;
+    a.err = ds->err;
+    a.N = d.num_seqs;
+    a.T = d.total_tokens;
+    a.max_seqlen = d.max_seqlen;
+    a.Hq = d.num_q_heads;
+    a.Hkv = d.num_kv_heads;
+    a.G = d.num_q_heads / d.num_kv_heads;
+    a.causal = causal ? 1 : 0;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    return prefill_mma_launch(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SINKATTN_OK : SINKATTN_ERR_CUDA;
+}
+
+sinkattn_status_t sinkattn_merge(const float* partial_o, const float* partial_lse, const float* sinks, void* out,
+                                 float* lse, const sinkattn_merge_dims_t* dims, void* stream) {
+    if (!dims) return SINKATTN_ERR_INVALID_ARG;
+    if (dims->num_splits < 0 || dims->num_rows < 0 || dims->num_heads <= 0) return SINKATTN_ERR_INVALID_ARG;
+    if (dims->head_dim != kHeadDim) return SINKATTN_ERR_UNSUPPORTED;
+    if (dims->num_rows == 0) return SINKATTN_OK;
+    if (!out || (dims->num_splits > 0 && (!partial_o || !partial_lse))) return SINKATTN_ERR_INVALID_ARG;
+    if (!aligned(out, 16) || !aligned(partial_o, 8) || !aligned(partial_lse, 4) || (sinks && !aligned(sinks, 4)) ||
+        (lse && !aligned(lse, 4)))
+        return SINKATTN_ERR_INVALID_ARG;
+    MergeArgs a;
+    a.part_o = partial_o;
+    a.part_lse = partial_lse;
+    a.sinks = sinks;
+    a.out = static_cast<__nv_bfloat16*>(out);
+    a.lse = lse;
+    a.S = dims->num_splits;
+    a.R = dims->num_rows;
+    a.H = dims->num_heads;
+    return merge_launch(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SINKATTN_OK : SINKATTN_ERR_CUDA;
+}
+
+sinkattn_status_t sinkattn_get_error(void* stream) {
+    DeviceState* ds = nullptr;
+    sinkattn_status_t st = device_state(&ds);
+    if (st != SINKATTN_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SINKATTN_ERR_CUDA;
+    unsigned word = 0;
+    if (cudaMemcpyFromSymbol(&word, g_error_word, sizeof word) != cudaSuccess) return SINKATTN_ERR_CUDA;
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof zero) != cudaSuccess) return SINKATTN_ERR_CUDA;
+    for (int code = 1; code < 32; ++code)
+        if (word & (1u << code)) return static_cast<sinkattn_status_t>(code);
+    return SINKATTN_OK;
+}
+
+}  // extern "C"

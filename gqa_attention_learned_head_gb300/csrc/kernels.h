@@ -1,0 +1,77 @@
+// kernels.h -- host-side launch interface between the C ABI layer (api.cu)
+// and the kernel translation units.  Internal to libsinkattn.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace sinkattn {
+
+constexpr int kHeadDim = 64;
+constexpr int kPageSize = 16;
+
+// ------------------------------------------------------------------ decode
+struct DecodeArgs {
+    const __nv_bfloat16* q;   // [B, Hq, 64]
+    const int32_t* page_table;  // [B, max_pages]
+    const int32_t* kv_lens;     // [B]
+    const float* sinks;         // [Hq]
+    __nv_bfloat16* out;         // [B, Hq, 64]
+    float* lse;                 // [B, Hq] or null
+    float* part_o;              // [slots, G, 64]
+    float* part_lse;            // [slots, G]
+    int2* seg_meta;             // [B*Hkv]: (first slot, number of pieces)
+    unsigned* err;              // device error word
+    int B, Hq, Hkv, G, num_pages, max_pages;
+    int workers;                // number of worker warps sharing the work
+    int min_pages_per_worker;   // automatic mode: never cut shares finer than this
+    int fixed_workers;          // 1: `workers` shares exactly (capped at the page count)
+    float scale_log2;           // scale * log2(e)
+};
+
+struct DecodePlan {
+    int grid;            // CTAs of the split kernel
+    int workers;         // worker warps
+    size_t smem;         // dynamic shared memory of the split kernel
+    size_t slots;        // partial-result slots the workspace must hold
+    size_t ws_bytes;     // workspace bytes
+};
+
+// Plan the decode launch for the current device (no device memory touched).
+cudaError_t decode_plan(int B, int Hq, int Hkv, int num_workers, DecodePlan* plan);
+cudaError_t decode_launch(const DecodeArgs& args, const DecodePlan& plan, const CUtensorMap& tmap_k,
+                          const CUtensorMap& tmap_v, cudaStream_t stream);
+
+// ------------------------------------------------------------------ merge
+struct MergeArgs {
+    const float* part_o;    // [S, R, H, 64]
+    const float* part_lse;  // [S, R, H]
+    const float* sinks;     // [H] or null
+    __nv_bfloat16* out;     // [R, H, 64]
+    float* lse;             // [R, H] or null
+    int S, R, H;
+};
+cudaError_t merge_launch(const MergeArgs& args, cudaStream_t stream);
+
+// ------------------------------------------------------------------ prefill
+struct PrefillArgs {
+    const __nv_bfloat16* q;  // [T, Hq, 64]
+    const __nv_bfloat16* k;  // [T, Hkv, 64]
+    const __nv_bfloat16* v;  // [T, Hkv, 64]
+    const int32_t* cu_seqlens;  // [N+1]
+    const float* sinks;         // [Hq]
+    __nv_bfloat16* out;         // [T, Hq, 64]
+    float* lse;                 // [T, Hq] or null
+    unsigned* err;
+    int N, T, max_seqlen, Hq, Hkv, G, causal;
+    float scale_log2;
+};
+// Tensor-core (tcgen05) prefill; the tensor maps are built by the caller.
+cudaError_t prefill_tc_launch(const PrefillArgs& args, const CUtensorMap& tmap_q, const CUtensorMap& tmap_k,
+                              const CUtensorMap& tmap_v, cudaStream_t stream);
+// Warp-level mma.sync prefill, kept as the legacy-tensor-path baseline.
+cudaError_t prefill_mma_launch(const PrefillArgs& args, cudaStream_t stream);
+
+}  // namespace sinkattn

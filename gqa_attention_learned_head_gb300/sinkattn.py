@@ -1,0 +1,195 @@
+"""Python binding of libsinkattn: argument marshalling only.
+
+Each function takes torch tensors already on the GPU, checks dtypes and
+shapes, allocates missing outputs with ``torch.empty`` and calls the C ABI
+(``include/sinkattn.h``) with raw device pointers and the current CUDA stream.
+Every arithmetic step runs in the library's kernels; there is no fallback:
+if ``libsinkattn.so`` is absent, importing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+
+import torch
+
+_LIB_PATH = Path(__file__).resolve().parent / "_build" / "libsinkattn.so"
+
+OK = 0
+ERR_INVALID_ARG = 1
+ERR_UNSUPPORTED = 2
+ERR_WORKSPACE = 3
+ERR_BAD_PAGE = 4
+ERR_TIMEOUT = 5
+ERR_CUDA = 6
+ERR_BAD_LENGTH = 7
+
+
+class SinkAttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+class DecodeDims(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("batch", "num_q_heads", "num_kv_heads", "head_dim", "page_size",
+                                              "num_pages", "max_pages", "num_workers")]
+
+
+class PrefillDims(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("num_seqs", "total_tokens", "max_seqlen", "num_q_heads",
+                                              "num_kv_heads", "head_dim")]
+
+
+class MergeDims(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("num_splits", "num_rows", "num_heads", "head_dim")]
+
+
+EXPORTS = ("sinkattn_decode", "sinkattn_prefill", "sinkattn_merge", "sinkattn_decode_workspace_size",
+           "sinkattn_get_error", "sinkattn_status_string", "sinkattn_version")
+
+
+def _load():
+    if not _LIB_PATH.exists():
+        raise ImportError(f"libsinkattn is not built ({_LIB_PATH} missing); run "
+                          "`python -m gqa_attention_learned_head_gb300.build` (needs nvcc)")
+    lib = ctypes.CDLL(str(_LIB_PATH))
+    P, i32, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+    lib.sinkattn_decode.argtypes = [P, P, P, P, P, P, f32, P, P, ctypes.POINTER(DecodeDims), P, sz, P]
+    lib.sinkattn_prefill.argtypes = [P, P, P, P, P, f32, i32, P, P, ctypes.POINTER(PrefillDims), P]
+    lib.sinkattn_merge.argtypes = [P, P, P, P, P, ctypes.POINTER(MergeDims), P]
+    lib.sinkattn_decode_workspace_size.argtypes = [ctypes.POINTER(DecodeDims)]
+    lib.sinkattn_decode_workspace_size.restype = sz
+    lib.sinkattn_get_error.argtypes = [P]
+    lib.sinkattn_status_string.argtypes = [ctypes.c_int]
+    lib.sinkattn_status_string.restype = ctypes.c_char_p
+    lib.sinkattn_version.restype = i32
+    for fn in ("sinkattn_decode", "sinkattn_prefill", "sinkattn_merge", "sinkattn_get_error"):
+        getattr(lib, fn).restype = ctypes.c_int
+    return lib
+
+
+_lib = _load()
+library_path = str(_LIB_PATH)
+
+
+def status_string(status: int) -> str:
+    return _lib.sinkattn_status_string(int(status)).decode()
+
+
+def version() -> int:
+    return int(_lib.sinkattn_version())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t, name, dtype, ndim):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {ndim}-d tensor, got shape {tuple(t.shape)}")
+
+
+def _check(status, what):
+    if status != OK:
+        raise SinkAttnError(status, what)
+
+
+def decode_dims(q, k_pages, page_table, num_workers=0) -> DecodeDims:
+    B, Hq, D = q.shape
+    P, Hkv, PS, _ = k_pages.shape
+    return DecodeDims(B, Hq, Hkv, D, PS, P, page_table.shape[1], num_workers)
+
+
+def sinkattn_decode_workspace_size(q, k_pages, page_table, num_workers=0) -> int:
+    return int(_lib.sinkattn_decode_workspace_size(ctypes.byref(decode_dims(q, k_pages, page_table, num_workers))))
+
+
+def sinkattn_decode(q, k_pages, v_pages, page_table, kv_lens, sinks, scale, out=None, lse=None, workspace=None,
+                    num_workers=0, return_lse=True, stream=None):
+    """Paged split-KV decode.  Shapes: see ``include/sinkattn.h``.  Returns (out, lse)."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_pages, "k_pages", torch.bfloat16, 4)
+    _need(v_pages, "v_pages", torch.bfloat16, 4)
+    _need(page_table, "page_table", torch.int32, 2)
+    _need(kv_lens, "kv_lens", torch.int32, 1)
+    _need(sinks, "sinks", torch.float32, 1)
+    if v_pages.shape != k_pages.shape:
+        raise ValueError("k_pages and v_pages must have the same shape")
+    B, Hq, D = q.shape
+    if page_table.shape[0] != B or kv_lens.shape[0] != B or sinks.shape[0] != Hq or k_pages.shape[1] == 0:
+        raise ValueError("inconsistent decode shapes")
+    dims = decode_dims(q, k_pages, page_table, num_workers)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty(B, Hq, device=q.device, dtype=torch.float32)
+    if workspace is None:
+        nbytes = int(_lib.sinkattn_decode_workspace_size(ctypes.byref(dims)))
+        if nbytes == 0:
+            raise SinkAttnError(ERR_INVALID_ARG, "sinkattn_decode_workspace_size")
+        workspace = torch.empty(nbytes, device=q.device, dtype=torch.uint8)
+    st = _lib.sinkattn_decode(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table), _ptr(kv_lens), _ptr(sinks),
+                              float(scale), _ptr(out), _ptr(lse), ctypes.byref(dims), _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "sinkattn_decode")
+    return out, lse
+
+
+def sinkattn_prefill(q, k, v, cu_seqlens, sinks, scale, causal=True, max_seqlen=None, out=None, lse=None,
+                     return_lse=True, stream=None):
+    """Packed varlen prefill.  ``max_seqlen`` (an upper bound of the lengths) is required."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k, "k", torch.bfloat16, 3)
+    _need(v, "v", torch.bfloat16, 3)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    _need(sinks, "sinks", torch.float32, 1)
+    if max_seqlen is None:
+        raise ValueError("max_seqlen is required (an upper bound of the sequence lengths)")
+    T, Hq, D = q.shape
+    if k.shape != v.shape or k.shape[0] != T or sinks.shape[0] != Hq:
+        raise ValueError("inconsistent prefill shapes")
+    dims = PrefillDims(cu_seqlens.shape[0] - 1, T, int(max_seqlen), Hq, k.shape[1], D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty(T, Hq, device=q.device, dtype=torch.float32)
+    st = _lib.sinkattn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), _ptr(sinks), float(scale),
+                               int(bool(causal)), _ptr(out), _ptr(lse), ctypes.byref(dims), _stream(stream))
+    _check(st, "sinkattn_prefill")
+    return out, lse
+
+
+def sinkattn_merge(partial_o, partial_lse, sinks=None, out=None, lse=None, return_lse=True, stream=None):
+    """LSE merge of partials [S,R,H,64] / [S,R,H]; ``sinks`` adds the sink once."""
+    _need(partial_o, "partial_o", torch.float32, 4)
+    _need(partial_lse, "partial_lse", torch.float32, 3)
+    if sinks is not None:
+        _need(sinks, "sinks", torch.float32, 1)
+    S, R, H, D = partial_o.shape
+    if partial_lse.shape != (S, R, H):
+        raise ValueError("partial_lse must be [S, R, H]")
+    dims = MergeDims(S, R, H, D)
+    if out is None:
+        out = torch.empty(R, H, D, device=partial_o.device, dtype=torch.bfloat16)
+    if lse is None and return_lse:
+        lse = torch.empty(R, H, device=partial_o.device, dtype=torch.float32)
+    st = _lib.sinkattn_merge(_ptr(partial_o), _ptr(partial_lse), _ptr(sinks), _ptr(out), _ptr(lse),
+                             ctypes.byref(dims), _stream(stream))
+    _check(st, "sinkattn_merge")
+    return out, lse
+
+
+def sinkattn_get_error(stream=None) -> int:
+    """Synchronises the stream; returns and clears the device error word (0 = no problem)."""
+    return int(_lib.sinkattn_get_error(_stream(stream)))

@@ -178,14 +178,22 @@ def causal_prefill(device="cpu", seed=0):
     return make_prefill(64, 8, [8192, 8192], seed=seed, device=device)
 
 
+def mixed_serving_prefill(device="cpu", seed=0):
+    """The prefill half of the mixed serving batch: 8 causal sequences, lengths in [256, 4096]."""
+    return make_prefill(64, 8, (8, 256, 4096), seed=seed, device=device)
+
+
+def mixed_serving_decode(device="cpu", seed=0):
+    """The decode half of the mixed serving batch: 256 paged requests, kv_len in [1024, 32768]."""
+    return make_decode(256, 64, 8, (1024, 32768), seed=seed + 1, device=device)
+
+
 def mixed_serving(device="cpu", seed=0):
     """8 causal prefills with lengths in [256, 4096] plus 256 paged decodes with kv_len in [1024, 32768].
 
     The prefill part is drawn from ``seed`` and the decode part from ``seed + 1``.
     """
-    pre = make_prefill(64, 8, (8, 256, 4096), seed=seed, device=device)
-    dec = make_decode(256, 64, 8, (1024, 32768), seed=seed + 1, device=device)
-    return pre, dec
+    return mixed_serving_prefill(device, seed), mixed_serving_decode(device, seed)
 
 
 WORKLOADS = {

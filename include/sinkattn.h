@@ -1,0 +1,189 @@
+/*
+ * sinkattn.h -- C ABI of libsinkattn: grouped-query attention with a
+ * per-head learned sink logit, for one NVIDIA GB300 (sm_103a).
+ *
+ * The method (source: "GPT-OSS on day 0", Perplexity blog, sections
+ * "Attention: GQA with attention sinks" and "Kernels for GPT-OSS / Sink
+ * Attention"):  every query head h owns a learned logit sink[h] that joins
+ * the softmax normaliser beside the scaled scores s_j = scale * <q, k_j> and
+ * has no value row.  For one query row with visible keys J:
+ *     M   = max(sink[h], max_j s_j)
+ *     Z   = exp(sink[h] - M) + sum_j exp(s_j - M)
+ *     out = sum_j exp(s_j - M) / Z * v_j,      lse = M + ln Z.
+ * sink[h] is compared with the scaled scores as it is (it is not multiplied
+ * by `scale`).  Query head h reads key/value head h / (Hq / Hkv).
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller, dense and
+ *     row-major in the layout stated beside each argument.  bf16 tensors and
+ *     `out` must be 16-byte aligned; int32/f32 tensors 4-byte aligned.
+ *   - The library allocates no device memory, frees nothing and never
+ *     synchronises on the call path: the work is enqueued on `stream` (a
+ *     cudaStream_t passed as void*; NULL = the legacy default stream) on the
+ *     CUDA device that is current for the calling thread.
+ *   - The return value reports host-side validation and launch errors only.
+ *     Problems found on the device (an out-of-range page id or length, a
+ *     pipeline wait that ran out) are recorded in a per-device error word
+ *     that sinkattn_get_error() reads; the kernels never trap.
+ *   - head_dim must be 64 and the KV page size 16; anything else returns
+ *     SINKATTN_ERR_UNSUPPORTED.
+ */
+#ifndef SINKATTN_H_
+#define SINKATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SINKATTN_OK = 0,
+    SINKATTN_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned pointer */
+    SINKATTN_ERR_UNSUPPORTED = 2,  /* head_dim != 64, page size != 16, group size > 16, ... */
+    SINKATTN_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required */
+    SINKATTN_ERR_BAD_PAGE = 4,     /* device: a page id outside [0, num_pages) was met */
+    SINKATTN_ERR_TIMEOUT = 5,      /* device: a pipeline wait gave up; results are invalid */
+    SINKATTN_ERR_CUDA = 6,         /* a CUDA runtime call failed */
+    SINKATTN_ERR_BAD_LENGTH = 7    /* device: a kv_len outside [0, max_pages*16] was met */
+} sinkattn_status_t;
+
+/* Sizes of a paged decode call. */
+typedef struct {
+    int32_t batch;             /* B >= 0 requests, one query token each (B <= 32768)    */
+    int32_t num_q_heads;       /* Hq                                                     */
+    int32_t num_kv_heads;      /* Hkv; Hq % Hkv == 0 and Hq / Hkv <= 16                  */
+    int32_t head_dim;          /* must be 64                                             */
+    int32_t page_size;         /* must be 16                                             */
+    int32_t num_pages;         /* P, pages in the K/V pools                              */
+    int32_t max_pages;         /* row length of page_table (>= 1)                        */
+    int32_t num_workers;       /* 0 = automatic; otherwise the number of equal shares the
+                                  flattened (request, KV head, page) work is cut into.  A
+                                  request whose pages span several shares is split and
+                                  merged; the result does not depend on this value.     */
+} sinkattn_decode_dims_t;
+
+/* Sizes of a packed variable-length prefill call. */
+typedef struct {
+    int32_t num_seqs;          /* N >= 0 sequences                                       */
+    int32_t total_tokens;      /* T = cu_seqlens[N]                                      */
+    int32_t max_seqlen;        /* an upper bound of every sequence length                */
+    int32_t num_q_heads;       /* Hq                                                     */
+    int32_t num_kv_heads;      /* Hkv; Hq % Hkv == 0                                     */
+    int32_t head_dim;          /* must be 64                                             */
+} sinkattn_prefill_dims_t;
+
+/* Sizes of a merge call. */
+typedef struct {
+    int32_t num_splits;        /* S partial results per row (>= 0)                       */
+    int32_t num_rows;          /* R                                                      */
+    int32_t num_heads;         /* H                                                      */
+    int32_t head_dim;          /* must be 64                                             */
+} sinkattn_merge_dims_t;
+
+/*
+ * Bytes of device workspace sinkattn_decode needs for `dims` on the current
+ * device.  0 on invalid dims.  The workspace holds the split-KV partial
+ * results and a small per-(request, KV head) table; it needs no
+ * initialisation and its contents are dead after the call completes.
+ */
+size_t sinkattn_decode_workspace_size(const sinkattn_decode_dims_t *dims);
+
+/*
+ * Paged decode with split-KV and a merge that counts the sink once.
+ * Source: "GPT-OSS on day 0", section "Kernels for GPT-OSS / Sink Attention"
+ * (parallelism over heads and along the KV length; online softmax whose
+ * running max is seeded from the head's sink in the first block only), and
+ * "Accelerating Sonar through speculation", section "Inference with
+ * speculative decoding" (KV pages allocated per request; page metadata copied
+ * to the GPU before the attention kernel).
+ *
+ *   q          [B, Hq, 64]        bf16   one query token per request
+ *   k_pages    [P, Hkv, 16, 64]   bf16   page p, KV head g, slot t: key of one token
+ *   v_pages    [P, Hkv, 16, 64]   bf16   same layout for values
+ *   page_table [B, max_pages]     int32  token t of request b lives in page
+ *                                        page_table[b][t/16], slot t%16; entries past
+ *                                        the request's last page are never read
+ *   kv_lens    [B]                int32  cached tokens per request, 0..max_pages*16
+ *   sinks      [Hq]               f32    learned sink logit of each query head
+ *   scale      softmax scale applied to q.k (usually 1/sqrt(64))
+ *   out        [B, Hq, 64]        bf16   attention output
+ *   lse        [B, Hq]            f32    natural-log log-sum-exp including the sink,
+ *                                        or NULL
+ *   workspace  device scratch of at least sinkattn_decode_workspace_size(dims) bytes,
+ *              256-byte aligned; it must not be shared by calls that may overlap.
+ *
+ * A request with kv_len 0 gives out = 0 and lse = sink[h].  Page ids outside
+ * [0, P) are skipped (their tokens count as absent) and raise
+ * SINKATTN_ERR_BAD_PAGE in the error word; kv_len outside [0, max_pages*16] is
+ * clamped and raises SINKATTN_ERR_BAD_LENGTH.
+ */
+sinkattn_status_t sinkattn_decode(const void *q, const void *k_pages, const void *v_pages,
+                                  const int32_t *page_table, const int32_t *kv_lens,
+                                  const float *sinks, float scale, void *out, float *lse,
+                                  const sinkattn_decode_dims_t *dims, void *workspace,
+                                  size_t workspace_bytes, void *stream);
+
+/*
+ * Causal (or full) prefill over packed variable-length sequences.
+ * Source: "GPT-OSS on day 0", section "Kernels for GPT-OSS / Sink Attention"
+ * (the same sink-aware kernel template serves prefill and decode).
+ *
+ *   q          [T, Hq, 64]   bf16   query rows of all sequences, packed
+ *   k, v       [T, Hkv, 64]  bf16   keys / values, packed the same way
+ *   cu_seqlens [N+1]         int32  sequence n is rows cu_seqlens[n] .. cu_seqlens[n+1]-1;
+ *                                   cu_seqlens[0] = 0, non-decreasing, cu_seqlens[N] = T
+ *   sinks      [Hq]          f32
+ *   causal     1: row i of a sequence sees keys 0..i of that sequence;
+ *              0: it sees the whole sequence
+ *   out        [T, Hq, 64]   bf16
+ *   lse        [T, Hq]       f32    natural log, or NULL
+ *
+ * A sequence longer than dims->max_seqlen is computed only up to
+ * max_seqlen rows; its remaining rows are left untouched and
+ * SINKATTN_ERR_BAD_LENGTH is raised in the error word.
+ */
+sinkattn_status_t sinkattn_prefill(const void *q, const void *k, const void *v,
+                                   const int32_t *cu_seqlens, const float *sinks, float scale,
+                                   int32_t causal, void *out, float *lse,
+                                   const sinkattn_prefill_dims_t *dims, void *stream);
+
+/*
+ * Log-sum-exp merge of split partial results.
+ * Source: "GPT-OSS on day 0", section "Kernels for GPT-OSS / Sink Attention"
+ * (when attention is split into blocks along the sequence, the sink belongs to
+ * one block only).
+ *
+ *   partial_o   [S, R, H, 64] f32   o_c = normalised output of split c
+ *   partial_lse [S, R, H]     f32   natural-log lse_c of split c; -inf marks an
+ *                                   empty split (its o_c is ignored)
+ *   sinks       [H] f32, or NULL.  NULL: the sink is already inside one split.
+ *               Given: the splits hold no sink and the merge adds exp(sink[h])
+ *               exactly once.
+ *   out         [R, H, 64]    bf16  sum_c exp(lse_c - L) o_c
+ *   lse         [R, H]        f32   L = log(sum_c exp(lse_c) [+ exp(sink[h])]), or NULL
+ * A row with no live split and no sink gives out = 0 and lse = -inf.
+ */
+sinkattn_status_t sinkattn_merge(const float *partial_o, const float *partial_lse,
+                                 const float *sinks, void *out, float *lse,
+                                 const sinkattn_merge_dims_t *dims, void *stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the current device's error
+ * word (SINKATTN_OK when no kernel reported a problem).  If several problems
+ * were recorded, the one with the lowest status code is returned.
+ */
+sinkattn_status_t sinkattn_get_error(void *stream);
+
+/* Static English text for a status code. */
+const char *sinkattn_status_string(sinkattn_status_t status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t sinkattn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SINKATTN_H_ */

@@ -1,0 +1,71 @@
+"""libsinkattn loads, exports every entry point its header declares, and
+rejects bad arguments on the host before touching a device (no GPU needed)."""
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+ROOT = Path(__file__).resolve().parents[1]
+
+
+@pytest.fixture(scope="module")
+def S():
+    from gqa_attention_learned_head_gb300 import build
+
+    build.build()
+    from gqa_attention_learned_head_gb300 import sinkattn
+
+    return sinkattn
+
+
+def declared_functions():
+    text = (ROOT / "include" / "sinkattn.h").read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sinkattn_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_three_calls():
+    names = declared_functions()
+    for fn in ("sinkattn_decode", "sinkattn_prefill", "sinkattn_merge"):
+        assert fn in names
+
+
+def test_library_exports_every_declared_symbol(S):
+    lib = ctypes.CDLL(S.library_path)
+    for fn in declared_functions():
+        assert hasattr(lib, fn), f"{fn} not exported"
+    assert set(S.EXPORTS) <= set(declared_functions())
+
+
+def test_status_strings(S):
+    assert S.status_string(0) == "ok"
+    assert "page" in S.status_string(S.ERR_BAD_PAGE)
+    assert S.status_string(99) == "unknown status"
+    assert S.version() >= 10000
+
+
+def test_host_validation_without_device(S):
+    lib = S._lib
+    d = S.DecodeDims(2, 8, 2, 32, 16, 10, 4, 0)  # head_dim 32
+    st = lib.sinkattn_decode(None, None, None, None, None, None, 0.125, None, None, ctypes.byref(d), None, 0, None)
+    assert st == S.ERR_UNSUPPORTED
+    d = S.DecodeDims(2, 8, 3, 64, 16, 10, 4, 0)  # Hq % Hkv != 0
+    assert lib.sinkattn_decode(None, None, None, None, None, None, 0.125, None, None, ctypes.byref(d), None, 0,
+                               None) == S.ERR_INVALID_ARG
+    d = S.DecodeDims(2, 64, 2, 64, 16, 10, 4, 0)  # group of 32 heads
+    assert lib.sinkattn_decode(None, None, None, None, None, None, 0.125, None, None, ctypes.byref(d), None, 0,
+                               None) == S.ERR_UNSUPPORTED
+    d = S.DecodeDims(2, 8, 2, 64, 8, 10, 4, 0)  # page size 8
+    assert lib.sinkattn_decode(None, None, None, None, None, None, 0.125, None, None, ctypes.byref(d), None, 0,
+                               None) == S.ERR_UNSUPPORTED
+    assert lib.sinkattn_decode_workspace_size(ctypes.byref(d)) == 0
+    p = S.PrefillDims(1, 10, 10, 8, 2, 128)
+    assert lib.sinkattn_prefill(None, None, None, None, None, 0.1, 1, None, None, ctypes.byref(p), None) == \
+        S.ERR_UNSUPPORTED
+    p = S.PrefillDims(-1, 10, 10, 8, 2, 64)
+    assert lib.sinkattn_prefill(None, None, None, None, None, 0.1, 1, None, None, ctypes.byref(p), None) == \
+        S.ERR_INVALID_ARG
+    m = S.MergeDims(2, 4, 0, 64)
+    assert lib.sinkattn_merge(None, None, None, None, None, ctypes.byref(m), None) == S.ERR_INVALID_ARG
+    assert lib.sinkattn_merge(None, None, None, None, None, None, None) == S.ERR_INVALID_ARG

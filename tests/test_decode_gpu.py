@@ -1,0 +1,143 @@
+"""GPU decode (split-KV + merge) against the fp64 oracle, through the C ABI."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gqa_attention_learned_head_gb300 import workloads as W
+from parity_utils import assert_parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def S():
+    from gqa_attention_learned_head_gb300 import sinkattn
+
+    return sinkattn
+
+
+def run(S, inp, **kw):
+    g = inp.to("cuda")
+    out, lse = S.sinkattn_decode(g.q, g.k_pages, g.v_pages, g.page_table, g.kv_lens, g.sinks, g.scale, **kw)
+    err = S.sinkattn_get_error()
+    return out.float().cpu().numpy(), lse.cpu().numpy(), err
+
+
+def ref(inp, rows=None):
+    return oracle.decode(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens, inp.sinks, inp.scale,
+                         rows=rows)
+
+
+def test_tiny_decode(S):
+    inp = W.tiny_decode()
+    out, lse, err = run(S, inp)
+    assert err == 0
+    assert_parity(out, lse, *ref(inp), "tiny decode")
+
+
+def test_batched_paged_decode(S):
+    inp = W.batched_paged_decode()
+    out, lse, err = run(S, inp)
+    assert err == 0
+    assert_parity(out, lse, *ref(inp), "batched paged decode")
+
+
+@pytest.mark.parametrize("workers", [0, 4 * 8 * 32])
+def test_long_context_sampled(S, workers):
+    """Full-size long-context workload; 64 sampled (b, h) rows checked against the oracle.
+
+    workers = B * Hkv * 32 cuts every request into exactly 32 chunks of 4096 tokens."""
+    inp = W.long_context_decode()
+    out, lse, err = run(S, inp, num_workers=workers)
+    assert err == 0
+    rng = np.random.default_rng(0)
+    rows = np.stack([rng.integers(0, 4, 64), rng.integers(0, 64, 64)], 1).astype(np.int32)
+    ro, rl = ref(inp, rows)
+    assert_parity(out[rows[:, 0], rows[:, 1]], lse[rows[:, 0], rows[:, 1]], ro, rl, "long context")
+    assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
+
+
+@pytest.mark.parametrize("lens", [[0, 1, 15, 16, 17], [255, 256, 257, 4097], [0, 0, 0], [33]])
+@pytest.mark.parametrize("Hq,Hkv", [(4, 1), (64, 8), (16, 1), (6, 2)])
+def test_lengths_and_groups(S, lens, Hq, Hkv):
+    inp = W.make_decode(len(lens), Hq, Hkv, lens, seed=sum(lens) + Hq)
+    out, lse, err = run(S, inp)
+    assert err == 0
+    assert_parity(out, lse, *ref(inp), f"lens={lens} Hq={Hq} Hkv={Hkv}")
+
+
+@pytest.mark.parametrize("sink", [float("-inf"), -30.0, 0.0, 30.0])
+def test_sink_values(S, sink):
+    inp = W.make_decode(3, 16, 2, [0, 40, 700], seed=3)
+    inp.sinks[:] = sink
+    out, lse, err = run(S, inp)
+    assert err == 0
+    assert_parity(out, lse, *ref(inp), f"sink={sink}")
+
+
+@pytest.mark.parametrize("workers", [1, 2, 3, 7, 64, 1000, 5000])
+def test_split_count_does_not_change_result(S, workers):
+    inp = W.make_decode(5, 32, 4, [1, 100, 1000, 3000, 17], seed=4)
+    out, lse, err = run(S, inp, num_workers=workers)
+    assert err == 0
+    assert_parity(out, lse, *ref(inp), f"workers={workers}")
+
+
+def test_partial_last_page_garbage_is_ignored(S):
+    inp = W.make_decode(2, 8, 1, [17, 30], seed=5)
+    # slots past kv_len in each last page: fill with NaN and huge values
+    for b, L in enumerate([17, 30]):
+        last = int(inp.page_table[b, (L - 1) // 16])
+        inp.k_pages[last, :, L % 16:] = float("nan")
+        inp.v_pages[last, :, L % 16:] = float("inf")
+    out, lse, err = run(S, inp)
+    assert err == 0
+    assert_parity(out, lse, *ref(inp), "garbage tail")
+
+
+def test_bad_page_is_reported_and_skipped(S):
+    inp = W.make_decode(2, 8, 2, [40, 40], seed=6)
+    good = ref(inp)
+    inp.page_table[1, 1] = inp.k_pages.shape[0] + 5  # request 1 points outside the pool
+    out, lse, err = run(S, inp)
+    assert err == S.ERR_BAD_PAGE
+    assert_parity(out[0], lse[0], good[0][0], good[1][0], "untouched request")
+    assert np.all(np.isfinite(out[1]))
+
+
+def test_bad_length_is_reported(S):
+    inp = W.make_decode(2, 8, 2, [40, 20], seed=7)
+    g = inp.to("cuda")
+    g.kv_lens[1] = 10_000  # beyond max_pages * 16
+    S.sinkattn_decode(g.q, g.k_pages, g.v_pages, g.page_table, g.kv_lens, g.sinks, g.scale)
+    assert S.sinkattn_get_error() == S.ERR_BAD_LENGTH
+    assert S.sinkattn_get_error() == 0  # cleared by the read
+
+
+def test_workspace_too_small(S):
+    inp = W.make_decode(2, 8, 2, [40, 20], seed=8).to("cuda")
+    ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(S.SinkAttnError) as e:
+        S.sinkattn_decode(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens, inp.sinks, inp.scale,
+                          workspace=ws)
+    assert e.value.status == S.ERR_WORKSPACE
+
+
+def test_lse_optional_and_repeatable(S):
+    inp = W.make_decode(4, 64, 8, (100, 2000), seed=9).to("cuda")
+    o1, _ = S.sinkattn_decode(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens, inp.sinks, inp.scale,
+                              return_lse=False)
+    o2, _ = S.sinkattn_decode(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens, inp.sinks, inp.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2)  # deterministic
+
+
+def test_empty_batch(S):
+    inp = W.make_decode(1, 8, 2, [5], seed=10).to("cuda")
+    q = inp.q[:0]
+    out, lse = S.sinkattn_decode(q, inp.k_pages, inp.v_pages, inp.page_table[:0], inp.kv_lens[:0], inp.sinks,
+                                 inp.scale)
+    assert out.shape == (0, 8, 64) and S.sinkattn_get_error() == 0

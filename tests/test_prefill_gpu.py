@@ -1,0 +1,93 @@
+"""GPU causal varlen prefill against the fp64 oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gqa_attention_learned_head_gb300 import workloads as W
+from parity_utils import assert_parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def S():
+    from gqa_attention_learned_head_gb300 import sinkattn
+
+    return sinkattn
+
+
+def run(S, inp, max_seqlen=None):
+    g = inp.to("cuda")
+    out, lse = S.sinkattn_prefill(g.q, g.k, g.v, g.cu_seqlens, g.sinks, g.scale, g.causal,
+                                  max_seqlen=inp.max_seqlen if max_seqlen is None else max_seqlen)
+    err = S.sinkattn_get_error()
+    return out.float().cpu().numpy(), lse.cpu().numpy(), err
+
+
+def ref(inp, rows=None):
+    return oracle.prefill(inp.q, inp.k, inp.v, inp.cu_seqlens, inp.sinks, inp.scale, inp.causal, rows=rows)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("lens", [[1], [127, 128, 129], [300, 5, 64, 1000]])
+@pytest.mark.parametrize("Hq,Hkv", [(8, 2), (16, 2), (4, 4)])
+def test_small_varlen(S, causal, lens, Hq, Hkv):
+    inp = W.make_prefill(Hq, Hkv, lens, seed=len(lens) + Hq, causal=causal)
+    out, lse, err = run(S, inp)
+    assert err == 0
+    assert_parity(out, lse, *ref(inp), f"lens={lens} causal={causal} Hq={Hq} Hkv={Hkv}")
+
+
+@pytest.mark.parametrize("sink", [float("-inf"), -30.0, 30.0])
+def test_sink_values(S, sink):
+    inp = W.make_prefill(8, 1, [200, 77], seed=2)
+    inp.sinks[:] = sink
+    out, lse, err = run(S, inp)
+    assert err == 0
+    assert_parity(out, lse, *ref(inp), f"sink={sink}")
+
+
+def test_empty_sequences_in_batch(S):
+    inp = W.make_prefill(8, 2, [0, 50, 0, 130, 0], seed=3)
+    out, lse, err = run(S, inp)
+    assert err == 0
+    assert_parity(out, lse, *ref(inp), "empty sequences")
+
+
+def sampled_rows(inp, n, seed):
+    rng = np.random.default_rng(seed)
+    cu = inp.cu_seqlens.tolist()
+    T, Hq = inp.q.shape[0], inp.q.shape[1]
+    toks = list(rng.integers(0, T, n))
+    # always include every sequence's first and last row and a tile boundary
+    for s in range(len(cu) - 1):
+        if cu[s + 1] > cu[s]:
+            toks += [cu[s], cu[s + 1] - 1, min(cu[s] + 128, cu[s + 1] - 1)]
+    hs = rng.integers(0, Hq, len(toks))
+    return np.stack([np.array(toks), hs], 1).astype(np.int32)
+
+
+def test_causal_prefill_full_size_sampled(S):
+    inp = W.causal_prefill()
+    out, lse, err = run(S, inp)
+    assert err == 0
+    assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
+    rows = sampled_rows(inp, 96, 0)
+    ro, rl = ref(inp, rows)
+    assert_parity(out[rows[:, 0], rows[:, 1]], lse[rows[:, 0], rows[:, 1]], ro, rl, "causal prefill 2x8192")
+
+
+def test_mixed_serving_prefill_sampled(S):
+    inp = W.mixed_serving_prefill()
+    out, lse, err = run(S, inp)
+    assert err == 0
+    rows = sampled_rows(inp, 96, 1)
+    ro, rl = ref(inp, rows)
+    assert_parity(out[rows[:, 0], rows[:, 1]], lse[rows[:, 0], rows[:, 1]], ro, rl, "mixed prefill")
+
+
+def test_too_long_sequence_is_reported(S):
+    inp = W.make_prefill(4, 1, [100, 40], seed=4)
+    out, lse, err = run(S, inp, max_seqlen=64)
+    assert err == S.ERR_BAD_LENGTH
