@@ -3,6 +3,7 @@
 // error word that kernels report into instead of trapping.
 #include <sinkattn.h>
 
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -53,6 +54,16 @@ sinkattn_status_t device_state(DeviceState** out) {
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// The prefill runs on the tcgen05 kernel.  SINKATTN_PREFILL_KERNEL=mma selects the
+// warp-level mma.sync kernel instead; it exists as the measured baseline only.
+bool prefill_use_legacy_kernel() {
+    static const bool legacy = [] {
+        const char* s = std::getenv("SINKATTN_PREFILL_KERNEL");
+        return s && std::strcmp(s, "mma") == 0;
+    }();
+    return legacy;
+}
 
 // 2-D bf16 tensor map over rows of 64 elements (128 B), box = box_rows x 64, 128-byte swizzle.
 bool encode_rows(CUtensorMap* map, const void* base, unsigned long long rows, unsigned long long row_stride_bytes,
@@ -129,7 +140,8 @@ sinkattn_status_t sinkattn_decode(const void* q, const void* k_pages, const void
     sinkattn_status_t st = check_decode_dims(dims);
     if (st != SINKATTN_OK) return st;
     if (dims->batch == 0) return SINKATTN_OK;
-    if (!q || !k_pages || !v_pages || !page_table || !kv_lens || !sinks || !out) return SINKATTN_ERR_INVALID_ARG;
+    if (!q || !page_table || !kv_lens || !sinks || !out) return SINKATTN_ERR_INVALID_ARG;
+    if (dims->num_pages > 0 && (!k_pages || !v_pages)) return SINKATTN_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(out, 16) ||
         !aligned(page_table, 4) || !aligned(kv_lens, 4) || !aligned(sinks, 4) || (lse && !aligned(lse, 4)))
         return SINKATTN_ERR_INVALID_ARG;
@@ -142,9 +154,14 @@ sinkattn_status_t sinkattn_decode(const void* q, const void* k_pages, const void
     if (!workspace || workspace_bytes < plan.ws_bytes || !aligned(workspace, 256)) return SINKATTN_ERR_WORKSPACE;
 
     const int Hkv = dims->num_kv_heads, G = dims->num_q_heads / Hkv;
+    // With an empty pool every page id is out of range, so no copy is ever issued
+    // and the (zeroed) maps are never read.
     CUtensorMap tk, tv;
-    const unsigned long long rows = (unsigned long long)(dims->num_pages > 0 ? dims->num_pages : 1) * Hkv * kPageSize;
-    if (!encode_rows(&tk, k_pages, rows, 128, kPageSize) || !encode_rows(&tv, v_pages, rows, 128, kPageSize))
+    std::memset(&tk, 0, sizeof tk);
+    std::memset(&tv, 0, sizeof tv);
+    const unsigned long long rows = (unsigned long long)dims->num_pages * Hkv * kPageSize;
+    if (rows > 0 &&
+        (!encode_rows(&tk, k_pages, rows, 128, kPageSize) || !encode_rows(&tv, v_pages, rows, 128, kPageSize)))
         return SINKATTN_ERR_INVALID_ARG;
 
     DecodeArgs a;
@@ -210,7 +227,18 @@ sinkattn_status_t sinkattn_prefill(const void* q, const void* k, const void* v, 
     a.G = d.num_q_heads / d.num_kv_heads;
     a.causal = causal ? 1 : 0;
     a.scale_log2 = scale * 1.4426950408889634f;
-    return prefill_mma_launch(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SINKATTN_OK : SINKATTN_ERR_CUDA;
+    cudaError_t e;
+    if (prefill_use_legacy_kernel()) {
+        e = prefill_mma_launch(a, static_cast<cudaStream_t>(stream));
+    } else {
+        CUtensorMap tq, tk, tv;
+        if (!encode_thd(&tq, q, d.total_tokens, d.num_q_heads, 128) ||
+            !encode_thd(&tk, k, d.total_tokens, d.num_kv_heads, 128) ||
+            !encode_thd(&tv, v, d.total_tokens, d.num_kv_heads, 128))
+            return SINKATTN_ERR_INVALID_ARG;
+        e = prefill_tc_launch(a, tq, tk, tv, static_cast<cudaStream_t>(stream));
+    }
+    return e == cudaSuccess ? SINKATTN_OK : SINKATTN_ERR_CUDA;
 }
 
 sinkattn_status_t sinkattn_merge(const float* partial_o, const float* partial_lse, const float* sinks, void* out,

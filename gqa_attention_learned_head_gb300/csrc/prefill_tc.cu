@@ -1,0 +1,334 @@
+// prefill_tc.cu -- causal varlen prefill with a per-head sink on the fifth-
+// generation tensor cores (tcgen05 MMA, accumulators in tensor memory).
+//
+// Source of the method: "GPT-OSS on day 0" (Perplexity), section "Kernels for
+// GPT-OSS / Sink Attention": the online softmax starts from m = sink, d = 1, so
+// the sink sits in the row normaliser and contributes no value row; the same
+// sink-aware kernel serves prefill.
+//
+// One CTA = one tile of 128 query rows of one head; two CTAs share an SM.
+//   warp 0      TMA producer: Q once, then K_j / V_j tiles (128 keys x 64,
+//               128-byte swizzle) into a 2-stage ring.
+//   warp 1      allocates 256 TMEM columns; one lane issues every MMA:
+//                 S_j  = Q K_j^T   (M=128, N=128, K=64; SMEM x SMEM -> TMEM)
+//                 O   += P_j V_j   (M=128, N=64,  K=128; P read from TMEM)
+//   warps 4-7   softmax: thread r owns query row r (TMEM lane r).  It reads
+//               S_j, releases the S columns at once (so S_{j+1} can start),
+//               masks the diagonal tile, takes exp2 against a running max that
+//               is only moved when it grows by more than 2^8 (rare rescales of
+//               O in TMEM), writes P_j as bf16 into TMEM, and at the end writes
+//               O / d -- d including the sink term -- and the log-sum-exp.
+// TMEM columns: [0,128) S fp32, [128,192) O fp32, [192,256) P bf16 pairs.
+// Every wait is bounded; a wait that gives up sets the device error word.
+#include "kernels.h"
+#include "ptx.cuh"
+#include "tile_order.cuh"
+
+namespace sinkattn {
+namespace {
+
+constexpr int kBM = 128, kBN = 128;
+constexpr int kThreads = 256;
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColS = 0, kColO = 128, kColP = 192;
+constexpr uint32_t kTileBytes = 128 * 128;  // 128 rows x 64 bf16
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kNegInf = -__builtin_huge_valf();
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: O / d may grow by up to 2^8 before a rescale
+
+// Instruction descriptors, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16 (bits 7-9, 10-12 = 1),
+// N >> 3 at bits 17-22, M >> 4 at bits 24-28; bit 16 = B is MN-major.
+constexpr uint32_t kIdescQK = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+constexpr uint32_t kIdescPV =
+    (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((64u >> 3) << 17) | ((128u >> 4) << 24);
+
+// Shared-memory matrix descriptor for a 128-byte-swizzled tile whose 8-row groups are 1024 B apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4)       // start address
+           | ((uint64_t)(1024u >> 4) << 16)          // leading-dimension byte offset (unused by these shapes)
+           | ((uint64_t)(1024u >> 4) << 32)          // stride-dimension byte offset: next 8-row group
+           | (1ull << 46)                            // descriptor version
+           | (2ull << 61);                           // 128-byte swizzle
+}
+
+struct __align__(1024) Smem {
+    uint8_t q[kTileBytes];
+    uint8_t k[2][kTileBytes];
+    uint8_t v[2][kTileBytes];
+    uint64_t q_full, k_full[2], v_full[2], kv_empty[2], s_full, s_free, p_full, o_done, mma_done;
+    uint32_t tmem_base;
+};
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity));
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                      const __grid_constant__ CUtensorMap tmap_v, const PrefillArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    int* order_ints = reinterpret_cast<int*>(&sm + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    TileOrder<kThreads> order;
+    order.build(order_ints, a.cu_seqlens, a.N, a.T, a.max_seqlen, kBM, a.err);
+    const int idx = (int)(blockIdx.x / a.Hq), h = (int)(blockIdx.x % a.Hq);
+    if (idx >= order.total) return;  // whole CTA: no tile left
+    int seq, qt;
+    order.lookup(idx, seq, qt);
+    const int s0 = a.cu_seqlens[seq];
+    const int L = min(a.cu_seqlens[seq + 1] - s0, a.max_seqlen);
+    const int row0 = qt * kBM;
+    const int kvh = h / a.G;
+    const int kend = a.causal ? min(L, row0 + kBM) : L;
+    const int ntile = (kend + kBN - 1) / kBN;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&sm.q_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm.k_full[i], 1);
+            mbar_init(&sm.v_full[i], 1);
+            mbar_init(&sm.kv_empty[i], 1);
+        }
+        mbar_init(&sm.s_full, 1);
+        mbar_init(&sm.s_free, 128);
+        mbar_init(&sm.p_full, 128);
+        mbar_init(&sm.o_done, 1);
+        mbar_init(&sm.mma_done, 1);
+        fence_mbar_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 1) {
+        tmem_alloc(&sm.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = sm.tmem_base;
+
+    if (warp < 4) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 40;");
+        if (warp == 0 && lane == 0) {
+            // ------------------------------------------------------------ TMA producer
+            tma_prefetch_desc(&tmap_q);
+            tma_prefetch_desc(&tmap_k);
+            tma_prefetch_desc(&tmap_v);
+            mbar_arrive_expect_tx(&sm.q_full, kTileBytes);
+            tma_load_3d(sm.q, &tmap_q, 0, h, s0 + row0, &sm.q_full);
+            int issued = 0;
+            for (int j = 0; j < ntile; ++j) {
+                const int st = j & 1;
+                if (j >= 2 && !mbar_wait(&sm.kv_empty[st], ((j >> 1) - 1) & 1)) {
+                    atomicOr(a.err, kErrTimeout);
+                    break;
+                }
+                mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
+                tma_load_3d(sm.k[st], &tmap_k, 0, kvh, s0 + j * kBN, &sm.k_full[st]);
+                mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
+                tma_load_3d(sm.v[st], &tmap_v, 0, kvh, s0 + j * kBN, &sm.v_full[st]);
+                issued = j + 1;
+            }
+            // every copy this thread started has landed before the CTA can exit (bounded)
+            (void)mbar_wait(&sm.q_full, 0);
+            for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j) {
+                (void)mbar_wait(&sm.k_full[j & 1], (j >> 1) & 1);
+                (void)mbar_wait(&sm.v_full[j & 1], (j >> 1) & 1);
+            }
+        } else if (warp == 1 && lane == 0) {
+            // ------------------------------------------------------------ MMA issuer
+            const uint32_t tS = tbase + kColS, tO = tbase + kColO, tP = tbase + kColP;
+            const uint32_t qaddr = smem_u32(sm.q);
+            bool ok = mbar_wait(&sm.q_full, 0) && mbar_wait(&sm.k_full[0], 0);
+            if (ok) {
+                tc_fence_after();
+                const uint32_t kaddr = smem_u32(sm.k[0]);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    tc_mma_ss(tS, sw128_desc(qaddr + kk * 32), sw128_desc(kaddr + kk * 32), kIdescQK, kk > 0);
+                tc_commit(&sm.s_full);
+            }
+            for (int j = 0; ok && j < ntile; ++j) {
+                if (j + 1 < ntile) {
+                    const int st = (j + 1) & 1;
+                    ok = mbar_wait(&sm.k_full[st], ((j + 1) >> 1) & 1) && mbar_wait(&sm.s_free, j & 1);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t kaddr = smem_u32(sm.k[st]);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc_mma_ss(tS, sw128_desc(qaddr + kk * 32), sw128_desc(kaddr + kk * 32), kIdescQK, kk > 0);
+                    tc_commit(&sm.s_full);
+                }
+                ok = mbar_wait(&sm.v_full[j & 1], (j >> 1) & 1) && mbar_wait(&sm.p_full, j & 1);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t vaddr = smem_u32(sm.v[j & 1]);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    tc_mma_ts(tO, tP + ks * 8, sw128_desc(vaddr + ks * 2048), kIdescPV, (j > 0 || ks > 0) ? 1u : 0u);
+                tc_commit(&sm.kv_empty[j & 1]);
+                tc_commit(&sm.o_done);
+            }
+            if (!ok) atomicOr(a.err, kErrTimeout);
+            tc_commit(&sm.mma_done);  // every MMA has finished before TMEM is released
+            (void)mbar_wait(&sm.mma_done, 0);
+        }
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 216;");
+        // ---------------------------------------------------------------- softmax warpgroup
+        const int r = threadIdx.x - 128;
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t tS = tbase + lane_off + kColS, tO = tbase + lane_off + kColO, tP = tbase + lane_off + kColP;
+        const int qrow = row0 + r;
+        const float scale_log2 = a.scale_log2;
+        float m = __ldg(&a.sinks[h]) * kLog2e;  // running max, seeded with the sink
+        float d = 1.f;                          // e^(sink - m) = 1
+        bool ok = true;
+        for (int j = 0; j < ntile; ++j) {
+            if (!(ok = warp_wait(&sm.s_full, j & 1))) break;
+            tc_fence_after();
+            float s[128];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
+            tc_wait_ld();
+            tc_fence_before();
+            mbar_arrive(&sm.s_free);
+
+            const int kb = j * kBN;
+            const bool masked = (kb + kBN > L) || (a.causal && kb + kBN - 1 > row0);
+            float mx = kNegInf;
+            if (masked) {
+                const int lim = a.causal ? min(L, qrow + 1) : L;  // keys [kb, lim) are visible
+#pragma unroll
+                for (int c = 0; c < 128; ++c) {
+                    s[c] = (kb + c < lim) ? s[c] * scale_log2 : kNegInf;
+                    mx = fmaxf(mx, s[c]);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 128; ++c) {
+                    s[c] *= scale_log2;
+                    mx = fmaxf(mx, s[c]);
+                }
+            }
+            const float m_new = fmaxf(m, mx);
+            float factor = 1.f;
+            bool rescale_o = false;
+            if (j == 0 || m_new > m + kRescaleThreshold) {
+                factor = (m_new == kNegInf) ? 1.f : fast_exp2(m - m_new);
+                rescale_o = (j > 0);
+                m = m_new;
+                d *= factor;
+            }
+            const float mref = (m == kNegInf) ? 0.f : m;
+            float sum = 0.f;
+            uint32_t pk[64];
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+                const float p0 = fast_exp2(s[2 * c] - mref), p1 = fast_exp2(s[2 * c + 1] - mref);
+                sum += p0 + p1;
+                pk[c] = pack_bf16(p0, p1);
+            }
+            d += sum;
+            if (j > 0) {  // P_{j-1} consumed and O_{j-1} final before P and O are touched
+                if (!(ok = warp_wait(&sm.o_done, (j - 1) & 1))) break;
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, rescale_o)) {
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + c * 32, o);
+                        tc_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * factor);
+                        tmem_st32(tO + c * 32, o);
+                    }
+                }
+            }
+            tmem_st32(tP, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+            tmem_st32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+            tc_wait_st();
+            tc_fence_before();
+            mbar_arrive(&sm.p_full);
+        }
+        if (ok) ok = warp_wait(&sm.o_done, (ntile - 1) & 1);
+        if (ok) {
+            tc_fence_after();
+            uint32_t o[64];
+            tmem_ld32(tO, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
+            tmem_ld32(tO + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
+            tc_wait_ld();
+            if (qrow < L) {
+                const float inv = d > 0.f ? 1.f / d : 0.f;
+                const long long tok = (long long)s0 + qrow;
+                uint4* dst = reinterpret_cast<uint4*>(a.out + (tok * a.Hq + h) * kHeadDim);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint4 w;
+                    w.x = pack_bf16(__uint_as_float(o[8 * c + 0]) * inv, __uint_as_float(o[8 * c + 1]) * inv);
+                    w.y = pack_bf16(__uint_as_float(o[8 * c + 2]) * inv, __uint_as_float(o[8 * c + 3]) * inv);
+                    w.z = pack_bf16(__uint_as_float(o[8 * c + 4]) * inv, __uint_as_float(o[8 * c + 5]) * inv);
+                    w.w = pack_bf16(__uint_as_float(o[8 * c + 6]) * inv, __uint_as_float(o[8 * c + 7]) * inv);
+                    dst[c] = w;
+                }
+                if (a.lse) a.lse[tok * a.Hq + h] = d > 0.f ? (m + log2f(d)) * kLn2 : kNegInf;
+            }
+        } else if (lane == 0) {
+            atomicOr(a.err, kErrTimeout);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tbase, kTmemCols);
+    }
+}
+
+}  // namespace
+
+cudaError_t prefill_tc_launch(const PrefillArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                              const CUtensorMap& tv, cudaStream_t stream) {
+    const int kmax = (a.max_seqlen + kBM - 1) / kBM;
+    const long long tiles_ub = (long long)(a.T + kBM - 1) / kBM + a.N;
+    const long long grid = tiles_ub * a.Hq;
+    if (grid > 0x7fffffffll) return cudaErrorInvalidConfiguration;
+    const size_t smem = 1024 + sizeof(Smem) + tile_order_smem_ints(a.N, kmax) * sizeof(int);
+    static thread_local size_t set_to[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 64 || set_to[dev] < smem) {
+        e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        if (dev < 64) set_to[dev] = smem;
+    }
+    prefill_tc_kernel<<<(unsigned)grid, kThreads, smem, stream>>>(tq, tk, tv, a);
+    return cudaGetLastError();
+}
+
+}  // namespace sinkattn

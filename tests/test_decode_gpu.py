@@ -109,9 +109,9 @@ def test_bad_page_is_reported_and_skipped(S):
 
 
 def test_bad_length_is_reported(S):
-    inp = W.make_decode(2, 8, 2, [40, 20], seed=7)
+    inp = W.make_decode(2, 8, 2, [48, 48], seed=7)  # full page-table rows: 3 pages each
     g = inp.to("cuda")
-    g.kv_lens[1] = 10_000  # beyond max_pages * 16
+    g.kv_lens[1] = 10_000  # beyond max_pages * 16 = 48: clamped to 48
     S.sinkattn_decode(g.q, g.k_pages, g.v_pages, g.page_table, g.kv_lens, g.sinks, g.scale)
     assert S.sinkattn_get_error() == S.ERR_BAD_LENGTH
     assert S.sinkattn_get_error() == 0  # cleared by the read
