@@ -58,6 +58,8 @@ def _load():
     lib.sinkattn_decode.argtypes = [P, P, P, P, P, P, f32, P, P, ctypes.POINTER(DecodeDims), P, sz, P]
     lib.sinkattn_prefill.argtypes = [P, P, P, P, P, f32, i32, P, P, ctypes.POINTER(PrefillDims), P]
     lib.sinkattn_merge.argtypes = [P, P, P, P, P, ctypes.POINTER(MergeDims), P]
+    lib.sinkattn_decode_noalloc.argtypes = [P, P, P, P, P, P, f32, P, P, ctypes.POINTER(DecodeDims), P]
+    lib.sinkattn_decode_noalloc.restype = ctypes.c_int
     lib.sinkattn_decode_workspace_size.argtypes = [ctypes.POINTER(DecodeDims)]
     lib.sinkattn_decode_workspace_size.restype = sz
     lib.sinkattn_get_error.argtypes = [P]
@@ -187,6 +189,34 @@ def sinkattn_merge(partial_o, partial_lse, sinks=None, out=None, lse=None, retur
     st = _lib.sinkattn_merge(_ptr(partial_o), _ptr(partial_lse), _ptr(sinks), _ptr(out), _ptr(lse),
                              ctypes.byref(dims), _stream(stream))
     _check(st, "sinkattn_merge")
+    return out, lse
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20  # SINKATTN_DECODE_NOALLOC_SCRATCH_BYTES
+
+
+def sinkattn_decode_noalloc(q, k_pages, v_pages, page_table, kv_lens, sinks, scale, out, lse=None, stream=None):
+    """Decode with the library's built-in scratch instead of a workspace.
+
+    For callers that cannot allocate device memory on this path (a framework
+    owning the whole device through its own pool, a plugin interface that
+    passes only inputs and outputs, a loop that must avoid cudaMalloc's
+    device synchronisation).  ``out`` (and ``lse`` if wanted) must be given:
+    this function allocates nothing.  Problems needing more than 16 MiB of
+    scratch raise SinkAttnError(ERR_WORKSPACE); calls must not overlap on the GPU.
+    """
+    for t, name, dt, nd in ((q, "q", torch.bfloat16, 3), (k_pages, "k_pages", torch.bfloat16, 4),
+                            (v_pages, "v_pages", torch.bfloat16, 4), (page_table, "page_table", torch.int32, 2),
+                            (kv_lens, "kv_lens", torch.int32, 1), (sinks, "sinks", torch.float32, 1),
+                            (out, "out", torch.bfloat16, 3)):
+        _need(t, name, dt, nd)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 2)
+    dims = decode_dims(q, k_pages, page_table)
+    st = _lib.sinkattn_decode_noalloc(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table), _ptr(kv_lens),
+                                      _ptr(sinks), float(scale), _ptr(out), _ptr(lse), ctypes.byref(dims),
+                                      _stream(stream))
+    _check(st, "sinkattn_decode_noalloc")
     return out, lse
 
 

@@ -170,6 +170,33 @@ sinkattn_status_t sinkattn_merge(const float *partial_o, const float *partial_ls
                                  const sinkattn_merge_dims_t *dims, void *stream);
 
 /*
+ * sinkattn_decode without a workspace argument, for callers that cannot
+ * allocate device memory: a framework that has reserved the whole device for
+ * its own pool, a plugin interface that passes only input and output buffers,
+ * or a serving loop that must not call cudaMalloc / cudaFree because they can
+ * synchronise the device.  The blog posts describing the method have no
+ * counterpart to this call; it is a deployment convenience.
+ *
+ * Arguments, layouts and results are those of sinkattn_decode.  The split-KV
+ * scratch lives in a fixed array inside the library, of
+ * SINKATTN_DECODE_NOALLOC_SCRATCH_BYTES, held by every device that loads the
+ * library until the process exits.  The call allocates and frees nothing.
+ *   - A problem needing more scratch than that (see
+ *     sinkattn_decode_workspace_size) returns SINKATTN_ERR_WORKSPACE and
+ *     launches nothing.
+ *   - The first call on a device looks up the array's device address; make it
+ *     before any stream capture begins.
+ *   - Every call shares the one array, which keeps the last call's contents;
+ *     no value in it needs to start at zero.  Calls that can overlap on the
+ *     GPU race on the array: order them (one stream, or events).
+ */
+#define SINKATTN_DECODE_NOALLOC_SCRATCH_BYTES (16u << 20)
+sinkattn_status_t sinkattn_decode_noalloc(const void *q, const void *k_pages, const void *v_pages,
+                                          const int32_t *page_table, const int32_t *kv_lens,
+                                          const float *sinks, float scale, void *out, float *lse,
+                                          const sinkattn_decode_dims_t *dims, void *stream);
+
+/*
  * Synchronises `stream`, then returns and clears the current device's error
  * word (SINKATTN_OK when no kernel reported a problem).  If several problems
  * were recorded, the one with the lowest status code is returned.
