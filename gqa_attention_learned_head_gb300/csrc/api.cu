@@ -3,6 +3,10 @@
 // error word that kernels report into instead of trapping.
 #include <sinkattn.h>
 
+#include <unistd.h>
+
+#include <atomic>
+#include <chrono>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -54,6 +58,20 @@ sinkattn_status_t device_state(DeviceState** out) {
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Epoch of a decode call: unique within the process, never 0, below 2^40.  The start
+// is salted with the clock and the process id so that counters left in reused device
+// memory by another process are unlikely to carry a matching epoch.
+unsigned long long next_epoch() {
+    static std::atomic<unsigned long long> counter{
+        (static_cast<unsigned long long>(std::chrono::steady_clock::now().time_since_epoch().count()) ^
+         (static_cast<unsigned long long>(getpid()) << 20)) & ((1ull << 39) - 1)};
+    unsigned long long e;
+    do {
+        e = counter.fetch_add(1) & ((1ull << 40) - 1);
+    } while (e == 0);
+    return e;
+}
 
 // The prefill runs on the tcgen05 kernel.  SINKATTN_PREFILL_KERNEL=mma selects the
 // warp-level mma.sync kernel instead; it exists as the measured baseline only.
@@ -174,8 +192,8 @@ sinkattn_status_t sinkattn_decode(const void* q, const void* k_pages, const void
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     a.part_o = reinterpret_cast<float*>(ws);
     a.part_lse = a.part_o + plan.slots * G * kHeadDim;
-    size_t meta_off = (plan.slots * G * kHeadDim * 4 + plan.slots * G * 4 + 255) & ~size_t(255);
-    a.seg_meta = reinterpret_cast<int2*>(ws + meta_off);
+    a.counters = reinterpret_cast<unsigned long long*>(ws + plan.counters_offset);
+    a.epoch = next_epoch();
     a.err = ds->err;
     a.B = dims->batch;
     a.Hq = dims->num_q_heads;
@@ -184,7 +202,7 @@ sinkattn_status_t sinkattn_decode(const void* q, const void* k_pages, const void
     a.num_pages = dims->num_pages;
     a.max_pages = dims->max_pages;
     a.workers = plan.workers;
-    a.min_pages_per_worker = 8;
+    a.min_pages_per_worker = plan.min_pages;
     a.fixed_workers = dims->num_workers > 0 ? 1 : 0;
     a.scale_log2 = scale * 1.4426950408889634f;
     return decode_launch(a, plan, tk, tv, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SINKATTN_OK

@@ -10,15 +10,24 @@
 // metadata copied to the GPU).
 //
 // GB300 design (not the pages' FlashInfer template):
-//  * Work = the flattened list of (request b, KV head g, page) units.  Every
-//    CTA recomputes the per-request page prefix sum from kv_lens in shared
-//    memory, so the split needs no host-side knowledge of the lengths (no
-//    host sync; graph-capturable).  Worker warp w takes the contiguous share
-//    [w*U/W, (w+1)*U/W) of the U units: the load is balanced to one page.
-//  * A share that covers a whole (b, g) segment writes the final output;
-//    otherwise each piece writes an fp32 partial (o_c, lse_c) and
-//    merge_pieces_kernel combines them.  Only the piece holding page 0 is
-//    seeded with the sink, so the sink is counted exactly once.
+//  * Work = the flattened list of (request b, KV head g, page) units; a
+//    (b, g) pair is a "segment".  Every CTA recomputes the per-request page
+//    prefix sum from kv_lens in shared memory, so the split needs no host-side
+//    knowledge of the lengths (no host sync; graph-capturable).  CTA c takes
+//    the contiguous share [c*U/C, (c+1)*U/C) of the U units: balanced to one
+//    page.  The share is cut at segment ends into "pieces".
+//  * A piece of >= 4 pages is spread over the CTA's 4 warps page by page
+//    (warp k takes pages k, k+4, ...); the warps then combine their online-
+//    softmax states in shared memory.  A shorter piece goes whole to one warp.
+//  * A piece that is a whole segment writes the final output.  Otherwise it
+//    writes an fp32 partial (o_c, lse_c) and bumps the segment's arrival
+//    counter; the CTA that completes a segment merges its partials by
+//    log-sum-exp (all 4 warps, at the end of its share) -- one kernel, no
+//    second launch.  Only the piece holding page 0 is seeded with the sink,
+//    so the sink is counted exactly once.  The counters carry the call's epoch
+//    in their high bits, so the workspace needs no zeroing, and the CTA that
+//    completes a segment resets its counter to 0, so replaying the same
+//    launch also works.
 //  * Each warp streams its pages through a private ring of kStages shared-
 //    memory stages.  One stage = the K and V slices of one (page, KV head):
 //    2 x 2 KiB, loaded by two TMA tensor copies with 128-byte swizzle (so the
@@ -31,78 +40,214 @@
 #include "kernels.h"
 #include "ptx.cuh"
 
+#ifndef SINKATTN_DECODE_STAGES
+#define SINKATTN_DECODE_STAGES 2
+#endif
+#ifndef SINKATTN_DECODE_MIN_PAGES
+#define SINKATTN_DECODE_MIN_PAGES 32
+#endif
+#ifndef SINKATTN_DECODE_MIN_BLOCKS
+#define SINKATTN_DECODE_MIN_BLOCKS 4
+#endif
+
 namespace sinkattn {
 namespace {
 
-constexpr int kWarps = 4;             // worker warps per CTA
-constexpr int kStages = 4;            // ring depth per warp
+constexpr int kWarps = 4;                        // warps per CTA
+constexpr int kStages = SINKATTN_DECODE_STAGES;  // ring depth per warp
 constexpr int kSliceBytes = kPageSize * kHeadDim * 2;  // 2048: one (page, KV head) of K or V
 constexpr int kStageBytes = 2 * kSliceBytes;
+constexpr int kMaxMerge = 2;  // a share completes at most its first and its last segment
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kNegInf = -__builtin_huge_valf();
+constexpr int kCountBits = 24;  // low bits of a segment counter: arrivals; high bits: call epoch
 
-__host__ __device__ constexpr size_t split_smem_fixed() {
-    return 1024 /* alignment slack */ + size_t(kWarps) * kStages * (kStageBytes + 8 + 4) + kWarps * 4;
-}
-
-__device__ __forceinline__ int clamp_len(int L, int cap) { return L < 0 ? 0 : (L > cap ? cap : L); }
-
-// Position of unit x in the flattened (request, KV head, page) order.
-struct Cursor {
-    int b, g, page, n;  // request, KV head, page within the request, pages of the request
+// Shared memory: ring | mbarriers | bad-page flags | combine area | merge queue | prefix[B+1].
+template <int NT>
+struct SmemLayout {
+    static constexpr int kHeads = 8 * NT;
+    static constexpr size_t ring = size_t(kWarps) * kStages * kStageBytes;
+    static constexpr size_t bars = ring;
+    static constexpr size_t bad = bars + size_t(kWarps) * kStages * 8;
+    static constexpr size_t cmb_o = bad + size_t(kWarps) * kStages * 4;                   // [2][warps][heads][64] f32
+    static constexpr size_t cmb_md = cmb_o + 2 * size_t(kWarps) * kHeads * kHeadDim * 4;  // [2][warps][heads] m, d
+    static constexpr size_t misc = cmb_md + 2 * size_t(kWarps) * kHeads * 8;              // scan scratch, counts
+    static constexpr size_t pend = misc + 8 * 4;                                          // partial pieces: <= 2
+    static constexpr size_t queue = pend + 2 * 4;
+    static constexpr size_t prefix = queue + kMaxMerge * 4;
+    static constexpr size_t fixed = prefix + 1024 /* alignment slack */;
 };
 
-__device__ __forceinline__ Cursor locate(const int* prefix, int B, int Hkv, long long x) {
-    int lo = 0, hi = B - 1;  // smallest b with prefix[b+1]*Hkv > x
-    while (lo < hi) {
-        int mid = (lo + hi) >> 1;
-        if ((long long)prefix[mid + 1] * Hkv > x) hi = mid;
-        else lo = mid + 1;
-    }
-    Cursor c;
-    c.b = lo;
-    c.n = prefix[lo + 1] - prefix[lo];
-    long long off = x - (long long)prefix[lo] * Hkv;
-    c.g = (int)(off / c.n);
-    c.page = (int)(off - (long long)c.g * c.n);
-    return c;
-}
-
-__device__ __forceinline__ void advance(Cursor& c, const int* prefix, int B, int Hkv) {
-    if (++c.page < c.n) return;
-    c.page = 0;
-    if (++c.g < Hkv) return;
-    c.g = 0;
-    do { ++c.b; } while (c.b < B && prefix[c.b + 1] == prefix[c.b]);
-    if (c.b < B) c.n = prefix[c.b + 1] - prefix[c.b];
-}
+__device__ __forceinline__ int clamp_len(int L, int cap) { return L < 0 ? 0 : (L > cap ? cap : L); }
 
 __device__ __forceinline__ uint32_t ld_u32(const __nv_bfloat16* p) {
     return __ldg(reinterpret_cast<const unsigned int*>(p));
 }
 
-// Worker count actually used for U units (identical in every CTA).
-__device__ __forceinline__ long long effective_workers(const DecodeArgs& a, long long U) {
-    long long w = a.workers;
-    if (!a.fixed_workers) {
-        long long want = (U + a.min_pages_per_worker - 1) / a.min_pages_per_worker;
-        if (want < w) w = want;
+__device__ __forceinline__ void cta_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory"); }
+
+// One piece of a CTA's share: units [ps, pe) of segment (b, g) whose first unit is seg_start.
+struct Piece {
+    long long ps, pe, seg_start;
+    int b, g, n, idx;
+    __device__ int len() const { return (int)(pe - ps); }
+    __device__ int page0() const { return (int)(ps - seg_start); }
+    __device__ bool split() const { return len() >= kWarps; }
+    // Units of this piece that warp w processes, and the page of its t-th one.
+    __device__ int count(int w) const {
+        if (split()) return len() > w ? (len() - w + kWarps - 1) / kWarps : 0;
+        return (idx % kWarps) == w ? len() : 0;
     }
-    if (w > U) w = U;
-    return w < 1 ? 1 : w;
+    __device__ int page(int w, int t) const { return page0() + (split() ? w + t * kWarps : t); }
+};
+
+__device__ __forceinline__ void piece_first(Piece& p, const int* prefix, int B, int Hkv, long long x0, long long x1) {
+    int lo = 0, hi = B - 1;  // smallest b with prefix[b+1]*Hkv > x0
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if ((long long)prefix[mid + 1] * Hkv > x0) hi = mid;
+        else lo = mid + 1;
+    }
+    p.b = lo;
+    p.n = prefix[lo + 1] - prefix[lo];
+    const long long off = x0 - (long long)prefix[lo] * Hkv;
+    p.g = (int)(off / p.n);
+    p.seg_start = (long long)prefix[lo] * Hkv + (long long)p.g * p.n;
+    p.ps = x0;
+    p.pe = min(x1, p.seg_start + p.n);
+    p.idx = 0;
+}
+
+// Moves to the next piece; p.ps >= x1 afterwards means the share is done.
+__device__ __forceinline__ void piece_next(Piece& p, const int* prefix, int B, int Hkv, long long x1) {
+    p.ps = p.pe;
+    ++p.idx;
+    if (p.ps >= x1) return;
+    p.seg_start = p.pe;  // a piece that ends before x1 ends at its segment's end
+    if (++p.g == Hkv) {
+        p.g = 0;
+        do { ++p.b; } while (p.b < B && prefix[p.b + 1] == prefix[p.b]);
+        p.n = prefix[p.b + 1] - prefix[p.b];
+    }
+    p.pe = min(x1, p.seg_start + p.n);
+}
+
+// CTA count actually used for U units (identical in every CTA).
+__device__ __forceinline__ long long effective_shares(const DecodeArgs& a, long long U) {
+    long long c = a.workers;
+    if (!a.fixed_workers) {
+        const long long want = (U + a.min_pages_per_worker - 1) / a.min_pages_per_worker;
+        if (want < c) c = want;
+    }
+    if (c > U) c = U;
+    return c < 1 ? 1 : c;
+}
+
+__device__ __forceinline__ unsigned long long cas_acq_rel(unsigned long long* p, unsigned long long cmp,
+                                                          unsigned long long val) {
+    unsigned long long old;
+    asm volatile("atom.acq_rel.gpu.global.cas.b64 %0, [%1], %2, %3;" : "=l"(old) : "l"(p), "l"(cmp), "l"(val)
+                 : "memory");
+    return old;
+}
+
+// Records one more finished piece of a segment; true for the piece that completes it.  The
+// compare-and-swap has release semantics (this CTA's partials, ordered before it by the CTA
+// barrier, become visible first) and acquire semantics (the other pieces' partials are visible
+// to the merge that follows).  The first attempt guesses that this is the last arrival, so the
+// arrival that completes a segment -- the one on the critical path -- needs one round trip.
+__device__ __forceinline__ bool arrive_last(unsigned long long* ctr, unsigned long long epoch, int pieces) {
+    unsigned long long old = (epoch << kCountBits) | (unsigned long long)(pieces - 1), nw;
+    while (true) {
+        nw = ((old >> kCountBits) == epoch) ? old + 1 : ((epoch << kCountBits) | 1ull);
+        const unsigned long long prev = cas_acq_rel(ctr, old, nw);
+        if (prev == old) break;
+        old = prev;
+    }
+    const bool last = (int)(nw & ((1ull << kCountBits) - 1)) == pieces;
+    // epoch 0 is never used: the next call starts afresh (no arrival can follow the last one)
+    if (last) *reinterpret_cast<volatile unsigned long long*>(ctr) = 0ull;
+    return last;
+}
+
+// Shares (CTAs) that hold units of segment seg: first share and count.
+__device__ __forceinline__ void segment_pieces(long long seg_start, int n, long long C, long long U, long long& c_first,
+                                               int& pieces) {
+    c_first = ((seg_start + 1) * C - 1) / U;
+    const long long c_last = ((seg_start + n) * C - 1) / U;
+    pieces = (int)(c_last - c_first + 1);
+}
+
+// Log-sum-exp merge of one head of one segment from its partials (base-2 lse), by 16 lanes:
+// lane l of the half-warp owns head-dims 4l..4l+3.  Pieces are taken 8 at a time with all loads
+// issued together and combined online.
+__device__ __forceinline__ void merge_head(const DecodeArgs& a, int b, int g, int h, long long slot0, int pieces,
+                                           int hl) {
+    constexpr int kChunk = 8;
+    const int G = a.G;
+    const float* lp = a.part_lse + slot0 * G + h;
+    const float* op = a.part_o + (slot0 * G + h) * kHeadDim + 4 * hl;
+    float M = kNegInf, sum = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c0 = 0; c0 < pieces; c0 += kChunk) {
+        float l[kChunk];
+        float4 v[kChunk];
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i) {
+            const bool in = c0 + i < pieces;
+            l[i] = in ? __ldcg(lp + (long long)(c0 + i) * G) : kNegInf;
+            v[i] = in ? __ldcg(reinterpret_cast<const float4*>(op + (long long)(c0 + i) * G * kHeadDim))
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float Mc = M;
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i) Mc = fmaxf(Mc, l[i]);
+        if (Mc == kNegInf) continue;
+        const float r = M == kNegInf ? 0.f : exp2f(M - Mc);
+        sum *= r;
+        o.x *= r;
+        o.y *= r;
+        o.z *= r;
+        o.w *= r;
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i) {
+            const float w = l[i] == kNegInf ? 0.f : exp2f(l[i] - Mc);
+            sum += w;
+            o.x += w * v[i].x;
+            o.y += w * v[i].y;
+            o.z += w * v[i].z;
+            o.w += w * v[i].w;
+        }
+        M = Mc;
+    }
+    const long long row = (long long)b * a.Hq + g * G + h;
+    uint2* dst = reinterpret_cast<uint2*>(a.out + row * kHeadDim) + hl;
+    if (M == kNegInf) {  // no live key and no finite sink in any piece
+        *dst = make_uint2(0u, 0u);
+        if (hl == 0 && a.lse) a.lse[row] = kNegInf;
+        return;
+    }
+    const float inv = 1.f / sum;
+    *dst = make_uint2(pack_bf16(o.x * inv, o.y * inv), pack_bf16(o.z * inv, o.w * inv));
+    if (hl == 0 && a.lse) a.lse[row] = (M + log2f(sum)) * kLn2;
 }
 
 template <int NT>  // NT = ceil(G / 8) groups of 8 query heads
-__global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
+__global__ void __launch_bounds__(kWarps * 32, SINKATTN_DECODE_MIN_BLOCKS) decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                                                    const __grid_constant__ CUtensorMap tmap_v,
                                                                    const DecodeArgs a) {
+    using L = SmemLayout<NT>;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(ring + kWarps * kStages * kStageBytes);
-    int* bad = reinterpret_cast<int*>(bars + kWarps * kStages);
-    int* wtot = bad + kWarps * kStages;
-    int* prefix = wtot + kWarps;  // [B + 1] exclusive prefix of pages per request
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::bars);
+    int* bad = reinterpret_cast<int*>(sm + L::bad);
+    float* cmb_o = reinterpret_cast<float*>(sm + L::cmb_o);
+    float* cmb_md = reinterpret_cast<float*>(sm + L::cmb_md);
+    int* misc = reinterpret_cast<int*>(sm + L::misc);  // [0..3] scan scratch, [4] merge queue, [6] pend count
+    int* pend = reinterpret_cast<int*>(sm + L::pend);    // segments of this share's partial pieces
+    int* queue = reinterpret_cast<int*>(sm + L::queue);  // segments this CTA completes and merges
+    int* prefix = reinterpret_cast<int*>(sm + L::prefix);  // [B + 1] exclusive prefix of pages per request
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int B = a.B, Hkv = a.Hkv, G = a.G, cap = a.max_pages * kPageSize;
@@ -112,9 +257,9 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const __grid_
     for (int base = 0; base < B; base += kWarps * 32) {
         int b = base + tid, n = 0;
         if (b < B) {
-            int L = a.kv_lens[b];
-            if ((L < 0 || L > cap) && blockIdx.x == 0) atomicOr(a.err, kErrBadLength);
-            n = (clamp_len(L, cap) + kPageSize - 1) / kPageSize;
+            int Lb = a.kv_lens[b];
+            if ((Lb < 0 || Lb > cap) && blockIdx.x == 0) atomicOr(a.err, kErrBadLength);
+            n = (clamp_len(Lb, cap) + kPageSize - 1) / kPageSize;
         }
         int incl = n;
 #pragma unroll
@@ -122,12 +267,12 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const __grid_
             int y = __shfl_up_sync(0xffffffffu, incl, o);
             if (lane >= o) incl += y;
         }
-        if (lane == 31) wtot[warp] = incl;
+        if (lane == 31) misc[warp] = incl;
         __syncthreads();
         int woff = 0, tot = 0;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
-            int v = wtot[w];
+            int v = misc[w];
             woff += (w < warp) ? v : 0;
             tot += v;
         }
@@ -135,18 +280,33 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const __grid_
         running += tot;
         __syncthreads();
     }
-    if (tid == 0) prefix[B] = running;
+    if (tid == 0) {
+        prefix[B] = running;
+        misc[4] = 0;
+    }
     __syncthreads();
+
+    // ---- 2. requests with no cached token: all mass on the sink (out = 0, lse = sink)
+    {
+        const long long rows = (long long)B * a.Hq;
+        for (long long r = (long long)blockIdx.x * blockDim.x + tid; r < rows; r += (long long)gridDim.x * blockDim.x) {
+            const int b = (int)(r / a.Hq);
+            if (prefix[b + 1] != prefix[b]) continue;
+            uint4* dst = reinterpret_cast<uint4*>(a.out + r * kHeadDim);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+            if (a.lse) a.lse[r] = __ldg(&a.sinks[r - (long long)b * a.Hq]);
+        }
+    }
 
     const long long U = (long long)running * Hkv;
     if (U == 0) return;
-    const long long W = effective_workers(a, U);
-    const long long w = (long long)blockIdx.x * kWarps + warp;
-    if (w >= W) return;
-    const long long x0 = w * U / W, x1 = (w + 1) * U / W;
-    const int npg = (int)(x1 - x0);
+    const long long C = effective_shares(a, U);
+    const long long cta = blockIdx.x;
+    if (cta >= C) return;
+    const long long x0 = cta * U / C, x1 = (cta + 1) * U / C;
 
-    uint8_t* my_ring = ring + warp * kStages * kStageBytes;
+    uint8_t* my_ring = sm + warp * kStages * kStageBytes;
     uint64_t* my_bars = bars + warp * kStages;
     int* my_bad = bad + warp * kStages;
     if (lane == 0) {
@@ -158,22 +318,30 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const __grid_
     }
     __syncwarp();
 
-    // ---- 2. producer: lane l resolves unit (x0 + base + l) to a pool row, 32 units at a time
-    int win_base = -64, win_row = -1;
-    auto issue = [&](int j) {  // warp-uniform; stage j % kStages must be free
-        if (j - win_base >= 32) {
-            win_base = j;
-            int jj = j + lane, row = -1;
-            if (jj < npg) {
-                Cursor c = locate(prefix, B, Hkv, x0 + jj);
-                int pid = __ldg(&a.page_table[(long long)c.b * a.max_pages + c.page]);
-                if (pid >= 0 && pid < a.num_pages) row = (pid * Hkv + c.g) * kPageSize;
+    // ---- 3. producer: walks this warp's units piece by piece; lanes resolve 32 page ids at a time
+    Piece pp;
+    piece_first(pp, prefix, B, Hkv, x0, x1);
+    int pt = 0, pcnt = pp.count(warp), win_base = -64, win_row = -1, issued = 0;
+    auto issue = [&]() -> bool {  // warp-uniform
+        while (pt >= pcnt) {
+            piece_next(pp, prefix, B, Hkv, x1);
+            if (pp.ps >= x1) return false;
+            pt = 0;
+            pcnt = pp.count(warp);
+            win_base = -64;
+        }
+        if (pt - win_base >= 32) {
+            win_base = pt;
+            int row = -1;
+            if (pt + lane < pcnt) {
+                const int pid = __ldg(&a.page_table[(long long)pp.b * a.max_pages + pp.page(warp, pt + lane)]);
+                if (pid >= 0 && pid < a.num_pages) row = (pid * Hkv + pp.g) * kPageSize;
             }
             win_row = row;
         }
-        int row = __shfl_sync(0xffffffffu, win_row, j - win_base);
+        const int row = __shfl_sync(0xffffffffu, win_row, pt - win_base);
         if (lane == 0) {
-            int s = j % kStages;
+            const int s = issued % kStages;
             uint8_t* dst = my_ring + s * kStageBytes;
             if (row >= 0) {
                 my_bad[s] = 0;
@@ -186,235 +354,299 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const __grid_
                 mbar_arrive(&my_bars[s]);
             }
         }
+        ++pt;
+        ++issued;
+        return true;
     };
-    for (int j = 0; j < kStages && j < npg; ++j) issue(j);
+    bool more = true;
+    for (int j = 0; j < kStages && more; ++j) more = issue();
 
-    // ---- 3. consumer
+    // ---- 4. consumer: piece by piece
     const int gq = lane >> 2, tq = lane & 3;  // mma fragment coordinates
-    Cursor cc = locate(prefix, B, Hkv, x0);
-    uint32_t qf[NT][4][2];
     float O[4][NT][4];
     float m[NT][2], d[NT][2];
-    int kv_len = 0;
-    bool piece_open = false, piece_first = false;
-    int stopped_at = -1;  // consumer position of a wait that gave up
-    int issued = min(kStages, npg);
+    int consumed = 0;
+    bool failed = false;  // a wait gave up: skip all further work, keep the barriers
 
-    for (int i = 0; i < npg; ++i) {
-        if (!piece_open) {
-            piece_open = true;
-            piece_first = (cc.page == 0);
-            kv_len = clamp_len(__ldg(&a.kv_lens[cc.b]), cap);
-            const __nv_bfloat16* qb = a.q + ((long long)cc.b * a.Hq + (long long)cc.g * G) * kHeadDim;
+    // Per-piece inputs (query fragments, sink logits, cache length), fetched one piece ahead.
+    struct PieceIn {
+        uint32_t qf[NT][4][2];
+        float sink2[NT][2];
+        int kv_len;
+    };
+    auto fetch = [&](const Piece& p, PieceIn& in) {
+        in.kv_len = clamp_len(__ldg(&a.kv_lens[p.b]), cap);
+        const __nv_bfloat16* qb = a.q + ((long long)p.b * a.Hq + (long long)p.g * G) * kHeadDim;
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                const int hl = nt * 8 + gq;
+        for (int nt = 0; nt < NT; ++nt) {
+            const int hl = nt * 8 + gq;
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    qf[nt][kk][0] = hl < G ? ld_u32(qb + hl * kHeadDim + kk * 16 + 2 * tq) : 0u;
-                    qf[nt][kk][1] = hl < G ? ld_u32(qb + hl * kHeadDim + kk * 16 + 8 + 2 * tq) : 0u;
-                }
+            for (int kk = 0; kk < 4; ++kk) {
+                in.qf[nt][kk][0] = hl < G ? ld_u32(qb + hl * kHeadDim + kk * 16 + 2 * tq) : 0u;
+                in.qf[nt][kk][1] = hl < G ? ld_u32(qb + hl * kHeadDim + kk * 16 + 8 + 2 * tq) : 0u;
+            }
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int h = nt * 8 + 2 * tq + e;
-                    m[nt][e] = (piece_first && h < G) ? __ldg(&a.sinks[cc.g * G + h]) * kLog2e : kNegInf;
-                    d[nt][e] = (piece_first && lane < 4) ? 1.f : 0.f;  // the sink's own e^(sink-m)=1, once per head
-                }
-#pragma unroll
-                for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) O[mt][nt][e] = 0.f;
+            for (int e = 0; e < 2; ++e) {
+                const int h = nt * 8 + 2 * tq + e;
+                in.sink2[nt][e] = h < G ? __ldg(&a.sinks[p.g * G + h]) * kLog2e : kNegInf;
             }
         }
+    };
+    PieceIn cur, nxt;
+    Piece cp;
+    piece_first(cp, prefix, B, Hkv, x0, x1);
+    fetch(cp, cur);
+    int pend_n = 0;  // partial pieces of this share (at most its first and its last), thread 0 only
 
-        const int s = i % kStages;
-        const bool ok = mbar_wait(&my_bars[s], (i / kStages) & 1);
-        if (!__all_sync(0xffffffffu, ok)) {
-            stopped_at = i;
-            break;
+    for (int pidx = 0; cp.ps < x1; ++pidx) {
+        Piece np = cp;
+        piece_next(np, prefix, B, Hkv, x1);
+        if (np.ps < x1) fetch(np, nxt);  // in flight while this piece is processed
+
+        const int cnt = cp.count(warp);
+        const bool first = cp.page0() == 0;                       // this piece holds the segment's page 0
+        const bool seeded = first && (!cp.split() || warp == 0);  // ... and this warp carries the sink
+        const int seg = cp.b * Hkv + cp.g;
+        const bool whole = first && (cp.pe == cp.seg_start + cp.n);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                m[nt][e] = seeded ? cur.sink2[nt][e] : kNegInf;
+                d[nt][e] = (seeded && lane < 4) ? 1.f : 0.f;  // the sink's own e^(sink-m)=1, once per head
+            }
+#pragma unroll
+            for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) O[mt][nt][e] = 0.f;
         }
-        const int valid = my_bad[s] ? 0 : min(kPageSize, kv_len - cc.page * kPageSize);
-        uint8_t* st = my_ring + s * kStageBytes;
-        if (valid < kPageSize) {
-            // Rows past the cache end (or a skipped page) may hold anything; zero the
-            // value rows so that 0-weight * garbage cannot produce NaN.
-            uint4* vz = reinterpret_cast<uint4*>(st + kSliceBytes);
-            for (int c = valid * 8 + lane; c < kPageSize * 8; c += 32) vz[c] = make_uint4(0, 0, 0, 0);
+
+        for (int t = 0; t < cnt && !failed; ++t) {
+            const int s = consumed % kStages;
+            if (!__all_sync(0xffffffffu, mbar_wait(&my_bars[s], (consumed / kStages) & 1))) {
+                failed = true;
+                if (lane == 0) atomicOr(a.err, kErrTimeout);
+                break;
+            }
+            const int page = cp.page(warp, t);
+            const int valid = my_bad[s] ? 0 : min(kPageSize, cur.kv_len - page * kPageSize);
+            uint8_t* st = my_ring + s * kStageBytes;
+            if (valid < kPageSize) {
+                // Rows past the cache end (or a skipped page) may hold anything; zero the
+                // value rows so that 0-weight * garbage cannot produce NaN.
+                uint4* vz = reinterpret_cast<uint4*>(st + kSliceBytes);
+                for (int c = valid * 8 + lane; c < kPageSize * 8; c += 32) vz[c] = make_uint4(0, 0, 0, 0);
+                __syncwarp();
+            }
+            const uint32_t kb = smem_u32(st), vb = kb + kSliceBytes;
+
+            // S^T = K Q^T : 16 tokens x 8 heads per n-tile
+            float acc[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const int row = ((lane >> 3) & 1) * 8 + (lane & 7);
+                const int chunk = 2 * kk + (lane >> 4);
+                uint32_t af[4];
+                ldmatrix_x4(af, kb + row * 128 + ((chunk ^ (row & 7)) << 4));
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[nt], af, cur.qf[nt][kk][0], cur.qf[nt][kk][1]);
+            }
+
+            // online softmax (base 2); this thread holds tokens gq, gq+8 and heads 2tq, 2tq+1
+            uint32_t pb[NT][2];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                float sc[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int tok = gq + (e >= 2 ? 8 : 0);
+                    sc[e] = tok < valid ? acc[nt][e] * a.scale_log2 : kNegInf;
+                }
+                float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
+#pragma unroll
+                for (int o = 4; o < 32; o <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+                }
+                const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
+                const bool dead0 = (mn0 == kNegInf), dead1 = (mn1 == kNegInf);
+                const float al0 = dead0 ? 1.f : fast_exp2(m[nt][0] - mn0);
+                const float al1 = dead1 ? 1.f : fast_exp2(m[nt][1] - mn1);
+                const float p0 = dead0 ? 0.f : fast_exp2(sc[0] - mn0);
+                const float p2 = dead0 ? 0.f : fast_exp2(sc[2] - mn0);
+                const float p1 = dead1 ? 0.f : fast_exp2(sc[1] - mn1);
+                const float p3 = dead1 ? 0.f : fast_exp2(sc[3] - mn1);
+                d[nt][0] = d[nt][0] * al0 + (p0 + p2);
+                d[nt][1] = d[nt][1] * al1 + (p1 + p3);
+                m[nt][0] = mn0;
+                m[nt][1] = mn1;
+#pragma unroll
+                for (int mt = 0; mt < 4; ++mt) {
+                    O[mt][nt][0] *= al0;
+                    O[mt][nt][1] *= al1;
+                    O[mt][nt][2] *= al0;
+                    O[mt][nt][3] *= al1;
+                }
+                pb[nt][0] = movmatrix_trans(pack_bf16(p0, p1));  // tokens 0..7  -> B rows k = 2tq, 2tq+1
+                pb[nt][1] = movmatrix_trans(pack_bf16(p2, p3));  // tokens 8..15
+            }
+
+            // O^T += V^T P^T : 4 tiles of 16 head-dims
+#pragma unroll
+            for (int mt = 0; mt < 4; ++mt) {
+                const int j = lane >> 3;
+                const int row = (j >> 1) * 8 + (lane & 7);
+                const int chunk = 2 * mt + (j & 1);
+                uint32_t af[4];
+                ldmatrix_x4_trans(af, vb + row * 128 + ((chunk ^ (row & 7)) << 4));
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(O[mt][nt], af, pb[nt][0], pb[nt][1]);
+            }
+
+            // release the stage and refill it
+            fence_proxy_async_smem();
             __syncwarp();
+            ++consumed;
+            if (more) more = issue();
         }
-        const uint32_t kb = smem_u32(st), vb = kb + kSliceBytes;
 
-        // S^T = K Q^T : 16 tokens x 8 heads per n-tile
-        float acc[NT][4];
+        // ---- end of the piece: this warp's normaliser over its lanes
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+            for (int e = 0; e < 2; ++e)
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            const int row = ((lane >> 3) & 1) * 8 + (lane & 7);
-            const int chunk = 2 * kk + (lane >> 4);
-            uint32_t af[4];
-            ldmatrix_x4(af, kb + row * 128 + ((chunk ^ (row & 7)) << 4));
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[nt], af, qf[nt][kk][0], qf[nt][kk][1]);
-        }
+                for (int o = 4; o < 32; o <<= 1) d[nt][e] += __shfl_xor_sync(0xffffffffu, d[nt][e], o);
 
-        // online softmax (base 2); this thread holds tokens gq, gq+8 and heads 2tq, 2tq+1
-        uint32_t pb[NT][2];
+        const long long slot = cta + seg;  // partial slot of this piece
+        if (!whole && tid == 0) pend[pend_n++] = seg;  // counted at the end of the share
+        if (!cp.split()) {
+            if (cnt > 0) {
+                // one warp holds the whole piece: normalise and write
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            float sc[4];
+                for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int tok = gq + (e >= 2 ? 8 : 0);
-                sc[e] = tok < valid ? acc[nt][e] * a.scale_log2 : kNegInf;
+                    for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int h = nt * 8 + 2 * tq + (e & 1);
+                            const int dim = mt * 16 + gq + (e >= 2 ? 8 : 0);
+                            if (h >= G) continue;
+                            const float dt = d[nt][e & 1];
+                            const float v = dt > 0.f ? O[mt][nt][e] / dt : 0.f;
+                            if (whole)
+                                a.out[((long long)cp.b * a.Hq + cp.g * G + h) * kHeadDim + dim] =
+                                    __float2bfloat16_rn(v);
+                            else
+                                a.part_o[(slot * G + h) * kHeadDim + dim] = v;
+                        }
+                    if (lane < 4) {
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int h = nt * 8 + 2 * tq + e;
+                            if (h >= G) continue;
+                            const float l2 = d[nt][e] > 0.f ? m[nt][e] + log2f(d[nt][e]) : kNegInf;
+                            if (whole) {
+                                if (a.lse) a.lse[(long long)cp.b * a.Hq + cp.g * G + h] = l2 * kLn2;
+                            } else {
+                                a.part_lse[slot * G + h] = l2;
+                            }
+                        }
+                    }
+                }
             }
-            float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
-#pragma unroll
-            for (int o = 4; o < 32; o <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-            }
-            const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
-            const bool dead0 = (mn0 == kNegInf), dead1 = (mn1 == kNegInf);
-            const float al0 = dead0 ? 1.f : fast_exp2(m[nt][0] - mn0);
-            const float al1 = dead1 ? 1.f : fast_exp2(m[nt][1] - mn1);
-            const float p0 = dead0 ? 0.f : fast_exp2(sc[0] - mn0);
-            const float p2 = dead0 ? 0.f : fast_exp2(sc[2] - mn0);
-            const float p1 = dead1 ? 0.f : fast_exp2(sc[1] - mn1);
-            const float p3 = dead1 ? 0.f : fast_exp2(sc[3] - mn1);
-            d[nt][0] = d[nt][0] * al0 + (p0 + p2);
-            d[nt][1] = d[nt][1] * al1 + (p1 + p3);
-            m[nt][0] = mn0;
-            m[nt][1] = mn1;
-#pragma unroll
-            for (int mt = 0; mt < 4; ++mt) {
-                O[mt][nt][0] *= al0;
-                O[mt][nt][1] *= al1;
-                O[mt][nt][2] *= al0;
-                O[mt][nt][3] *= al1;
-            }
-            pb[nt][0] = movmatrix_trans(pack_bf16(p0, p1));  // tokens 0..7  -> B rows k = 2tq, 2tq+1
-            pb[nt][1] = movmatrix_trans(pack_bf16(p2, p3));  // tokens 8..15
-        }
-
-        // O^T += V^T P^T : 4 tiles of 16 head-dims
-#pragma unroll
-        for (int mt = 0; mt < 4; ++mt) {
-            const int j = lane >> 3;
-            const int row = (j >> 1) * 8 + (lane & 7);
-            const int chunk = 2 * mt + (j & 1);
-            uint32_t af[4];
-            ldmatrix_x4_trans(af, vb + row * 128 + ((chunk ^ (row & 7)) << 4));
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(O[mt][nt], af, pb[nt][0], pb[nt][1]);
-        }
-
-        // release the stage and refill it
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (issued < npg) issue(issued++);
-
-        // end of a piece: normalise and write
-        const bool seg_last = (cc.page == cc.n - 1);
-        if (seg_last || i == npg - 1) {
-            const int seg = cc.b * Hkv + cc.g;
-            const bool whole = piece_first && seg_last;
+        } else {
+            // ---- a split piece: combine the four warps' states in shared memory (double buffered,
+            // so one barrier per piece suffices)
+            float* co = cmb_o + (pidx & 1) * (kWarps * L::kHeads * kHeadDim);
+            float* cmd = cmb_md + (pidx & 1) * (kWarps * L::kHeads * 2);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                float inv[2], lse2[2];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    float dt = d[nt][e];
-#pragma unroll
-                    for (int o = 4; o < 32; o <<= 1) dt += __shfl_xor_sync(0xffffffffu, dt, o);
-                    inv[e] = dt > 0.f ? 1.f / dt : 0.f;
-                    lse2[e] = dt > 0.f ? (m[nt][e] + log2f(dt)) * kLn2 : kNegInf;
-                }
 #pragma unroll
                 for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int h = nt * 8 + 2 * tq + (e & 1);
                         const int dim = mt * 16 + gq + (e >= 2 ? 8 : 0);
-                        if (h >= G) continue;
-                        const float v = O[mt][nt][e] * inv[e & 1];
-                        if (whole)
-                            a.out[((long long)cc.b * a.Hq + cc.g * G + h) * kHeadDim + dim] = __float2bfloat16_rn(v);
-                        else
-                            a.part_o[((w + seg) * G + h) * kHeadDim + dim] = v;
+                        co[(warp * L::kHeads + h) * kHeadDim + dim] = O[mt][nt][e];
                     }
                 if (lane < 4) {
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int h = nt * 8 + 2 * tq + e;
-                        if (h >= G) continue;
-                        if (whole) {
-                            if (a.lse) a.lse[(long long)cc.b * a.Hq + cc.g * G + h] = lse2[e];
-                        } else {
-                            a.part_lse[(w + seg) * G + h] = lse2[e];
-                        }
+                        cmd[(warp * L::kHeads + h) * 2 + 0] = m[nt][e];
+                        cmd[(warp * L::kHeads + h) * 2 + 1] = d[nt][e];
                     }
                 }
             }
-            if (piece_first && lane == 0) {
-                // pieces of this segment: owners of its first and last unit are consecutive workers
-                const long long seg_end = (long long)prefix[cc.b] * Hkv + (long long)(cc.g + 1) * cc.n;
-                const long long w_last = (seg_end * W - 1) / U;
-                a.seg_meta[seg] = make_int2((int)(w + seg), (int)(w_last - w + 1));
+            cta_bar();
+            for (int h = warp; h < G; h += kWarps) {
+                float M = kNegInf;
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) M = fmaxf(M, cmd[(w * L::kHeads + h) * 2]);
+                float dt = 0.f, ox = 0.f, oy = 0.f;
+                if (M != kNegInf) {
+#pragma unroll
+                    for (int w = 0; w < kWarps; ++w) {
+                        const float mw = cmd[(w * L::kHeads + h) * 2];
+                        const float sw = mw == kNegInf ? 0.f : fast_exp2(mw - M);
+                        const float2 v = reinterpret_cast<const float2*>(co + (w * L::kHeads + h) * kHeadDim)[lane];
+                        dt += sw * cmd[(w * L::kHeads + h) * 2 + 1];
+                        ox += sw * v.x;
+                        oy += sw * v.y;
+                    }
+                }
+                const float inv = dt > 0.f ? 1.f / dt : 0.f;
+                const float l2 = dt > 0.f ? M + log2f(dt) : kNegInf;
+                if (whole) {
+                    const long long row = (long long)cp.b * a.Hq + cp.g * G + h;
+                    reinterpret_cast<__nv_bfloat162*>(a.out + row * kHeadDim)[lane] =
+                        __floats2bfloat162_rn(ox * inv, oy * inv);
+                    if (lane == 0 && a.lse) a.lse[row] = l2 * kLn2;
+                } else {
+                    reinterpret_cast<float2*>(a.part_o + (slot * G + h) * kHeadDim)[lane] =
+                        make_float2(ox * inv, oy * inv);
+                    if (lane == 0) a.part_lse[slot * G + h] = l2;
+                }
             }
-            piece_open = false;
         }
-        advance(cc, prefix, B, Hkv);
+        cp = np;
+        if (cp.ps < x1) cur = nxt;
     }
 
-    if (stopped_at >= 0) {
-        if (lane == 0) atomicOr(a.err, kErrTimeout);
+    if (tid == 0) misc[6] = pend_n;
+    if (failed) {
         // let copies already in flight land (bounded) before the CTA's shared memory is released
-        for (int j = stopped_at; j < issued; ++j) (void)mbar_wait(&my_bars[j % kStages], (j / kStages) & 1);
+        for (int j = consumed; j < issued; ++j) (void)mbar_wait(&my_bars[j % kStages], (j / kStages) & 1);
     }
-}
 
-// Combines the pieces of every split (request, KV head) segment; also writes the
-// rows of empty requests (all mass on the sink: out = 0, lse = sink).
-__global__ void __launch_bounds__(128) merge_pieces_kernel(const DecodeArgs a) {
-    const int lane = threadIdx.x & 31;
-    const long long row = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
-    if (row >= (long long)a.B * a.Hq) return;
-    const int b = (int)(row / a.Hq), h = (int)(row - (long long)b * a.Hq);
-    const int g = h / a.G, hl = h - g * a.G;
-    const int L = clamp_len(__ldg(&a.kv_lens[b]), a.max_pages * kPageSize);
-    __nv_bfloat162* out2 = reinterpret_cast<__nv_bfloat162*>(a.out + row * kHeadDim) + lane;
-    if (L == 0) {
-        *out2 = __floats2bfloat162_rn(0.f, 0.f);
-        if (lane == 0 && a.lse) a.lse[row] = __ldg(&a.sinks[h]);
-        return;
+    // ---- 5. count this share's partial pieces (at most two); merge the segments it completes
+    __syncthreads();  // every partial of this CTA is written (CTA scope) ...
+    if (tid < 2 && tid < misc[6]) {  // ... and the release CAS publishes them device-wide
+        const int seg = pend[tid];
+        const int b = seg / Hkv, g = seg - b * Hkv;
+        const int n = prefix[b + 1] - prefix[b];
+        long long c_first;
+        int pieces;
+        segment_pieces((long long)prefix[b] * Hkv + (long long)g * n, n, C, U, c_first, pieces);
+        if (arrive_last(&a.counters[seg], a.epoch, pieces)) queue[atomicAdd(&misc[4], 1)] = seg;
     }
-    const int2 meta = a.seg_meta[(long long)b * a.Hkv + g];
-    if (meta.y <= 1) return;
-    const float* lp = a.part_lse + (long long)meta.x * a.G + hl;
-    const float* op = a.part_o + ((long long)meta.x * a.G + hl) * kHeadDim + 2 * lane;
-    float M = kNegInf;
-    for (int c = 0; c < meta.y; ++c) M = fmaxf(M, lp[(long long)c * a.G]);
-    float sum = 0.f, ox = 0.f, oy = 0.f;
-    for (int c = 0; c < meta.y; ++c) {
-        const float wgt = __expf(lp[(long long)c * a.G] - M);
-        sum += wgt;
-        const float2 v = *reinterpret_cast<const float2*>(op + (long long)c * a.G * kHeadDim);
-        ox += wgt * v.x;
-        oy += wgt * v.y;
+    __syncthreads();
+    const int nq = misc[4];
+    // (segment, head) items over half-warps: 8 per pass of the CTA
+    for (int item = warp * 2 + (lane >> 4); item < nq * G; item += kWarps * 2) {
+        const int seg = queue[item / G], h = item % G;
+        const int b = seg / Hkv, g = seg - b * Hkv;
+        const int n = prefix[b + 1] - prefix[b];
+        long long c_first;
+        int pieces;
+        segment_pieces((long long)prefix[b] * Hkv + (long long)g * n, n, C, U, c_first, pieces);
+        merge_head(a, b, g, h, c_first + seg, pieces, lane & 15);
     }
-    const float inv = 1.f / sum;
-    *out2 = __floats2bfloat162_rn(ox * inv, oy * inv);
-    if (lane == 0 && a.lse) a.lse[row] = M + logf(sum);
-}
-
-template <int NT>
-cudaError_t launch_split(const DecodeArgs& args, const DecodePlan& plan, const CUtensorMap& tk,
-                         const CUtensorMap& tv, cudaStream_t stream) {
-    decode_split_kernel<NT><<<plan.grid, kWarps * 32, plan.smem, stream>>>(tk, tv, args);
-    return cudaGetLastError();
 }
 
 template <int NT>
@@ -431,38 +663,65 @@ cudaError_t ensure_smem_attr(size_t smem) {
 
 }  // namespace
 
-cudaError_t decode_plan(int B, int Hq, int Hkv, int num_workers, DecodePlan* plan) {
-    const int G = Hq / Hkv;
-    const size_t smem = split_smem_fixed() + size_t(B + 1) * 4;
-    cudaError_t e = G <= 8 ? ensure_smem_attr<1>(smem) : ensure_smem_attr<2>(smem);
+// Resident CTAs per SM x SM count for one (device, group width, shared memory) triple,
+// remembered so that repeated calls skip the occupancy query.
+cudaError_t resident_ctas(int NT, size_t smem, long long* ctas) {
+    struct Entry {
+        int dev, NT;
+        size_t smem;
+        long long ctas;
+    };
+    static thread_local Entry cache[8] = {};
+    static thread_local int next = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    int dev = 0, sms = 0, per_sm = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    for (const Entry& c : cache)
+        if (c.ctas > 0 && c.dev == dev && c.NT == NT && c.smem == smem) {
+            *ctas = c.ctas;
+            return cudaSuccess;
+        }
+    e = NT == 1 ? ensure_smem_attr<1>(smem) : ensure_smem_attr<2>(smem);
+    if (e != cudaSuccess) return e;
+    int sms = 0, per_sm = 0;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    e = G <= 8 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_split_kernel<1>, kWarps * 32, smem)
-               : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_split_kernel<2>, kWarps * 32, smem);
+    e = NT == 1 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_split_kernel<1>, kWarps * 32, smem)
+                : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_split_kernel<2>, kWarps * 32, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
-    long long workers = num_workers > 0 ? num_workers : (long long)sms * per_sm * kWarps;
-    plan->workers = (int)workers;
-    plan->grid = (int)((workers + kWarps - 1) / kWarps);
+    cache[next] = Entry{dev, NT, smem, (long long)sms * per_sm};
+    next = (next + 1) % 8;
+    *ctas = (long long)sms * per_sm;
+    return cudaSuccess;
+}
+
+cudaError_t decode_plan(int B, int Hq, int Hkv, int num_workers, DecodePlan* plan) {
+    const int G = Hq / Hkv;
+    const int NT = G <= 8 ? 1 : 2;
+    const size_t smem = (NT == 1 ? SmemLayout<1>::fixed : SmemLayout<2>::fixed) + size_t(B + 1) * 4;
+    long long resident = 0;
+    cudaError_t e = resident_ctas(NT, smem, &resident);
+    if (e != cudaSuccess) return e;
+    const long long shares = num_workers > 0 ? num_workers : resident;
+    plan->workers = (int)shares;
+    plan->min_pages = SINKATTN_DECODE_MIN_PAGES;
+    plan->grid = (int)shares;
     plan->smem = smem;
-    plan->slots = (size_t)workers + (size_t)B * Hkv;
+    plan->slots = (size_t)shares + (size_t)B * Hkv;
     size_t bytes = plan->slots * G * kHeadDim * 4;   // partial o
-    bytes += plan->slots * G * 4;                    // partial lse
-    bytes = (bytes + 255) & ~size_t(255);
-    bytes += (size_t)B * Hkv * sizeof(int2);         // segment table
-    plan->ws_bytes = bytes;
+    bytes += plan->slots * G * 4;                    // partial lse (base 2)
+    plan->counters_offset = (bytes + 255) & ~size_t(255);
+    plan->ws_bytes = plan->counters_offset + (size_t)B * Hkv * sizeof(unsigned long long);
     return cudaSuccess;
 }
 
 cudaError_t decode_launch(const DecodeArgs& args, const DecodePlan& plan, const CUtensorMap& tk,
                           const CUtensorMap& tv, cudaStream_t stream) {
     if (args.B == 0) return cudaSuccess;
-    cudaError_t e = args.G <= 8 ? launch_split<1>(args, plan, tk, tv, stream) : launch_split<2>(args, plan, tk, tv, stream);
-    if (e != cudaSuccess) return e;
-    const long long rows = (long long)args.B * args.Hq;
-    merge_pieces_kernel<<<(unsigned)((rows + 3) / 4), 128, 0, stream>>>(args);
+    if (args.G <= 8)
+        decode_split_kernel<1><<<plan.grid, kWarps * 32, plan.smem, stream>>>(tk, tv, args);
+    else
+        decode_split_kernel<2><<<plan.grid, kWarps * 32, plan.smem, stream>>>(tk, tv, args);
     return cudaGetLastError();
 }
 

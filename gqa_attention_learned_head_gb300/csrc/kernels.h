@@ -21,8 +21,9 @@ struct DecodeArgs {
     __nv_bfloat16* out;         // [B, Hq, 64]
     float* lse;                 // [B, Hq] or null
     float* part_o;              // [slots, G, 64]
-    float* part_lse;            // [slots, G]
-    int2* seg_meta;             // [B*Hkv]: (first slot, number of pieces)
+    float* part_lse;            // [slots, G], base-2 log-sum-exp
+    unsigned long long* counters;  // [B*Hkv]: (call epoch << 24) | pieces arrived
+    unsigned long long epoch;      // this call's epoch, in [1, 2^40)
     unsigned* err;              // device error word
     int B, Hq, Hkv, G, num_pages, max_pages;
     int workers;                // number of worker warps sharing the work
@@ -34,9 +35,11 @@ struct DecodeArgs {
 struct DecodePlan {
     int grid;            // CTAs of the split kernel
     int workers;         // worker warps
+    int min_pages;       // automatic mode: never cut shares finer than this many pages
     size_t smem;         // dynamic shared memory of the split kernel
-    size_t slots;        // partial-result slots the workspace must hold
-    size_t ws_bytes;     // workspace bytes
+    size_t slots;            // partial-result slots the workspace must hold
+    size_t counters_offset;  // byte offset of the per-segment arrival counters
+    size_t ws_bytes;         // workspace bytes
 };
 
 // Plan the decode launch for the current device (no device memory touched).
