@@ -172,24 +172,35 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(x, world):
+def _reduce(x, world, op):
+    """All-reduce one float over the ranks (NCCL: on the GPU; gloo: on the CPU)."""
     if world == 1:
         return x
     import torch.distributed as dist
 
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=op)
     return float(t.item())
+
+
+def max_over_ranks(x, world):
+    import torch.distributed as dist
+
+    return _reduce(x, world, dist.ReduceOp.MAX)
 
 
 def sum_over_ranks(x, world):
-    if world == 1:
-        return x
     import torch.distributed as dist
 
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.SUM)
-    return float(t.item())
+    return _reduce(x, world, dist.ReduceOp.SUM)
+
+
+def weak_scaling_value(units_this_rank, ms_this_rank, world):
+    """Whole-job throughput: units all ranks processed / the slowest rank's time (units per second)."""
+    total = sum_over_ranks(float(units_this_rank), world)
+    slowest = max_over_ranks(float(ms_this_rank), world)
+    return total / (slowest * 1e-3), slowest
 
 
 def timed_steps(step, K, warmup, flush, stream):
