@@ -220,21 +220,30 @@ __global__ void __launch_bounds__(kThreads, 2)
 
             const int kb = j * kBN;
             const bool masked = (kb + kBN > L) || (a.causal && kb + kBN - 1 > row0);
-            float mx = kNegInf;
-            if (masked) {
-                const int lim = a.causal ? min(L, qrow + 1) : L;  // keys [kb, lim) are visible
+            // The row max is taken on the raw scores (scale > 0) with eight independent 3-input max
+            // chains; p = exp2(s * scale_log2 - m) is then one FFMA and one MUFU per score.
+            float mul = scale_log2;
+            if (!(scale_log2 > 0.f)) {  // zero or negative scale: scale first, mask after
 #pragma unroll
-                for (int c = 0; c < 128; ++c) {
-                    s[c] = (kb + c < lim) ? s[c] * scale_log2 : kNegInf;
-                    mx = fmaxf(mx, s[c]);
-                }
-            } else {
-#pragma unroll
-                for (int c = 0; c < 128; ++c) {
-                    s[c] *= scale_log2;
-                    mx = fmaxf(mx, s[c]);
-                }
+                for (int c = 0; c < 128; ++c) s[c] *= scale_log2;
+                mul = 1.f;
             }
+            if (masked) {
+                const int lim = (a.causal ? min(L, qrow + 1) : L) - kb;  // keys kb + [0, lim) are visible
+#pragma unroll
+                for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? s[c] : kNegInf;
+            }
+            float acc[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = fmax3(s[i], s[8 + i], s[16 + i]);
+#pragma unroll
+            for (int c = 24; c < 120; c += 16)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[i] = fmax3(acc[i], s[c + i], s[c + 8 + i]);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = fmaxf(acc[i], s[120 + i]);
+            const float mx_raw = fmaxf(fmax3(acc[0], acc[1], acc[2]), fmax3(acc[3], acc[4], fmax3(acc[5], acc[6], acc[7])));
+            const float mx = mx_raw == kNegInf ? kNegInf : mx_raw * mul;
             const float m_new = fmaxf(m, mx);
             float factor = 1.f;
             bool rescale_o = false;
@@ -244,15 +253,17 @@ __global__ void __launch_bounds__(kThreads, 2)
                 m = m_new;
                 d *= factor;
             }
-            const float mref = (m == kNegInf) ? 0.f : m;
-            float sum = 0.f;
+            const float neg_m = (m == kNegInf) ? 0.f : -m;
+            float sums[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             uint32_t pk[64];
 #pragma unroll
             for (int c = 0; c < 64; ++c) {
-                const float p0 = fast_exp2(s[2 * c] - mref), p1 = fast_exp2(s[2 * c + 1] - mref);
-                sum += p0 + p1;
+                const float p0 = fast_exp2(fmaf(s[2 * c], mul, neg_m));
+                const float p1 = fast_exp2(fmaf(s[2 * c + 1], mul, neg_m));
+                sums[c & 7] += p0 + p1;
                 pk[c] = pack_bf16(p0, p1);
             }
+            const float sum = ((sums[0] + sums[1]) + (sums[2] + sums[3])) + ((sums[4] + sums[5]) + (sums[6] + sums[7]));
             d += sum;
             if (j > 0) {  // P_{j-1} consumed and O_{j-1} final before P and O are touched
                 if (!(ok = warp_wait(&sm.o_done, (j - 1) & 1))) break;
