@@ -7,11 +7,15 @@
 // sink-aware kernel serves prefill.
 //
 // One CTA = one tile of 128 query rows of one head; two CTAs share an SM.
-//   warp 0      TMA producer: Q once, then K_j / V_j tiles (128 keys x 64,
-//               128-byte swizzle) into a 2-stage ring.
-//   warp 1      allocates 256 TMEM columns; one lane issues every MMA:
-//                 S_j  = Q K_j^T   (M=128, N=128, K=64; SMEM x SMEM -> TMEM)
-//                 O   += P_j V_j   (M=128, N=64,  K=128; P read from TMEM)
+//   warps 0, 3  TMA producers: Q once and K_j tiles into a 3-stage ring
+//               (warp 0), V_j tiles into a 2-stage ring (warp 3); 128 keys x 64,
+//               128-byte swizzle.
+//   warp 1      allocates 256 TMEM columns; one lane issues S_j = Q K_j^T
+//               (M=128, N=128, K=64; SMEM x SMEM -> TMEM) as soon as the softmax
+//               has read S_{j-1}.
+//   warp 2      one lane issues O += P_j V_j (M=128, N=64, K=128; P read from
+//               TMEM) as soon as P_j is written.  Two issuers, so that neither
+//               chain waits on the other's wake-up.
 //   warps 4-7   softmax: thread r owns query row r (TMEM lane r).  It reads
 //               S_j, releases the S columns at once (so S_{j+1} can start),
 //               masks the diagonal tile, takes exp2 against a running max that
@@ -37,6 +41,31 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kNegInf = -__builtin_huge_valf();
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: O / d may grow by up to 2^8 before a rescale
 
+#ifndef SINKATTN_EXP_EMU
+#define SINKATTN_EXP_EMU 0  // of every 8 score pairs, this many take exp2 on the FMA pipe (0 measured best)
+#endif
+// Cubic for 2^f on [-1/2, 1/2], minimax in relative error (max 7.5e-5); derived by exp2_poly.py.
+constexpr float kExp2C0 = 0.9999280571937561f;
+constexpr float kExp2C1 = 0.6932609677314758f;
+constexpr float kExp2C2 = 0.2426111251115799f;
+constexpr float kExp2C3 = 0.0551716685295105f;
+constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23: adding it rounds to an integer in the low bits
+
+// exp2 of two values without the MUFU: 2^x = 2^round(x) * p(x - round(x)).  Arguments below -125
+// (including -inf) are clamped there, giving ~2e-38 instead of 0, which no sum can notice.
+__device__ __forceinline__ float2 exp2_fma2(float2 x) {
+    x.x = fmaxf(x.x, -125.f);
+    x.y = fmaxf(x.y, -125.f);
+    const float2 t = fadd2(x, make_float2(kRoundMagic, kRoundMagic));
+    const float2 r = fadd2(t, make_float2(-kRoundMagic, -kRoundMagic));
+    const float2 f = ffma2(r, make_float2(-1.f, -1.f), x);
+    float2 p = ffma2(f, make_float2(kExp2C3, kExp2C3), make_float2(kExp2C2, kExp2C2));
+    p = ffma2(p, f, make_float2(kExp2C1, kExp2C1));
+    p = ffma2(p, f, make_float2(kExp2C0, kExp2C0));
+    return make_float2(__int_as_float(__float_as_int(p.x) + (__float_as_int(t.x) << 23)),
+                       __int_as_float(__float_as_int(p.y) + (__float_as_int(t.y) << 23)));
+}  // log2 units: O / d may grow by up to 2^8 before a rescale
+
 // Instruction descriptors, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16 (bits 7-9, 10-12 = 1),
 // N >> 3 at bits 17-22, M >> 4 at bits 24-28; bit 16 = B is MN-major.
 constexpr uint32_t kIdescQK = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
@@ -52,11 +81,14 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
            | (2ull << 61);                           // 128-byte swizzle
 }
 
+constexpr int kKStages = 3, kVStages = 2;  // K runs further ahead: S_{j+1} is issued early
+
 struct __align__(1024) Smem {
     uint8_t q[kTileBytes];
-    uint8_t k[2][kTileBytes];
-    uint8_t v[2][kTileBytes];
-    uint64_t q_full, k_full[2], v_full[2], kv_empty[2], s_full, s_free, p_full, o_done, mma_done;
+    uint8_t k[kKStages][kTileBytes];
+    uint8_t v[kVStages][kTileBytes];
+    uint64_t q_full, k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
+    uint64_t s_full, s_free, p_full, o_done, mma_done;
     uint32_t tmem_base;
 };
 
@@ -108,16 +140,19 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     if (threadIdx.x == 0) {
         mbar_init(&sm.q_full, 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kKStages; ++i) {
             mbar_init(&sm.k_full[i], 1);
+            mbar_init(&sm.k_empty[i], 1);  // released by the S issuer
+        }
+        for (int i = 0; i < kVStages; ++i) {
             mbar_init(&sm.v_full[i], 1);
-            mbar_init(&sm.kv_empty[i], 1);
+            mbar_init(&sm.v_empty[i], 1);  // released by the PV issuer
         }
         mbar_init(&sm.s_full, 1);
         mbar_init(&sm.s_free, 128);
         mbar_init(&sm.p_full, 128);
         mbar_init(&sm.o_done, 1);
-        mbar_init(&sm.mma_done, 1);
+        mbar_init(&sm.mma_done, 2);
         fence_mbar_init();
         fence_proxy_async_smem();
     }
@@ -133,68 +168,81 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (warp < 4) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 40;");
         if (warp == 0 && lane == 0) {
-            // ------------------------------------------------------------ TMA producer
+            // ------------------------------------------------------------ TMA producer: Q, then K_j
             tma_prefetch_desc(&tmap_q);
             tma_prefetch_desc(&tmap_k);
-            tma_prefetch_desc(&tmap_v);
             mbar_arrive_expect_tx(&sm.q_full, kTileBytes);
             tma_load_3d(sm.q, &tmap_q, 0, h, s0 + row0, &sm.q_full);
             int issued = 0;
             for (int j = 0; j < ntile; ++j) {
-                const int st = j & 1;
-                if (j >= 2 && !mbar_wait(&sm.kv_empty[st], ((j >> 1) - 1) & 1)) {
+                const int st = j % kKStages;
+                if (j >= kKStages && !mbar_wait(&sm.k_empty[st], ((j / kKStages) - 1) & 1)) {
                     atomicOr(a.err, kErrTimeout);
                     break;
                 }
                 mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
                 tma_load_3d(sm.k[st], &tmap_k, 0, kvh, s0 + j * kBN, &sm.k_full[st]);
-                mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
-                tma_load_3d(sm.v[st], &tmap_v, 0, kvh, s0 + j * kBN, &sm.v_full[st]);
                 issued = j + 1;
             }
             // every copy this thread started has landed before the CTA can exit (bounded)
             (void)mbar_wait(&sm.q_full, 0);
-            for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j) {
-                (void)mbar_wait(&sm.k_full[j & 1], (j >> 1) & 1);
-                (void)mbar_wait(&sm.v_full[j & 1], (j >> 1) & 1);
+            for (int j = issued - kKStages < 0 ? 0 : issued - kKStages; j < issued; ++j)
+                (void)mbar_wait(&sm.k_full[j % kKStages], (j / kKStages) & 1);
+        } else if (warp == 3 && lane == 0) {
+            // ------------------------------------------------------------ TMA producer: V_j
+            tma_prefetch_desc(&tmap_v);
+            int issued = 0;
+            for (int j = 0; j < ntile; ++j) {
+                const int st = j % kVStages;
+                if (j >= kVStages && !mbar_wait(&sm.v_empty[st], ((j / kVStages) - 1) & 1)) {
+                    atomicOr(a.err, kErrTimeout);
+                    break;
+                }
+                mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
+                tma_load_3d(sm.v[st], &tmap_v, 0, kvh, s0 + j * kBN, &sm.v_full[st]);
+                issued = j + 1;
             }
+            for (int j = issued - kVStages < 0 ? 0 : issued - kVStages; j < issued; ++j)
+                (void)mbar_wait(&sm.v_full[j % kVStages], (j / kVStages) & 1);
         } else if (warp == 1 && lane == 0) {
-            // ------------------------------------------------------------ MMA issuer
-            const uint32_t tS = tbase + kColS, tO = tbase + kColO, tP = tbase + kColP;
+            // ------------------------------------------------------------ S issuer: S_j = Q K_j^T
+            // Needs only K_j and the S columns released by the softmax, so S_{j+1} is computed
+            // while the softmax still works on tile j.
+            const uint32_t tS = tbase + kColS;
             const uint32_t qaddr = smem_u32(sm.q);
-            bool ok = mbar_wait(&sm.q_full, 0) && mbar_wait(&sm.k_full[0], 0);
-            if (ok) {
+            bool ok = mbar_wait(&sm.q_full, 0);
+            for (int j = 0; ok && j < ntile; ++j) {
+                const int st = j % kKStages;
+                ok = mbar_wait(&sm.k_full[st], (j / kKStages) & 1) && (j == 0 || mbar_wait(&sm.s_free, (j - 1) & 1));
+                if (!ok) break;
                 tc_fence_after();
-                const uint32_t kaddr = smem_u32(sm.k[0]);
+                const uint32_t kaddr = smem_u32(sm.k[st]);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     tc_mma_ss(tS, sw128_desc(qaddr + kk * 32), sw128_desc(kaddr + kk * 32), kIdescQK, kk > 0);
                 tc_commit(&sm.s_full);
+                tc_commit(&sm.k_empty[st]);  // K_j read
             }
+            if (!ok) atomicOr(a.err, kErrTimeout);
+            tc_commit(&sm.mma_done);  // every MMA of both issuers has finished before TMEM is released
+            (void)mbar_wait(&sm.mma_done, 0);
+        } else if (warp == 2 && lane == 0) {
+            // ------------------------------------------------------------ PV issuer: O += P_j V_j
+            const uint32_t tO = tbase + kColO, tP = tbase + kColP;
+            bool ok = true;
             for (int j = 0; ok && j < ntile; ++j) {
-                if (j + 1 < ntile) {
-                    const int st = (j + 1) & 1;
-                    ok = mbar_wait(&sm.k_full[st], ((j + 1) >> 1) & 1) && mbar_wait(&sm.s_free, j & 1);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t kaddr = smem_u32(sm.k[st]);
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        tc_mma_ss(tS, sw128_desc(qaddr + kk * 32), sw128_desc(kaddr + kk * 32), kIdescQK, kk > 0);
-                    tc_commit(&sm.s_full);
-                }
-                ok = mbar_wait(&sm.v_full[j & 1], (j >> 1) & 1) && mbar_wait(&sm.p_full, j & 1);
+                ok = mbar_wait(&sm.v_full[j % kVStages], (j / kVStages) & 1) && mbar_wait(&sm.p_full, j & 1);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t vaddr = smem_u32(sm.v[j & 1]);
+                const uint32_t vaddr = smem_u32(sm.v[j % kVStages]);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
                     tc_mma_ts(tO, tP + ks * 8, sw128_desc(vaddr + ks * 2048), kIdescPV, (j > 0 || ks > 0) ? 1u : 0u);
-                tc_commit(&sm.kv_empty[j & 1]);
+                tc_commit(&sm.v_empty[j % kVStages]);  // V_j read
                 tc_commit(&sm.o_done);
             }
             if (!ok) atomicOr(a.err, kErrTimeout);
-            tc_commit(&sm.mma_done);  // every MMA has finished before TMEM is released
+            tc_commit(&sm.mma_done);
             (void)mbar_wait(&sm.mma_done, 0);
         }
     } else {
@@ -254,16 +302,27 @@ __global__ void __launch_bounds__(kThreads, 2)
                 d *= factor;
             }
             const float neg_m = (m == kNegInf) ? 0.f : -m;
-            float sums[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            // p = exp2(s * scale_log2 - m) in pairs with packed FMAs; SINKATTN_EXP_EMU of every 8
+            // pairs use the FMA-pipe polynomial, the rest the MUFU, so that neither pipe is the limit.
+            const float2 mul2 = make_float2(mul, mul), negm2 = make_float2(neg_m, neg_m);
+            float2 sums[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                              make_float2(0.f, 0.f)};
             uint32_t pk[64];
 #pragma unroll
             for (int c = 0; c < 64; ++c) {
-                const float p0 = fast_exp2(fmaf(s[2 * c], mul, neg_m));
-                const float p1 = fast_exp2(fmaf(s[2 * c + 1], mul, neg_m));
-                sums[c & 7] += p0 + p1;
-                pk[c] = pack_bf16(p0, p1);
+                const float2 xx = ffma2(make_float2(s[2 * c], s[2 * c + 1]), mul2, negm2);
+                float2 pp;
+                if ((c & 7) < SINKATTN_EXP_EMU) {
+                    pp = exp2_fma2(xx);
+                } else {
+                    pp.x = fast_exp2(xx.x);
+                    pp.y = fast_exp2(xx.y);
+                }
+                sums[c & 3] = fadd2(sums[c & 3], pp);
+                pk[c] = pack_bf16(pp.x, pp.y);
             }
-            const float sum = ((sums[0] + sums[1]) + (sums[2] + sums[3])) + ((sums[4] + sums[5]) + (sums[6] + sums[7]));
+            const float2 s01 = fadd2(fadd2(sums[0], sums[1]), fadd2(sums[2], sums[3]));
+            const float sum = s01.x + s01.y;
             d += sum;
             if (j > 0) {  // P_{j-1} consumed and O_{j-1} final before P and O are touched
                 if (!(ok = warp_wait(&sm.o_done, (j - 1) & 1))) break;

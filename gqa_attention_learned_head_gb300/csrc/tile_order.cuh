@@ -121,6 +121,32 @@ struct TileOrder {
         seq = found;
         tile = s_nt[found] - 1 - r;
     }
+
+    // Phase B for one warp on its own (no block barrier): all 32 lanes call it with the same
+    // idx < total and get the same answer.
+    __device__ void lookup_warp(int idx, int& seq, int& tile) const {
+        int lo = 0, hi = kmax - 1;  // largest r with C(r) <= idx
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (s_c[mid] <= idx) lo = mid;
+            else hi = mid - 1;
+        }
+        const int r = lo, lane = threadIdx.x & 31;
+        int j = idx - s_c[r], found = 0;
+        for (int c = 0; c < N; c += 32) {  // j-th sequence (in index order) with nt > r
+            const int n = c + lane;
+            unsigned bal = __ballot_sync(0xffffffffu, n < N && s_nt[n] > r);
+            const int cnt = __popc(bal);
+            if (j < cnt) {
+                for (int t = 0; t < j; ++t) bal &= bal - 1;
+                found = c + __ffs(bal) - 1;
+                break;
+            }
+            j -= cnt;
+        }
+        seq = found;
+        tile = s_nt[found] - 1 - r;
+    }
 };
 
 }  // namespace sinkattn
