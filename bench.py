@@ -388,11 +388,11 @@ def run_ours(args):
         value = total_bytes / (ms_max * 1e-3) / 1e9
         unit = "GB/s"
         achieved = nbytes / (ms * 1e-3) / 1e9
-        roof = {"bound": "hbm", "kernel": "decode_split_kernel + merge_pieces_kernel (one sinkattn_decode call)",
+        roof = {"bound": "hbm", "kernel": "decode_split_kernel (the only kernel of a sinkattn_decode call)",
                 "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                 "peak_source": f"{peak_src} hbm_gbs",
                 "traffic": profiled_traffic("decode_split_kernel", name, ["decode.cu", "ptx.cuh", "kernels.h"])}
-        launches = 2 * K
+        launches = K  # one decode_split_kernel per step
         cfg_extra = {"kv_tokens": int(inp.kv_lens.sum()), "kv_bytes_per_step": nbytes}
     else:
         inp, step, times, flops = bench_prefill(S, W, name, rank, K, Wu, flush, stream)
@@ -404,9 +404,11 @@ def run_ours(args):
         value = total_flops / (ms_max * 1e-3) / 1e12
         unit = "TFLOP/s"
         achieved = flops / (ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "kernel": "prefill kernel (one sinkattn_prefill call)", "achieved": achieved,
-                "peak": tc_peak, "unit": "TFLOP/s", "frac": achieved / tc_peak, "peak_source": f"{peak_src} bf16_tflops",
-                "traffic": None}
+        roof = {"bound": "tensor", "kernel": "prefill_tc_kernel (the only kernel of a sinkattn_prefill call)",
+                "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s", "frac": achieved / tc_peak,
+                "peak_source": f"{peak_src} bf16_tflops",
+                "traffic": profiled_traffic("prefill_tc_kernel", "causal_prefill",
+                                            ["prefill_tc.cu", "ptx.cuh", "kernels.h", "tile_order.cuh"])}
         launches = K
         cfg_extra = {"tokens": int(inp.q.shape[0]), "flops_per_step": flops}
     # keep the GPU under the same load for >= 1.5 s of clock samples (not timed)
@@ -484,7 +486,9 @@ def run_ours(args):
                                          num_workers=4 * 8 * W.LONG_CONTEXT_CHUNKS)
             lms = statistics.mean(lt)
             secondary.append({"workload": WORKLOAD_TEXT["long_context_decode"], "value": lb / (lms * 1e-3) / 1e9,
-                              "unit": "GB/s", "ms_per_step": lms, "frac_of_hbm_peak": lb / (lms * 1e-3) / 1e9 / hbm_peak})
+                              "unit": "GB/s", "ms_per_step": lms, "frac_of_hbm_peak": lb / (lms * 1e-3) / 1e9 / hbm_peak,
+                              "traffic": profiled_traffic("decode_split_kernel", "long_context_decode",
+                                                          ["decode.cu", "ptx.cuh", "kernels.h"])})
             del li
             pi, _, pt_, pf = bench_prefill(S, W, "causal_prefill", rank, Ks, Wu, flush, stream)
             pms = statistics.mean(pt_)
