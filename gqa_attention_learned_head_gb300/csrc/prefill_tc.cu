@@ -126,11 +126,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     TileOrder<kThreads> order;
-    order.build(order_ints, a.cu_seqlens, a.N, a.T, a.max_seqlen, kBM, a.err);
+    order.build_warp0(order_ints, a.cu_seqlens, a.N, a.T, a.max_seqlen, kBM, a.err);
+    __syncthreads();
+    order.finish_warp0_build();
     const int idx = (int)(blockIdx.x / a.Hq), h = (int)(blockIdx.x % a.Hq);
     if (idx >= order.total) return;  // whole CTA: no tile left
     int seq, qt;
-    order.lookup(idx, seq, qt);
+    order.lookup_warp(idx, seq, qt);  // every warp on its own
     const int s0 = a.cu_seqlens[seq];
     const int L = min(a.cu_seqlens[seq + 1] - s0, a.max_seqlen);
     const int row0 = qt * kBM;

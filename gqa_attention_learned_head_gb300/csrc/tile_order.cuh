@@ -86,6 +86,69 @@ struct TileOrder {
         __syncthreads();
     }
 
+    // Phase A done by warp 0 alone with shuffle scans; the caller then needs one block barrier
+    // before any thread reads the tables.  Same tables as build().
+    __device__ void build_warp0(int* smem, const int* cu, int N_, int T, int max_seqlen, int bm, unsigned* err) {
+        N = N_;
+        kmax = (max_seqlen + bm - 1) / bm;
+        s_nt = smem;
+        s_c = smem + N;
+        s_misc = s_c + kmax + 1;
+        total = 0;
+        if (threadIdx.x >= 32) return;
+        const int lane = threadIdx.x;
+        for (int r = lane; r <= kmax; r += 32) s_c[r] = 0;
+        __syncwarp();
+        int live = 0;
+        for (int n = lane; n < N; n += 32) {
+            const int lo = __ldg(&cu[n]), hi = __ldg(&cu[n + 1]);
+            int L = hi - lo;
+            if (lo < 0 || hi > T || L < 0 || L > max_seqlen) {
+                if (blockIdx.x == 0) atomicOr(err, kErrBadLength);
+                L = (lo < 0 || hi > T || L < 0) ? 0 : max_seqlen;
+            }
+            const int nt = (L + bm - 1) / bm;
+            s_nt[n] = nt;
+            if (nt > 0) {
+                atomicAdd(&s_c[nt - 1], 1);  // histogram of (tiles - 1)
+                ++live;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) live += __shfl_xor_sync(0xffffffffu, live, o);
+        __syncwarp();
+        // cnt(r) = live - #{n : nt(n) - 1 < r}; C(r) = sum_{r' < r} cnt(r')
+        int run_h = 0, run_c = 0;
+        for (int base = 0; base < kmax; base += 32) {
+            const int r = base + lane;
+            const int hv = r < kmax ? s_c[r] : 0;
+            int ih = hv;  // inclusive scan of the histogram
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, ih, o);
+                if (lane >= o) ih += y;
+            }
+            const int cnt = r < kmax ? live - (run_h + ih - hv) : 0;
+            int ic = cnt;  // inclusive scan of cnt
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, ic, o);
+                if (lane >= o) ic += y;
+            }
+            __syncwarp();
+            if (r < kmax) s_c[r] = run_c + ic - cnt;
+            run_h += __shfl_sync(0xffffffffu, ih, 31);
+            run_c += __shfl_sync(0xffffffffu, ic, 31);
+        }
+        total = run_c;
+        if (lane == 0) {
+            s_c[kmax] = total;
+            s_misc[0] = total;
+        }
+    }
+    // After the block barrier that follows build_warp0: every thread learns the total.
+    __device__ void finish_warp0_build() { total = s_misc[0]; }
+
     // Phase B: every thread calls it with the same idx < total.  Returns
     // the sequence and the query-tile index inside it.
     __device__ void lookup(int idx, int& seq, int& tile) {
