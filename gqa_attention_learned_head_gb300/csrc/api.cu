@@ -73,14 +73,18 @@ unsigned long long next_epoch() {
     return e;
 }
 
-// The prefill runs on the tcgen05 kernel.  SINKATTN_PREFILL_KERNEL=mma selects the
-// warp-level mma.sync kernel instead; it exists as the measured baseline only.
-bool prefill_use_legacy_kernel() {
-    static const bool legacy = [] {
+// Which prefill kernel runs.  By default the two-head tcgen05 kernel when the query-head group
+// size is even, else the one-head tcgen05 kernel.  SINKATTN_PREFILL_KERNEL=tc forces the one-head
+// kernel and =mma the warp-level mma.sync kernel (kept as the measured baseline only).
+enum class PrefillKernel { kAuto, kOneHead, kLegacy };
+PrefillKernel prefill_kernel_choice() {
+    static const PrefillKernel choice = [] {
         const char* s = std::getenv("SINKATTN_PREFILL_KERNEL");
-        return s && std::strcmp(s, "mma") == 0;
+        if (s && std::strcmp(s, "mma") == 0) return PrefillKernel::kLegacy;
+        if (s && std::strcmp(s, "tc") == 0) return PrefillKernel::kOneHead;
+        return PrefillKernel::kAuto;
     }();
-    return legacy;
+    return choice;
 }
 
 // 2-D bf16 tensor map over rows of 64 elements (128 B), box = box_rows x 64, 128-byte swizzle.
@@ -246,7 +250,8 @@ sinkattn_status_t sinkattn_prefill(const void* q, const void* k, const void* v, 
     a.causal = causal ? 1 : 0;
     a.scale_log2 = scale * 1.4426950408889634f;
     cudaError_t e;
-    if (prefill_use_legacy_kernel()) {
+    const PrefillKernel which = prefill_kernel_choice();
+    if (which == PrefillKernel::kLegacy) {
         e = prefill_mma_launch(a, static_cast<cudaStream_t>(stream));
     } else {
         CUtensorMap tq, tk, tv;
@@ -254,7 +259,9 @@ sinkattn_status_t sinkattn_prefill(const void* q, const void* k, const void* v, 
             !encode_thd(&tk, k, d.total_tokens, d.num_kv_heads, 128) ||
             !encode_thd(&tv, v, d.total_tokens, d.num_kv_heads, 128))
             return SINKATTN_ERR_INVALID_ARG;
-        e = prefill_tc_launch(a, tq, tk, tv, static_cast<cudaStream_t>(stream));
+        e = (which == PrefillKernel::kAuto && a.G % 2 == 0)
+                ? prefill_pp_launch(a, tq, tk, tv, static_cast<cudaStream_t>(stream))
+                : prefill_tc_launch(a, tq, tk, tv, static_cast<cudaStream_t>(stream));
     }
     return e == cudaSuccess ? SINKATTN_OK : SINKATTN_ERR_CUDA;
 }

@@ -74,6 +74,9 @@ struct PrefillArgs {
 // Tensor-core (tcgen05) prefill; the tensor maps are built by the caller.
 cudaError_t prefill_tc_launch(const PrefillArgs& args, const CUtensorMap& tmap_q, const CUtensorMap& tmap_k,
                               const CUtensorMap& tmap_v, cudaStream_t stream);
+// tcgen05 prefill over two query heads of one KV group per CTA (group size must be even).
+cudaError_t prefill_pp_launch(const PrefillArgs& args, const CUtensorMap& tmap_q, const CUtensorMap& tmap_k,
+                              const CUtensorMap& tmap_v, cudaStream_t stream);
 // Warp-level mma.sync prefill, kept as the legacy-tensor-path baseline.
 cudaError_t prefill_mma_launch(const PrefillArgs& args, cudaStream_t stream);
 

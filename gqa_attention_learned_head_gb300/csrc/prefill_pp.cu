@@ -1,0 +1,450 @@
+// prefill_pp.cu -- causal varlen prefill with a per-head sink on the tcgen05
+// tensor cores, two query heads per CTA whose softmax phases take turns.
+//
+// Source of the method: "GPT-OSS on day 0" (Perplexity), section "Kernels for
+// GPT-OSS / Sink Attention": the online softmax starts from m = sink, d = 1, so
+// the sink sits in the row normaliser and contributes no value row.
+//
+// Why two heads: at head_dim 64 one 128x128 score tile costs the tensor core
+// as long (S = Q K^T plus O += P V) as the MUFU needs for its 16384 exp2.  Two
+// CTAs per SM that each own one tile drift into lock-step -- both softmaxes
+// compete for the MUFU, then both wait for the tensor core.  Here one CTA per
+// SM owns the same 128 query rows of two heads h0, h0 + 1 of one KV group, so
+// K_j and V_j are loaded once for both, and the two softmax warpgroups hand an
+// "exp turn" back and forth through mbarriers: while warpgroup 0 exponentiates
+// tile j, the tensor core runs warpgroup 1's products, and the other way round.
+//
+//   warp 0      TMA: both Q tiles once, then K_j into a 3-stage ring.
+//   warp 3      TMA: V_j into a 2-stage ring.
+//   warp 1      allocates all 512 TMEM columns; one lane issues S_w = Q_w K_j^T
+//               for w = 0, 1 as soon as warpgroup w has read its previous S.
+//   warp 2      one lane issues O_w += P_w V_j as soon as P_w is written.
+//   warps 4-7   softmax of head h0 (warpgroup 0), thread r owns query row r.
+//   warps 8-11  softmax of head h0 + 1 (warpgroup 1).
+// TMEM columns: S_w at 128 w, O_w at 256 + 64 w, P_w (bf16 pairs) at 384 + 64 w.
+// Every wait is bounded; a wait that gives up sets the device error word and
+// the kernel winds down (the other waits then give up too).
+#include "kernels.h"
+#include "ptx.cuh"
+#include "tile_order.cuh"
+
+namespace sinkattn {
+namespace {
+
+constexpr int kBM = 128, kBN = 128;
+constexpr int kThreads = 384;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
+constexpr uint32_t kTileBytes = 128 * 128;  // 128 rows x 64 bf16
+constexpr int kKStages = 3, kVStages = 2;
+constexpr uint32_t kProducerRegs = 72, kSoftmaxRegs = 208;  // 128 x 72 + 256 x 208 <= 384 x 168
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kNegInf = -__builtin_huge_valf();
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: O / d may grow by up to 2^8 before a rescale
+
+#ifndef SINKATTN_PP_EXP_EMU
+#define SINKATTN_PP_EXP_EMU 0  // of every 8 score pairs, this many take exp2 on the FMA pipe
+#endif
+// Cubic for 2^f on [-1/2, 1/2], minimax in relative error (max 7.5e-5); derived by exp2_poly.py.
+constexpr float kExp2C0 = 0.9999280571937561f;
+constexpr float kExp2C1 = 0.6932609677314758f;
+constexpr float kExp2C2 = 0.2426111251115799f;
+constexpr float kExp2C3 = 0.0551716685295105f;
+constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23: adding it rounds to an integer in the low bits
+
+// exp2 of two values without the MUFU: 2^x = 2^round(x) * p(x - round(x)).  Arguments below -125
+// (including -inf) are clamped there, giving ~2e-38 instead of 0, which no sum can notice.
+__device__ __forceinline__ float2 exp2_fma2(float2 x) {
+    x.x = fmaxf(x.x, -125.f);
+    x.y = fmaxf(x.y, -125.f);
+    const float2 t = fadd2(x, make_float2(kRoundMagic, kRoundMagic));
+    const float2 r = fadd2(t, make_float2(-kRoundMagic, -kRoundMagic));
+    const float2 f = ffma2(r, make_float2(-1.f, -1.f), x);
+    float2 p = ffma2(f, make_float2(kExp2C3, kExp2C3), make_float2(kExp2C2, kExp2C2));
+    p = ffma2(p, f, make_float2(kExp2C1, kExp2C1));
+    p = ffma2(p, f, make_float2(kExp2C0, kExp2C0));
+    return make_float2(__int_as_float(__float_as_int(p.x) + (__float_as_int(t.x) << 23)),
+                       __int_as_float(__float_as_int(p.y) + (__float_as_int(t.y) << 23)));
+}
+
+// Instruction descriptors, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16 (bits 7-9, 10-12 = 1),
+// N >> 3 at bits 17-22, M >> 4 at bits 24-28; bit 16 = B is MN-major.
+constexpr uint32_t kIdescQK = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+constexpr uint32_t kIdescPV =
+    (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((64u >> 3) << 17) | ((128u >> 4) << 24);
+
+// Shared-memory matrix descriptor for a 128-byte-swizzled tile whose 8-row groups are 1024 B apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4)       // start address
+           | ((uint64_t)(1024u >> 4) << 16)          // leading-dimension byte offset (unused by these shapes)
+           | ((uint64_t)(1024u >> 4) << 32)          // stride-dimension byte offset: next 8-row group
+           | (1ull << 46)                            // descriptor version
+           | (2ull << 61);                           // 128-byte swizzle
+}
+
+struct __align__(1024) Smem {
+    uint8_t q[2][kTileBytes];
+    uint8_t k[kKStages][kTileBytes];
+    uint8_t v[kVStages][kTileBytes];
+    uint64_t q_full, k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
+    uint64_t s_full[2], s_free[2], p_full[2], o_done[2];
+    uint64_t turn[2];  // turn[w] completes a phase when the other warpgroup has finished an exp phase
+    uint64_t mma_done;
+    uint32_t tmem_base;
+};
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+// exp2 on the MUFU as a volatile asm: the compiler keeps volatile asm statements in program order,
+// so these stay between the turn wait and the turn hand-off instead of being hoisted above the one
+// or sunk below the other towards their uses.
+__device__ __forceinline__ float ex2_in_turn(float x) {
+    float y;
+    asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity));
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_pp_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                      const __grid_constant__ CUtensorMap tmap_v, const PrefillArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    int* order_ints = reinterpret_cast<int*>(&sm + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    TileOrder<kThreads> order;
+    order.build_warp0(order_ints, a.cu_seqlens, a.N, a.T, a.max_seqlen, kBM, a.err);
+    __syncthreads();
+    order.finish_warp0_build();
+    const int npairs = a.Hq >> 1;
+    const int idx = (int)(blockIdx.x / npairs), h0 = 2 * (int)(blockIdx.x % npairs);
+    if (idx >= order.total) return;  // whole CTA: no tile left
+    int seq, qt;
+    order.lookup_warp(idx, seq, qt);  // every warp on its own
+    const int s0 = a.cu_seqlens[seq];
+    const int L = min(a.cu_seqlens[seq + 1] - s0, a.max_seqlen);
+    const int row0 = qt * kBM;
+    const int kvh = h0 / a.G;  // h0 and h0 + 1 share it: the group size is even
+    const int kend = a.causal ? min(L, row0 + kBM) : L;
+    const int ntile = (kend + kBN - 1) / kBN;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&sm.q_full, 1);
+        for (int i = 0; i < kKStages; ++i) {
+            mbar_init(&sm.k_full[i], 1);
+            mbar_init(&sm.k_empty[i], 1);  // released by the S issuer after both heads' S
+        }
+        for (int i = 0; i < kVStages; ++i) {
+            mbar_init(&sm.v_full[i], 1);
+            mbar_init(&sm.v_empty[i], 1);  // released by the PV issuer after both heads' PV
+        }
+        for (int w = 0; w < 2; ++w) {
+            mbar_init(&sm.s_full[w], 1);
+            mbar_init(&sm.s_free[w], 128);
+            mbar_init(&sm.p_full[w], 128);
+            mbar_init(&sm.o_done[w], 1);
+            mbar_init(&sm.turn[w], 4);  // one arrival per warp of the other warpgroup
+        }
+        mbar_init(&sm.mma_done, 2);
+        fence_mbar_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 1) {
+        tmem_alloc(&sm.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = sm.tmem_base;
+
+    if (warp < 4) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
+        if (warp == 0 && lane == 0) {
+            // ------------------------------------------------------------ TMA producer: Q_0, Q_1, then K_j
+            tma_prefetch_desc(&tmap_q);
+            tma_prefetch_desc(&tmap_k);
+            mbar_arrive_expect_tx(&sm.q_full, 2 * kTileBytes);
+            tma_load_3d(sm.q[0], &tmap_q, 0, h0, s0 + row0, &sm.q_full);
+            tma_load_3d(sm.q[1], &tmap_q, 0, h0 + 1, s0 + row0, &sm.q_full);
+            int issued = 0;
+            for (int j = 0; j < ntile; ++j) {
+                const int st = j % kKStages;
+                if (j >= kKStages && !mbar_wait(&sm.k_empty[st], ((j / kKStages) - 1) & 1)) {
+                    atomicOr(a.err, kErrTimeout);
+                    break;
+                }
+                mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
+                tma_load_3d(sm.k[st], &tmap_k, 0, kvh, s0 + j * kBN, &sm.k_full[st]);
+                issued = j + 1;
+            }
+            // every copy this thread started has landed before the CTA can exit (bounded)
+            (void)mbar_wait(&sm.q_full, 0);
+            for (int j = issued - kKStages < 0 ? 0 : issued - kKStages; j < issued; ++j)
+                (void)mbar_wait(&sm.k_full[j % kKStages], (j / kKStages) & 1);
+        } else if (warp == 3 && lane == 0) {
+            // ------------------------------------------------------------ TMA producer: V_j
+            tma_prefetch_desc(&tmap_v);
+            int issued = 0;
+            for (int j = 0; j < ntile; ++j) {
+                const int st = j % kVStages;
+                if (j >= kVStages && !mbar_wait(&sm.v_empty[st], ((j / kVStages) - 1) & 1)) {
+                    atomicOr(a.err, kErrTimeout);
+                    break;
+                }
+                mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
+                tma_load_3d(sm.v[st], &tmap_v, 0, kvh, s0 + j * kBN, &sm.v_full[st]);
+                issued = j + 1;
+            }
+            for (int j = issued - kVStages < 0 ? 0 : issued - kVStages; j < issued; ++j)
+                (void)mbar_wait(&sm.v_full[j % kVStages], (j / kVStages) & 1);
+        } else if (warp == 1 && lane == 0) {
+            // ------------------------------------------------------------ S issuer: S_w = Q_w K_j^T
+            bool ok = mbar_wait(&sm.q_full, 0);
+            for (int j = 0; ok && j < ntile; ++j) {
+                const int st = j % kKStages;
+                if (!(ok = mbar_wait(&sm.k_full[st], (j / kKStages) & 1))) break;
+                const uint32_t kaddr = smem_u32(sm.k[st]);
+#pragma unroll
+                for (int w = 0; w < 2; ++w) {
+                    if (j > 0 && !(ok = mbar_wait(&sm.s_free[w], (j - 1) & 1))) break;
+                    tc_fence_after();
+                    const uint32_t qaddr = smem_u32(sm.q[w]);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc_mma_ss(tbase + kColS + 128u * w, sw128_desc(qaddr + kk * 32), sw128_desc(kaddr + kk * 32),
+                                  kIdescQK, kk > 0);
+                    tc_commit(&sm.s_full[w]);
+                }
+                if (!ok) break;
+                tc_commit(&sm.k_empty[st]);  // K_j read by both products
+            }
+            if (!ok) atomicOr(a.err, kErrTimeout);
+            tc_commit(&sm.mma_done);  // every MMA of both issuers has finished before TMEM is released
+            (void)mbar_wait(&sm.mma_done, 0);
+        } else if (warp == 2 && lane == 0) {
+            // ------------------------------------------------------------ PV issuer: O_w += P_w V_j
+            bool ok = true;
+            for (int j = 0; ok && j < ntile; ++j) {
+                const int st = j % kVStages;
+                if (!(ok = mbar_wait(&sm.v_full[st], (j / kVStages) & 1))) break;
+                const uint32_t vaddr = smem_u32(sm.v[st]);
+#pragma unroll
+                for (int w = 0; w < 2; ++w) {
+                    if (!(ok = mbar_wait(&sm.p_full[w], j & 1))) break;
+                    tc_fence_after();
+                    const uint32_t tO = tbase + kColO + 64u * w, tP = tbase + kColP + 64u * w;
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks)
+                        tc_mma_ts(tO, tP + ks * 8, sw128_desc(vaddr + ks * 2048), kIdescPV,
+                                  (j > 0 || ks > 0) ? 1u : 0u);
+                    tc_commit(&sm.o_done[w]);
+                }
+                if (!ok) break;
+                tc_commit(&sm.v_empty[st]);  // V_j read by both products
+            }
+            if (!ok) atomicOr(a.err, kErrTimeout);
+            tc_commit(&sm.mma_done);
+            (void)mbar_wait(&sm.mma_done, 0);
+        }
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
+        // ---------------------------------------------------------------- softmax warpgroups
+        const int w = (warp - 4) >> 2;  // warpgroup = which of the two heads
+        const int h = h0 + w;
+        const int r = threadIdx.x - 128 - 128 * w;
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t tS = tbase + lane_off + kColS + 128u * w;
+        const uint32_t tO = tbase + lane_off + kColO + 64u * w;
+        const uint32_t tP = tbase + lane_off + kColP + 64u * w;
+        const int qrow = row0 + r;
+        const float scale_log2 = a.scale_log2;
+        float m = __ldg(&a.sinks[h]) * kLog2e;  // running max, seeded with the sink
+        float d = 1.f;                          // e^(sink - m) = 1
+        bool ok = true;
+        for (int j = 0; j < ntile; ++j) {
+            if (!(ok = warp_wait(&sm.s_full[w], j & 1))) break;
+            tc_fence_after();
+            float s[128];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
+            tc_wait_ld();
+            tc_fence_before();
+            mbar_arrive(&sm.s_free[w]);
+
+            const int kb = j * kBN;
+            const bool masked = (kb + kBN > L) || (a.causal && kb + kBN - 1 > row0);
+            // The row max is taken on the raw scores (scale > 0) with eight independent 3-input max
+            // chains; p = exp2(s * scale_log2 - m) is then one FFMA and one MUFU per score.
+            float mul = scale_log2;
+            if (!(scale_log2 > 0.f)) {  // zero or negative scale: scale first, mask after
+#pragma unroll
+                for (int c = 0; c < 128; ++c) s[c] *= scale_log2;
+                mul = 1.f;
+            }
+            if (masked) {
+                const int lim = (a.causal ? min(L, qrow + 1) : L) - kb;  // keys kb + [0, lim) are visible
+#pragma unroll
+                for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? s[c] : kNegInf;
+            }
+            float acc[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = fmax3(s[i], s[8 + i], s[16 + i]);
+#pragma unroll
+            for (int c = 24; c < 120; c += 16)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[i] = fmax3(acc[i], s[c + i], s[c + 8 + i]);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = fmaxf(acc[i], s[120 + i]);
+            const float mx_raw = fmaxf(fmax3(acc[0], acc[1], acc[2]), fmax3(acc[3], acc[4], fmax3(acc[5], acc[6], acc[7])));
+            const float mx = mx_raw == kNegInf ? kNegInf : mx_raw * mul;
+            const float m_new = fmaxf(m, mx);
+            float factor = 1.f;
+            bool rescale_o = false;
+            if (j == 0 || m_new > m + kRescaleThreshold) {
+                factor = (m_new == kNegInf) ? 1.f : fast_exp2(m - m_new);
+                rescale_o = (j > 0);
+                m = m_new;
+                d *= factor;
+            }
+            const float neg_m = (m == kNegInf) ? 0.f : -m;
+
+            // The exp turn: warpgroup 0 goes first at every tile, warpgroup 1 after it.
+            if (w == 0 ? j > 0 : true) {
+                if (!(ok = warp_wait(&sm.turn[w], (w == 0 ? j - 1 : j) & 1))) break;
+            }
+            const float2 mul2 = make_float2(mul, mul), negm2 = make_float2(neg_m, neg_m);
+            float2 sums[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                              make_float2(0.f, 0.f)};
+            uint32_t pk[64];
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+                const float2 xx = ffma2(make_float2(s[2 * c], s[2 * c + 1]), mul2, negm2);
+                float2 pp;
+                if ((c & 7) < SINKATTN_PP_EXP_EMU) {
+                    pp = exp2_fma2(xx);
+                } else {
+                    pp.x = ex2_in_turn(xx.x);
+                    pp.y = ex2_in_turn(xx.y);
+                }
+                sums[c & 3] = fadd2(sums[c & 3], pp);
+                pk[c] = pack_bf16(pp.x, pp.y);
+            }
+            const float2 s01 = fadd2(fadd2(sums[0], sums[1]), fadd2(sums[2], sums[3]));
+            d += s01.x + s01.y;
+            // Hand the turn over once this row's exponentials are summed: d >= 0 always holds, but the
+            // test makes the arrival wait for every exp2 of the tile.
+            __syncwarp();
+            if (lane == 0 && !(d < 0.f)) mbar_arrive(&sm.turn[w ^ 1]);  // the other warpgroup's turn
+            if (j > 0) {  // P_{j-1} consumed and O_{j-1} final before P and O are touched
+                if (!(ok = warp_wait(&sm.o_done[w], (j - 1) & 1))) break;
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, rescale_o)) {
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + c * 32, o);
+                        tc_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * factor);
+                        tmem_st32(tO + c * 32, o);
+                    }
+                }
+            }
+            tmem_st32(tP, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+            tmem_st32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+            tc_wait_st();
+            tc_fence_before();
+            mbar_arrive(&sm.p_full[w]);
+        }
+        if (ok) ok = warp_wait(&sm.o_done[w], (ntile - 1) & 1);
+        if (ok) {
+            tc_fence_after();
+            uint32_t o[64];
+            tmem_ld32(tO, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
+            tmem_ld32(tO + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
+            tc_wait_ld();
+            if (qrow < L) {
+                const float inv = d > 0.f ? 1.f / d : 0.f;
+                const long long tok = (long long)s0 + qrow;
+                uint4* dst = reinterpret_cast<uint4*>(a.out + (tok * a.Hq + h) * kHeadDim);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint4 v;
+                    v.x = pack_bf16(__uint_as_float(o[8 * c + 0]) * inv, __uint_as_float(o[8 * c + 1]) * inv);
+                    v.y = pack_bf16(__uint_as_float(o[8 * c + 2]) * inv, __uint_as_float(o[8 * c + 3]) * inv);
+                    v.z = pack_bf16(__uint_as_float(o[8 * c + 4]) * inv, __uint_as_float(o[8 * c + 5]) * inv);
+                    v.w = pack_bf16(__uint_as_float(o[8 * c + 6]) * inv, __uint_as_float(o[8 * c + 7]) * inv);
+                    dst[c] = v;
+                }
+                if (a.lse) a.lse[tok * a.Hq + h] = d > 0.f ? (m + log2f(d)) * kLn2 : kNegInf;
+            }
+        } else if (lane == 0) {
+            atomicOr(a.err, kErrTimeout);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tbase, kTmemCols);
+    }
+}
+
+}  // namespace
+
+cudaError_t prefill_pp_launch(const PrefillArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                              const CUtensorMap& tv, cudaStream_t stream) {
+    if (a.G % 2 != 0) return cudaErrorInvalidValue;  // heads are taken in pairs of one KV group
+    const int kmax = (a.max_seqlen + kBM - 1) / kBM;
+    const long long tiles_ub = (long long)(a.T + kBM - 1) / kBM + a.N;
+    const long long grid = tiles_ub * (a.Hq / 2);
+    if (grid > 0x7fffffffll) return cudaErrorInvalidConfiguration;
+    const size_t smem = 1024 + sizeof(Smem) + tile_order_smem_ints(a.N, kmax) * sizeof(int);
+    static thread_local size_t set_to[64] = {};
+    static thread_local int regs_ok[64] = {};  // 0 unknown, 1 checked
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 64 || !regs_ok[dev]) {
+        // The register split (setmaxnreg) must fit in what the block is launched with.
+        cudaFuncAttributes fa;
+        if ((e = cudaFuncGetAttributes(&fa, prefill_pp_kernel)) != cudaSuccess) return e;
+        if ((long long)fa.numRegs * kThreads < 128ll * kProducerRegs + 256ll * kSoftmaxRegs)
+            return cudaErrorInvalidConfiguration;
+        if (dev < 64) regs_ok[dev] = 1;
+    }
+    if (dev >= 64 || set_to[dev] < smem) {
+        e = cudaFuncSetAttribute(prefill_pp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        if (dev < 64) set_to[dev] = smem;
+    }
+    prefill_pp_kernel<<<(unsigned)grid, kThreads, smem, stream>>>(tq, tk, tv, a);
+    return cudaGetLastError();
+}
+
+}  // namespace sinkattn
