@@ -404,11 +404,13 @@ def run_ours(args):
         value = total_flops / (ms_max * 1e-3) / 1e12
         unit = "TFLOP/s"
         achieved = flops / (ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "kernel": "prefill_tc_kernel (the only kernel of a sinkattn_prefill call)",
+        # an even query-head group runs the two-head kernel, an odd one the one-head kernel
+        kname, ksrc = (("prefill_pp_kernel", "prefill_pp.cu") if (inp.q.shape[1] // inp.k.shape[1]) % 2 == 0
+                       else ("prefill_tc_kernel", "prefill_tc.cu"))
+        roof = {"bound": "tensor", "kernel": f"{kname} (the only kernel of a sinkattn_prefill call)",
                 "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s", "frac": achieved / tc_peak,
                 "peak_source": f"{peak_src} bf16_tflops",
-                "traffic": profiled_traffic("prefill_tc_kernel", "causal_prefill",
-                                            ["prefill_tc.cu", "ptx.cuh", "kernels.h", "tile_order.cuh"])}
+                "traffic": profiled_traffic(kname, name, [ksrc, "ptx.cuh", "kernels.h", "tile_order.cuh"])}
         launches = K
         cfg_extra = {"tokens": int(inp.q.shape[0]), "flops_per_step": flops}
     # keep the GPU under the same load for >= 1.5 s of clock samples (not timed)
