@@ -98,12 +98,15 @@ def _generator(seed, device):
 
 def make_decode(B, Hq, Hkv, kv_lens, seed=0, sink_std=1.0, contiguous=False,
                 device="cpu", D=HEAD_DIM, PS=PAGE_SIZE, extra_pages=0,
-                max_pages=None) -> DecodeInputs:
+                max_pages=None, q_len=None) -> DecodeInputs:
     """Paged decode inputs.
 
     kv_lens: a list of B ints, or a (lo, hi) tuple for inclusive-uniform
     lengths.  The pool holds exactly the pages the requests need (plus
     ``extra_pages`` unused ones), in a random order unless ``contiguous``.
+    q_len: None for one query token per request (q [B, Hq, D]); an int for
+    verification inputs, q [B, q_len, Hq, D] -- the last q_len cached tokens
+    of every request (kv_lens counts them).
     """
     g = _generator(seed, device)
     if isinstance(kv_lens, tuple):
@@ -124,7 +127,7 @@ def make_decode(B, Hq, Hkv, kv_lens, seed=0, sink_std=1.0, contiguous=False,
     for b, n in enumerate(npages):
         pt[b, :n] = perm[off:off + n].to(torch.int32)
         off += n
-    q = _normal_bf16(g, (B, Hq, D), device)
+    q = _normal_bf16(g, (B, Hq, D) if q_len is None else (B, q_len, Hq, D), device)
     kp = _normal_bf16(g, (P, Hkv, PS, D), device)
     vp = _normal_bf16(g, (P, Hkv, PS, D), device)
     sinks = torch.randn(Hq, generator=g, device=device, dtype=torch.float32) * sink_std
@@ -163,6 +166,12 @@ def tiny_decode(device="cpu"):
 def batched_paged_decode(device="cpu", seed=0):
     """Batch 32, 64 q / 8 KV heads, kv_len uniform in [512, 4096], permuted pages."""
     return make_decode(32, 64, 8, (512, 4096), seed=seed, device=device)
+
+
+def speculative_verify(device="cpu", seed=0):
+    """Verification of drafts: batch 32, 4 query tokens per request (3 drafted + the last
+    accepted one), 64 q / 8 KV heads, kv_len U[512, 4096] including the 4, permuted pages."""
+    return make_decode(32, 64, 8, (512, 4096), seed=seed, device=device, q_len=4)
 
 
 def long_context_decode(device="cpu", seed=0):

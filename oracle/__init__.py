@@ -52,7 +52,8 @@ def _load():
         _lib.oracle_prefill.argtypes = [i, P, i, i, i, i, P, P, P, P, f, i, i, P, P, P]
         _lib.oracle_decode_partials.argtypes = [i, i, i, i, i, i, i, P, P, P, P, P, P, f, i, i, i, P, P]
         _lib.oracle_merge.argtypes = [i, i, i, i, P, P, P, P, P]
-        for fn in ("oracle_decode", "oracle_prefill", "oracle_decode_partials", "oracle_merge",
+        _lib.oracle_verify.argtypes = [i, i, i, i, i, i, i, i, P, P, P, P, P, P, f, i, P, P, P]
+        for fn in ("oracle_decode", "oracle_prefill", "oracle_decode_partials", "oracle_merge", "oracle_verify",
                    "oracle_num_threads"):
             getattr(_lib, fn).restype = ctypes.c_int
     return _lib
@@ -113,6 +114,32 @@ def decode(q, k_pages, v_pages, page_table, kv_lens, sinks, scale, rows=None):
                                _ptr(pt), _ptr(kl), _ptr(sk), float(scale), n, _ptr(rows),
                                _ptr(out), _ptr(lse))
     _check(rc, "oracle.decode")
+    return out, lse
+
+
+def verify(q, k_pages, v_pages, page_table, kv_lens, sinks, scale, rows=None):
+    """Verification attention over drafted tokens by definition.
+
+    q [B,q_len,Hq,D] bf16: the last q_len cached tokens of each request; token
+    i sees cache tokens 0..kv_lens[b]-q_len+i.  Other arguments as decode.
+    rows: optional (b, i, h) triples.  Returns (out float64 [B,q_len,Hq,D] or
+    [n,D], lse float64).
+    """
+    q, kp, vp = _bf16_bits(q), _bf16_bits(k_pages), _bf16_bits(v_pages)
+    pt, kl, sk = _np(page_table, np.int32), _np(kv_lens, np.int32), _np(sinks, np.float32)
+    B, QL, Hq, D = q.shape
+    P, Hkv, PS, _ = kp.shape
+    if rows is not None:
+        rows = _np(rows, np.int32).reshape(-1, 3)
+        n = rows.shape[0]
+        out, lse = np.empty((n, D)), np.empty(n)
+    else:
+        n = B * QL * Hq
+        out, lse = np.empty((B, QL, Hq, D)), np.empty((B, QL, Hq))
+    rc = _load().oracle_verify(B, QL, Hq, Hkv, D, PS, pt.shape[1], P, _ptr(q), _ptr(kp), _ptr(vp),
+                               _ptr(pt), _ptr(kl), _ptr(sk), float(scale), n, _ptr(rows),
+                               _ptr(out), _ptr(lse))
+    _check(rc, "oracle.verify")
     return out, lse
 
 

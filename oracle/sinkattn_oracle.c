@@ -151,6 +151,69 @@ int oracle_decode(int B, int Hq, int Hkv, int D, int PS, int max_pages, int num_
 }
 
 /*
+ * Verification of drafted tokens (speculative decoding): q_len query tokens per
+ * request whose keys and values are already the last q_len entries of the
+ * request's paged cache.  Source: "Accelerating Sonar through speculation"
+ * (Perplexity), sections "Speculative decoding" (the target model runs over the
+ * drafted sequence and produces logits for every drafted token) and "Inference
+ * with speculative decoding" (verification batches over the paged KV cache).
+ * Reading where the page is silent: query token i (0-based) of request b sits
+ * at cache position kv_lens[b] - q_len + i and sees cache tokens 0 .. that
+ * position -- everything before the draft plus the draft up to itself; a
+ * position below 0 leaves the key set empty.
+ *   q [B, q_len, Hq, D]; k_pages, v_pages, page_table, kv_lens, sinks as decode.
+ * rows: n_rows (b, i, h) triples, or NULL for every (b, i, h) in order.
+ * out: [n_rows, D], lse: [n_rows] (n_rows = B*q_len*Hq when rows is NULL).
+ */
+int oracle_verify(int B, int q_len, int Hq, int Hkv, int D, int PS, int max_pages, int num_pages,
+                  const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
+                  const int32_t *page_table, const int32_t *kv_lens, const float *sinks,
+                  float scale, int n_rows, const int32_t *rows, double *out, double *lse) {
+    if (B < 0 || q_len <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || D <= 0 || PS <= 0) return ORACLE_BAD_ARG;
+    const int G = Hq / Hkv;
+    const long total = rows ? n_rows : (long)B * q_len * Hq;
+    int status = ORACLE_OK;
+#pragma omp parallel
+    {
+        long cap = 0;
+        double *s = NULL;
+        const uint16_t **kp = NULL, **vp = NULL;
+#pragma omp for schedule(dynamic, 1)
+        for (long r = 0; r < total; ++r) {
+            int b = rows ? rows[3 * r] : (int)(r / ((long)q_len * Hq));
+            int i = rows ? rows[3 * r + 1] : (int)((r / Hq) % q_len);
+            int h = rows ? rows[3 * r + 2] : (int)(r % Hq);
+            int kvh = h / G;
+            long J = (long)kv_lens[b] - q_len + i + 1; /* keys 0 .. position of token i */
+            if (J < 0) J = 0;
+            if (J > cap) {
+                cap = J;
+                s = realloc(s, sizeof(double) * cap);
+                kp = realloc((void *)kp, sizeof(void *) * cap);
+                vp = realloc((void *)vp, sizeof(void *) * cap);
+            }
+            int bad = 0;
+            for (long t = 0; t < J; ++t) {
+                kp[t] = paged_row(k_pages, page_table, max_pages, num_pages, Hkv, PS, D, b, kvh, t);
+                vp[t] = paged_row(v_pages, page_table, max_pages, num_pages, Hkv, PS, D, b, kvh, t);
+                if (!kp[t]) bad = 1;
+            }
+            if (bad) {
+#pragma omp atomic write
+                status = ORACLE_BAD_PAGE;
+                continue;
+            }
+            sink_row(q + (((long)b * q_len + i) * Hq + h) * D, kp, vp, J, D, (double)sinks[h], 1,
+                     (double)scale, s, out + r * D, lse + r);
+        }
+        free(s);
+        free((void *)kp);
+        free((void *)vp);
+    }
+    return status;
+}
+
+/*
  * Prefill over packed variable-length sequences.
  *   q [T, Hq, D], k and v [T, Hkv, D]; sequence n occupies tokens
  *   cu_seqlens[n] .. cu_seqlens[n+1]-1.  causal != 0: row i sees keys

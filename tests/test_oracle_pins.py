@@ -327,3 +327,71 @@ def test_row_selection_matches_full_result():
     for i, (t, h) in enumerate(rows):
         np.testing.assert_array_equal(o[i], out[t, h])
         assert l[i] == lse[t, h]
+
+
+# ---- verification of drafted tokens (speculative decoding)
+
+def test_verify_rows_equal_decode_over_their_prefix():
+    """Token i of a q_len draft is a decode over cache tokens 0..kv_len-q_len+i."""
+    QL = 3
+    inp = W.make_decode(3, 8, 2, [5, 40, 33], seed=21, q_len=QL)
+    out, lse = oracle.verify(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens, inp.sinks, inp.scale)
+    for i in range(QL):
+        lens = (inp.kv_lens - QL + i + 1).clamp(min=0)
+        ro, rl = oracle.decode(inp.q[:, i].contiguous(), inp.k_pages, inp.v_pages, inp.page_table, lens, inp.sinks,
+                               inp.scale)
+        assert np.abs(out[:, i] - ro).max() <= TOL
+        assert np.abs(lse[:, i] - rl).max() <= TOL
+
+
+def test_verify_equals_causal_prefill_tail():
+    """On a contiguous cache holding a whole sequence, the draft rows are the last rows of its causal prefill."""
+    QL, L, Hq, Hkv = 4, 37, 8, 2
+    pre = W.make_prefill(Hq, Hkv, [L], seed=22)
+    po, pl = oracle.prefill(pre.q, pre.k, pre.v, pre.cu_seqlens, pre.sinks, pre.scale, True)
+    npg = (L + W.PAGE_SIZE - 1) // W.PAGE_SIZE
+    kp = torch.zeros(npg * W.PAGE_SIZE, Hkv, 64, dtype=torch.bfloat16)
+    vp = torch.zeros_like(kp)
+    kp[:L], vp[:L] = pre.k, pre.v
+    kp = kp.view(npg, W.PAGE_SIZE, Hkv, 64).permute(0, 2, 1, 3).contiguous()
+    vp = vp.view(npg, W.PAGE_SIZE, Hkv, 64).permute(0, 2, 1, 3).contiguous()
+    pt = torch.arange(npg, dtype=torch.int32).view(1, npg)
+    q = pre.q[L - QL:].unsqueeze(0).contiguous()  # [1, QL, Hq, D]
+    out, lse = oracle.verify(q, kp, vp, pt, torch.tensor([L], dtype=torch.int32), pre.sinks, pre.scale)
+    assert np.abs(out[0] - po[L - QL:]).max() <= TOL
+    assert np.abs(lse[0] - pl[L - QL:]).max() <= TOL
+
+
+def test_verify_brute_force_tiny():
+    """Two drafted tokens over a 3-token cache, by explicit enumeration of each row's key set."""
+    inp = W.make_decode(1, 2, 1, [3], seed=23, q_len=2)
+    out, lse = oracle.verify(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens, inp.sinks, inp.scale)
+    k, v = gather_kv(inp, 0, 0)
+    for i, visible in ((0, 2), (1, 3)):  # token 0 sits at position 1, token 1 at position 2
+        for h in range(2):
+            qv = inp.q[0, i, h].double()
+            logits = [inp.scale * float(qv @ k[j]) for j in range(visible)] + [float(inp.sinks[h])]
+            m = max(logits)
+            w = [math.exp(x - m) for x in logits]
+            z = sum(w)
+            ref = sum(w[j] / z * v[j].numpy() for j in range(visible))
+            assert np.abs(out[0, i, h] - ref).max() <= TOL
+            assert abs(lse[0, i, h] - (m + math.log(z))) <= TOL
+
+
+def test_verify_short_cache_rows_fall_on_the_sink():
+    """A cache shorter than the draft leaves the earliest rows without keys: out 0, lse = sink."""
+    inp = W.make_decode(1, 4, 2, [2], seed=24, q_len=4)
+    out, lse = oracle.verify(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens, inp.sinks, inp.scale)
+    assert np.all(out[0, :2] == 0.0)
+    assert np.abs(lse[0, :2] - inp.sinks.double().numpy()[None]).max() == 0.0
+    assert np.all(np.abs(out[0, 2:]).max(axis=-1) > 0)
+
+
+def test_verify_row_selection_matches_full_result():
+    inp = W.make_decode(2, 8, 2, [20, 50], seed=25, q_len=3)
+    out, lse = oracle.verify(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens, inp.sinks, inp.scale)
+    rows = np.array([[1, 2, 7], [0, 0, 3], [1, 0, 0]], dtype=np.int32)
+    so, sl = oracle.verify(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens, inp.sinks, inp.scale, rows=rows)
+    for n, (b, i, h) in enumerate(rows):
+        assert np.array_equal(so[n], out[b, i, h]) and sl[n] == lse[b, i, h]

@@ -39,3 +39,14 @@ def test_prefill_shape():
     assert cu[0] == 0 and len(cu) == 6 and cu[-1] == p.q.shape[0]
     assert all(3 <= L <= 40 for L in p.seqlens)
     assert p.visible_pairs() == sum(L * (L + 1) // 2 for L in p.seqlens)
+
+
+def test_speculative_verify_shape():
+    d = W.speculative_verify()
+    lens = d.kv_lens.tolist()
+    assert d.q.shape == (32, 4, 64, 64) and len(lens) == 32 and all(512 <= L <= 4096 for L in lens)
+    npg = [(L + 15) // 16 for L in lens]
+    assert d.k_pages.shape == (sum(npg), 8, 16, 64)
+    # the same lengths and pool as the one-token workload: only q differs in size
+    b = W.batched_paged_decode()
+    assert lens == b.kv_lens.tolist() and torch.equal(d.page_table, b.page_table)
