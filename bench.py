@@ -2,15 +2,15 @@
 """Benchmark of libsinkattn (sink attention, GQA, paged split-KV decode + causal prefill).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload batched_paged_decode|long_context_decode|causal_prefill]
+                    [--workload batched_paged_decode|long_context_decode|speculative_verify|causal_prefill]
 
 Headline: decode KV GB/s on the batched paged decode workload (batch 32,
 64 q / 8 KV heads, head_dim 64, kv_len uniform in [512, 4096], 16-token pages
 randomly permuted in the pool).  One step = one sinkattn_decode call (split
 pass + merge), i.e. the whole decode hot path, on inputs resident in HBM.
 The L2 is flushed (256 MiB write, then a 512 MiB read) before every timed step.  Secondary lines
-for the long-context split-KV decode, the causal prefill and the mixed
-serving batch ride in the same JSON object under "secondary".
+for the long-context split-KV decode, the verification of drafted tokens (4 per request), the
+causal prefill and the mixed serving batch ride in the same JSON object under "secondary".
 
 Prints ONE JSON line on rank 0.  Under torchrun every rank runs its own
 independent batch (weak scaling, no collective on the data path); the
@@ -47,6 +47,8 @@ WORKLOAD_TEXT = {
     "long_context_decode": "long-context split-KV decode: batch 4, 64 q / 8 KV heads, head_dim 64, kv_len 131072, "
                            "32 chunks per request merged by LSE",
     "causal_prefill": "causal prefill: 2 x 8192 tokens (varlen), 64 q / 8 KV heads, head_dim 64",
+    "speculative_verify": "verification of drafts: batch 32, 4 query tokens per request over the paged cache, "
+                          "64 q / 8 KV heads, head_dim 64, kv_len U[512,4096] (drafts included), permuted pages",
     "mixed_serving": "mixed serving batch: 8 causal prefills L~U[256,4096] + 256 paged decodes kv_len~U[1024,32768], "
                      "64 q / 8 KV heads, two streams",
 }
@@ -248,6 +250,27 @@ def bench_decode(S, W, name, rank, K, warmup, flush, stream, num_workers=0):
     return inp, step, times, decode_bytes(inp.kv_lens, Hkv, D)
 
 
+def bench_verify(S, W, rank, K, warmup, flush, stream):
+    inp = W.speculative_verify(device="cuda", seed=rank)
+    B, QL, Hq, D = inp.q.shape
+    Hkv = inp.k_pages.shape[1]
+    ws = torch.empty(S.sinkattn_verify_workspace_size(inp.q, inp.k_pages, inp.page_table), dtype=torch.uint8,
+                     device="cuda")
+    out = torch.empty_like(inp.q)
+    lse = torch.empty(B, QL, Hq, dtype=torch.float32, device="cuda")
+
+    def step():
+        S.sinkattn_verify(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens, inp.sinks, inp.scale,
+                          out=out, lse=lse, workspace=ws, stream=stream)
+
+    with torch.cuda.stream(stream):
+        times = timed_steps(step, K, warmup, flush, stream)
+    err = S.sinkattn_get_error(stream)
+    if err:
+        raise RuntimeError(f"device error {S.status_string(err)}")
+    return inp, step, times, decode_bytes(inp.kv_lens, Hkv, D)
+
+
 def bench_prefill(S, W, name, rank, K, warmup, flush, stream):
     inp = (W.mixed_serving_prefill if name == "mixed_serving" else W.causal_prefill)(device="cuda", seed=rank)
     out = torch.empty_like(inp.q)
@@ -272,20 +295,25 @@ def cpu_baseline_decode(inp, budget_s=12.0):
 
     q, kp, vp = inp.q.cpu(), inp.k_pages.cpu(), inp.v_pages.cpu()
     pt, kl, sk = inp.page_table.cpu(), inp.kv_lens.cpu(), inp.sinks.cpu()
-    B, Hq, _ = q.shape
+    B, Hq = q.shape[0], q.shape[-2]
+    QL = q.shape[1] if q.dim() == 4 else 1  # verification inputs carry q_len query tokens per request
     Hkv = kp.shape[1]
     done_bytes, reqs = 0, 0
     t0 = time.perf_counter()
     b = 0
     while time.perf_counter() - t0 < budget_s:
-        rows = torch.stack([torch.full((Hq,), b % B, dtype=torch.int32), torch.arange(Hq, dtype=torch.int32)], 1)
-        oracle.decode(q, kp, vp, pt, kl, sk, inp.scale, rows=rows.numpy())
+        if q.dim() == 4:
+            rows = torch.tensor([[b % B, i, h] for i in range(QL) for h in range(Hq)], dtype=torch.int32)
+            oracle.verify(q, kp, vp, pt, kl, sk, inp.scale, rows=rows.numpy())
+        else:
+            rows = torch.stack([torch.full((Hq,), b % B, dtype=torch.int32), torch.arange(Hq, dtype=torch.int32)], 1)
+            oracle.decode(q, kp, vp, pt, kl, sk, inp.scale, rows=rows.numpy())
         done_bytes += int(kl[b % B]) * Hkv * 64 * 4
         reqs += 1
         b += 1
     dt = time.perf_counter() - t0
     return {"value": done_bytes / dt / 1e9, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{reqs} whole requests (all {Hq} heads) of the same workload, fp64, {dt:.1f} s"}
+            "sample": f"{reqs} whole requests (all {QL} x {Hq} query rows) of the same workload, fp64, {dt:.1f} s"}
 
 
 def cpu_baseline_prefill(inp, budget_s=8.0):
@@ -377,9 +405,12 @@ def run_ours(args):
     barrier(world)
     torch.cuda.synchronize()
     t_load0 = time.time()
-    if name in ("batched_paged_decode", "long_context_decode", "tiny_decode"):
+    if name in ("batched_paged_decode", "long_context_decode", "tiny_decode", "speculative_verify"):
         workers = 0
-        inp, step, times, nbytes = bench_decode(S, W, name, rank, K, Wu, flush, stream, workers)
+        if name == "speculative_verify":
+            inp, step, times, nbytes = bench_verify(S, W, rank, K, Wu, flush, stream)
+        else:
+            inp, step, times, nbytes = bench_decode(S, W, name, rank, K, Wu, flush, stream, workers)
         ms = statistics.mean(times)
         torch.cuda.synchronize()
         barrier(world)
@@ -388,11 +419,13 @@ def run_ours(args):
         value = total_bytes / (ms_max * 1e-3) / 1e9
         unit = "GB/s"
         achieved = nbytes / (ms * 1e-3) / 1e9
-        roof = {"bound": "hbm", "kernel": "decode_split_kernel (the only kernel of a sinkattn_decode call)",
+        kname, ksrc, call = (("verify_split_kernel", "verify.cu", "sinkattn_verify") if name == "speculative_verify"
+                             else ("decode_split_kernel", "decode.cu", "sinkattn_decode"))
+        roof = {"bound": "hbm", "kernel": f"{kname} (the only kernel of a {call} call)",
                 "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                 "peak_source": f"{peak_src} hbm_gbs",
-                "traffic": profiled_traffic("decode_split_kernel", name, ["decode.cu", "ptx.cuh", "kernels.h"])}
-        launches = K  # one decode_split_kernel per step
+                "traffic": profiled_traffic(kname, name, [ksrc, "ptx.cuh", "kernels.h", "split_kv.cuh"])}
+        launches = K  # one split kernel per step
         cfg_extra = {"kv_tokens": int(inp.kv_lens.sum()), "kv_bytes_per_step": nbytes}
     else:
         inp, step, times, flops = bench_prefill(S, W, name, rank, K, Wu, flush, stream)
@@ -453,19 +486,21 @@ def run_ours(args):
         h_pt = inp.page_table.cpu().pin_memory()
         h_kl = inp.kv_lens.cpu().pin_memory()
         h_out = torch.empty(inp.q.shape, dtype=torch.bfloat16).pin_memory()
-        h_lse = torch.empty(inp.q.shape[:2], dtype=torch.float32).pin_memory()
+        h_lse = torch.empty(inp.q.shape[:-1], dtype=torch.float32).pin_memory()
         d_q, d_pt, d_kl = torch.empty_like(inp.q), torch.empty_like(inp.page_table), torch.empty_like(inp.kv_lens)
-        ws = torch.empty(S.sinkattn_decode_workspace_size(inp.q, inp.k_pages, inp.page_table), dtype=torch.uint8,
-                         device="cuda")
+        verify = name == "speculative_verify"
+        ws_size = S.sinkattn_verify_workspace_size if verify else S.sinkattn_decode_workspace_size
+        api = S.sinkattn_verify if verify else S.sinkattn_decode
+        ws = torch.empty(ws_size(inp.q, inp.k_pages, inp.page_table), dtype=torch.uint8, device="cuda")
         d_out = torch.empty_like(inp.q)
-        d_lse = torch.empty(inp.q.shape[:2], dtype=torch.float32, device="cuda")
+        d_lse = torch.empty(inp.q.shape[:-1], dtype=torch.float32, device="cuda")
 
         def e2e_step():
             d_q.copy_(h_q, non_blocking=True)
             d_pt.copy_(h_pt, non_blocking=True)
             d_kl.copy_(h_kl, non_blocking=True)
-            S.sinkattn_decode(d_q, inp.k_pages, inp.v_pages, d_pt, d_kl, inp.sinks, inp.scale, out=d_out, lse=d_lse,
-                              workspace=ws, stream=stream)
+            api(d_q, inp.k_pages, inp.v_pages, d_pt, d_kl, inp.sinks, inp.scale, out=d_out, lse=d_lse, workspace=ws,
+                stream=stream)
             h_out.copy_(d_out, non_blocking=True)
             h_lse.copy_(d_lse, non_blocking=True)
 
@@ -490,8 +525,15 @@ def run_ours(args):
             secondary.append({"workload": WORKLOAD_TEXT["long_context_decode"], "value": lb / (lms * 1e-3) / 1e9,
                               "unit": "GB/s", "ms_per_step": lms, "frac_of_hbm_peak": lb / (lms * 1e-3) / 1e9 / hbm_peak,
                               "traffic": profiled_traffic("decode_split_kernel", "long_context_decode",
-                                                          ["decode.cu", "ptx.cuh", "kernels.h"])})
+                                                          ["decode.cu", "ptx.cuh", "kernels.h", "split_kv.cuh"])})
             del li
+            vi, _, vt, vb = bench_verify(S, W, rank, Ks, Wu, flush, stream)
+            vms = statistics.mean(vt)
+            secondary.append({"workload": WORKLOAD_TEXT["speculative_verify"], "value": vb / (vms * 1e-3) / 1e9,
+                              "unit": "GB/s", "ms_per_step": vms, "frac_of_hbm_peak": vb / (vms * 1e-3) / 1e9 / hbm_peak,
+                              "traffic": profiled_traffic("verify_split_kernel", "speculative_verify",
+                                                          ["verify.cu", "ptx.cuh", "kernels.h", "split_kv.cuh"])})
+            del vi
             pi, _, pt_, pf = bench_prefill(S, W, "causal_prefill", rank, Ks, Wu, flush, stream)
             pms = statistics.mean(pt_)
             secondary.append({"workload": WORKLOAD_TEXT["causal_prefill"], "value": pf / (pms * 1e-3) / 1e12,
@@ -565,7 +607,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="batched_paged_decode",
-                    choices=["batched_paged_decode", "long_context_decode", "tiny_decode", "causal_prefill"])
+                    choices=["batched_paged_decode", "long_context_decode", "tiny_decode", "speculative_verify",
+                             "causal_prefill"])
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernels-only", action="store_true",

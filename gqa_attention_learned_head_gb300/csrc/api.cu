@@ -124,6 +124,17 @@ sinkattn_status_t check_decode_dims(const sinkattn_decode_dims_t* d) {
     return SINKATTN_OK;
 }
 
+sinkattn_status_t check_verify_dims(const sinkattn_verify_dims_t* d) {
+    if (!d) return SINKATTN_ERR_INVALID_ARG;
+    const sinkattn_decode_dims_t dd = {d->batch,     d->num_q_heads, d->num_kv_heads, d->head_dim,  d->page_size,
+                                       d->num_pages, d->max_pages,   d->num_workers};
+    const sinkattn_status_t st = check_decode_dims(&dd);
+    if (st != SINKATTN_OK) return st;
+    if (d->q_len < 1) return SINKATTN_ERR_INVALID_ARG;
+    if (d->q_len > 16 || d->q_len * (d->num_q_heads / d->num_kv_heads) > kVerifyMaxRows) return SINKATTN_ERR_UNSUPPORTED;
+    return SINKATTN_OK;
+}
+
 }  // namespace
 }  // namespace sinkattn
 
@@ -210,6 +221,76 @@ sinkattn_status_t sinkattn_decode(const void* q, const void* k_pages, const void
     a.fixed_workers = dims->num_workers > 0 ? 1 : 0;
     a.scale_log2 = scale * 1.4426950408889634f;
     return decode_launch(a, plan, tk, tv, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SINKATTN_OK
+                                                                                            : SINKATTN_ERR_CUDA;
+}
+
+size_t sinkattn_verify_workspace_size(const sinkattn_verify_dims_t* dims) {
+    if (check_verify_dims(dims) != SINKATTN_OK) return 0;
+    VerifyPlan plan;
+    if (verify_plan(dims->batch, dims->q_len, dims->num_q_heads, dims->num_kv_heads, dims->num_workers, &plan) !=
+        cudaSuccess)
+        return 0;
+    return plan.ws_bytes;
+}
+
+sinkattn_status_t sinkattn_verify(const void* q, const void* k_pages, const void* v_pages, const int32_t* page_table,
+                                  const int32_t* kv_lens, const float* sinks, float scale, void* out, float* lse,
+                                  const sinkattn_verify_dims_t* dims, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
+    sinkattn_status_t st = check_verify_dims(dims);
+    if (st != SINKATTN_OK) return st;
+    if (dims->batch == 0) return SINKATTN_OK;
+    if (!q || !page_table || !kv_lens || !sinks || !out) return SINKATTN_ERR_INVALID_ARG;
+    if (dims->num_pages > 0 && (!k_pages || !v_pages)) return SINKATTN_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(out, 16) ||
+        !aligned(page_table, 4) || !aligned(kv_lens, 4) || !aligned(sinks, 4) || (lse && !aligned(lse, 4)))
+        return SINKATTN_ERR_INVALID_ARG;
+    if (!(scale == scale)) return SINKATTN_ERR_INVALID_ARG;
+    DeviceState* ds = nullptr;
+    if ((st = device_state(&ds)) != SINKATTN_OK) return st;
+    VerifyPlan plan;
+    if (verify_plan(dims->batch, dims->q_len, dims->num_q_heads, dims->num_kv_heads, dims->num_workers, &plan) !=
+        cudaSuccess)
+        return SINKATTN_ERR_CUDA;
+    if (!workspace || workspace_bytes < plan.ws_bytes || !aligned(workspace, 256)) return SINKATTN_ERR_WORKSPACE;
+
+    const int Hkv = dims->num_kv_heads, G = dims->num_q_heads / Hkv;
+    // With an empty pool every page id is out of range, so no copy is ever issued
+    // and the (zeroed) maps are never read.
+    CUtensorMap tk, tv;
+    std::memset(&tk, 0, sizeof tk);
+    std::memset(&tv, 0, sizeof tv);
+    const unsigned long long rows = (unsigned long long)dims->num_pages * Hkv * kPageSize;
+    if (rows > 0 &&
+        (!encode_rows(&tk, k_pages, rows, 128, kPageSize) || !encode_rows(&tv, v_pages, rows, 128, kPageSize)))
+        return SINKATTN_ERR_INVALID_ARG;
+
+    VerifyArgs a;
+    a.q = static_cast<const __nv_bfloat16*>(q);
+    a.page_table = page_table;
+    a.kv_lens = kv_lens;
+    a.sinks = sinks;
+    a.out = static_cast<__nv_bfloat16*>(out);
+    a.lse = lse;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    a.part_o = reinterpret_cast<float*>(ws);
+    a.part_lse = a.part_o + plan.slots * (size_t)dims->q_len * G * kHeadDim;
+    a.counters = reinterpret_cast<unsigned long long*>(ws + plan.counters_offset);
+    a.epoch = next_epoch();
+    a.err = ds->err;
+    a.B = dims->batch;
+    a.QL = dims->q_len;
+    a.Hq = dims->num_q_heads;
+    a.Hkv = Hkv;
+    a.G = G;
+    a.R = dims->q_len * G;
+    a.num_pages = dims->num_pages;
+    a.max_pages = dims->max_pages;
+    a.workers = plan.grid;
+    a.min_pages_per_worker = 0;  // set by the launcher
+    a.fixed_workers = dims->num_workers > 0 ? 1 : 0;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    return verify_launch(a, plan, tk, tv, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SINKATTN_OK
                                                                                             : SINKATTN_ERR_CUDA;
 }
 

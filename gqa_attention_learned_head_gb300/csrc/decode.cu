@@ -39,6 +39,7 @@
 //    movmatrix; O^T[64 x 8] += V^T * P^T.  Everything stays in registers.
 #include "kernels.h"
 #include "ptx.cuh"
+#include "split_kv.cuh"
 
 #ifndef SINKATTN_DECODE_STAGES
 #define SINKATTN_DECODE_STAGES 2
@@ -61,7 +62,6 @@ constexpr int kMaxMerge = 2;  // a share completes at most its first and its las
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kNegInf = -__builtin_huge_valf();
-constexpr int kCountBits = 24;  // low bits of a segment counter: arrivals; high bits: call epoch
 
 // Shared memory: ring | mbarriers | bad-page flags | combine area | merge queue | prefix[B+1].
 template <int NT>
@@ -79,20 +79,14 @@ struct SmemLayout {
     static constexpr size_t fixed = prefix + 1024 /* alignment slack */;
 };
 
-__device__ __forceinline__ int clamp_len(int L, int cap) { return L < 0 ? 0 : (L > cap ? cap : L); }
-
 __device__ __forceinline__ uint32_t ld_u32(const __nv_bfloat16* p) {
     return __ldg(reinterpret_cast<const unsigned int*>(p));
 }
 
 __device__ __forceinline__ void cta_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory"); }
 
-// One piece of a CTA's share: units [ps, pe) of segment (b, g) whose first unit is seg_start.
-struct Piece {
-    long long ps, pe, seg_start;
-    int b, g, n, idx;
-    __device__ int len() const { return (int)(pe - ps); }
-    __device__ int page0() const { return (int)(ps - seg_start); }
+// A piece as the decode processes it: one of >= kWarps pages is spread over the warps page by page.
+struct Piece : SegPiece {
     __device__ bool split() const { return len() >= kWarps; }
     // Units of this piece that warp w processes, and the page of its t-th one.
     __device__ int count(int w) const {
@@ -101,83 +95,6 @@ struct Piece {
     }
     __device__ int page(int w, int t) const { return page0() + (split() ? w + t * kWarps : t); }
 };
-
-__device__ __forceinline__ void piece_first(Piece& p, const int* prefix, int B, int Hkv, long long x0, long long x1) {
-    int lo = 0, hi = B - 1;  // smallest b with prefix[b+1]*Hkv > x0
-    while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if ((long long)prefix[mid + 1] * Hkv > x0) hi = mid;
-        else lo = mid + 1;
-    }
-    p.b = lo;
-    p.n = prefix[lo + 1] - prefix[lo];
-    const long long off = x0 - (long long)prefix[lo] * Hkv;
-    p.g = (int)(off / p.n);
-    p.seg_start = (long long)prefix[lo] * Hkv + (long long)p.g * p.n;
-    p.ps = x0;
-    p.pe = min(x1, p.seg_start + p.n);
-    p.idx = 0;
-}
-
-// Moves to the next piece; p.ps >= x1 afterwards means the share is done.
-__device__ __forceinline__ void piece_next(Piece& p, const int* prefix, int B, int Hkv, long long x1) {
-    p.ps = p.pe;
-    ++p.idx;
-    if (p.ps >= x1) return;
-    p.seg_start = p.pe;  // a piece that ends before x1 ends at its segment's end
-    if (++p.g == Hkv) {
-        p.g = 0;
-        do { ++p.b; } while (p.b < B && prefix[p.b + 1] == prefix[p.b]);
-        p.n = prefix[p.b + 1] - prefix[p.b];
-    }
-    p.pe = min(x1, p.seg_start + p.n);
-}
-
-// CTA count actually used for U units (identical in every CTA).
-__device__ __forceinline__ long long effective_shares(const DecodeArgs& a, long long U) {
-    long long c = a.workers;
-    if (!a.fixed_workers) {
-        const long long want = (U + a.min_pages_per_worker - 1) / a.min_pages_per_worker;
-        if (want < c) c = want;
-    }
-    if (c > U) c = U;
-    return c < 1 ? 1 : c;
-}
-
-__device__ __forceinline__ unsigned long long cas_acq_rel(unsigned long long* p, unsigned long long cmp,
-                                                          unsigned long long val) {
-    unsigned long long old;
-    asm volatile("atom.acq_rel.gpu.global.cas.b64 %0, [%1], %2, %3;" : "=l"(old) : "l"(p), "l"(cmp), "l"(val)
-                 : "memory");
-    return old;
-}
-
-// Records one more finished piece of a segment; true for the piece that completes it.  The
-// compare-and-swap has release semantics (this CTA's partials, ordered before it by the CTA
-// barrier, become visible first) and acquire semantics (the other pieces' partials are visible
-// to the merge that follows).  The first attempt guesses that this is the last arrival, so the
-// arrival that completes a segment -- the one on the critical path -- needs one round trip.
-__device__ __forceinline__ bool arrive_last(unsigned long long* ctr, unsigned long long epoch, int pieces) {
-    unsigned long long old = (epoch << kCountBits) | (unsigned long long)(pieces - 1), nw;
-    while (true) {
-        nw = ((old >> kCountBits) == epoch) ? old + 1 : ((epoch << kCountBits) | 1ull);
-        const unsigned long long prev = cas_acq_rel(ctr, old, nw);
-        if (prev == old) break;
-        old = prev;
-    }
-    const bool last = (int)(nw & ((1ull << kCountBits) - 1)) == pieces;
-    // epoch 0 is never used: the next call starts afresh (no arrival can follow the last one)
-    if (last) *reinterpret_cast<volatile unsigned long long*>(ctr) = 0ull;
-    return last;
-}
-
-// Shares (CTAs) that hold units of segment seg: first share and count.
-__device__ __forceinline__ void segment_pieces(long long seg_start, int n, long long C, long long U, long long& c_first,
-                                               int& pieces) {
-    c_first = ((seg_start + 1) * C - 1) / U;
-    const long long c_last = ((seg_start + n) * C - 1) / U;
-    pieces = (int)(c_last - c_first + 1);
-}
 
 // Log-sum-exp merge of one head of one segment from its partials (base-2 lse), by 16 lanes:
 // lane l of the half-warp owns head-dims 4l..4l+3.  Pieces are taken 8 at a time with all loads
@@ -301,7 +218,7 @@ __global__ void __launch_bounds__(kWarps * 32, SINKATTN_DECODE_MIN_BLOCKS) decod
 
     const long long U = (long long)running * Hkv;
     if (U == 0) return;
-    const long long C = effective_shares(a, U);
+    const long long C = effective_shares(a.workers, a.fixed_workers, a.min_pages_per_worker, U);
     const long long cta = blockIdx.x;
     if (cta >= C) return;
     const long long x0 = cta * U / C, x1 = (cta + 1) * U / C;

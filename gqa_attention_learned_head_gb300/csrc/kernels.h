@@ -47,6 +47,32 @@ cudaError_t decode_plan(int B, int Hq, int Hkv, int num_workers, DecodePlan* pla
 cudaError_t decode_launch(const DecodeArgs& args, const DecodePlan& plan, const CUtensorMap& tmap_k,
                           const CUtensorMap& tmap_v, cudaStream_t stream);
 
+// ------------------------------------------------------------------ draft verification
+constexpr int kVerifyMaxRows = 64;  // q_len * G query rows of one (request, KV head)
+struct VerifyArgs {
+    const __nv_bfloat16* q;     // [B, QL, Hq, 64]
+    const int32_t* page_table;  // [B, max_pages]
+    const int32_t* kv_lens;     // [B], counting the QL drafted tokens
+    const float* sinks;         // [Hq]
+    __nv_bfloat16* out;         // [B, QL, Hq, 64]
+    float* lse;                 // [B, QL, Hq] or null
+    float* part_o;              // [slots, R, 64]
+    float* part_lse;            // [slots, R], base-2 log-sum-exp
+    unsigned long long* counters;  // [B*Hkv]: (call epoch << 24) | pieces arrived
+    unsigned long long epoch;      // this call's epoch, in [1, 2^40)
+    unsigned* err;
+    int B, QL, Hq, Hkv, G, R, num_pages, max_pages;  // R = QL * G rows per segment
+    int workers, min_pages_per_worker, fixed_workers;
+    float scale_log2;
+};
+struct VerifyPlan {
+    int grid, warps, stages;
+    size_t smem, slots, counters_offset, ws_bytes;
+};
+cudaError_t verify_plan(int B, int QL, int Hq, int Hkv, int num_workers, VerifyPlan* plan);
+cudaError_t verify_launch(const VerifyArgs& args, const VerifyPlan& plan, const CUtensorMap& tmap_k,
+                          const CUtensorMap& tmap_v, cudaStream_t stream);
+
 // ------------------------------------------------------------------ merge
 struct MergeArgs {
     const float* part_o;    // [S, R, H, 64]

@@ -1,0 +1,575 @@
+// verify.cu -- attention of drafted tokens over the paged cache (verification
+// in speculative decoding), with a per-head learned sink.
+//
+// Source: "Accelerating Sonar through speculation" (Perplexity), sections
+// "Speculative decoding" (the target model runs over the drafted tokens and
+// produces logits for every one of them, so up to n + 1 tokens come out of one
+// step) and "Inference with speculative decoding" (verification batches over
+// the paged KV cache); the attention itself is the sink attention of "GPT-OSS
+// on day 0", section "Kernels for GPT-OSS / Sink Attention".  Query token i of
+// request b is the cache token at position kv_len - q_len + i (its K and V are
+// already in the pages) and sees cache tokens 0 .. that position.
+//
+// GB300 design: the decode's work split (split_kv.cuh: contiguous per-CTA
+// shares of (request, KV head, page) units, pieces, merge in the same launch),
+// but the R = q_len x G query rows of a (request, KV head) go through ONE pass
+// over its pages, so the draft costs the cache bytes once:
+//  * consumer warp w < W owns rows 8w .. 8w+7 (row r = i * G + head within the
+//    group); all consumer warps read every page of the share from one CTA ring
+//    of 3W + 1 stages, which a producer warp (warp W) fills by TMA (K and V
+//    slices of one (page, KV head), 128-byte swizzle) as soon as every consumer
+//    has released a stage.  The producer is a warp of its own so that its
+//    waits -- for the slowest consumer, for page ids, for a TMA issue slot --
+//    never hold up the products;
+//  * per warp and page the products are the decode's: S^T[16 tokens x 8 rows]
+//    = K Q^T and O^T[64 x 8] += V^T P^T with mma.m16n8k16, online softmax in
+//    registers, each row masked at its own causal limit;
+//  * no combine between warps (they own different rows); a piece that is not
+//    a whole segment writes fp32 partials per row and the CTA completing the
+//    segment merges them by log-sum-exp.
+// Every wait is bounded; a wait that gives up sets the device error word.
+#include <climits>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "split_kv.cuh"
+
+namespace sinkattn {
+namespace {
+
+constexpr int kSliceBytes = kPageSize * kHeadDim * 2;  // 2048: one (page, KV head) of K or V
+constexpr int kStageBytes = 2 * kSliceBytes;
+constexpr int kMinPages = 32;  // automatic mode: never cut shares finer than this
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kNegInf = -__builtin_huge_valf();
+
+// Shared memory: ring | full / empty barriers | bad-page flags | misc | pend | queue | prefix[B+1].
+struct Layout {
+    size_t ring, full, empty, bad, misc, pend, queue, prefix, total;
+    __host__ __device__ Layout(int stages, int B) {
+        ring = 0;
+        full = size_t(stages) * kStageBytes;
+        empty = full + size_t(stages) * 8;
+        bad = empty + size_t(stages) * 8;
+        misc = bad + size_t(stages) * 4;  // [0..8] scan scratch, [12] merge queue count, [13] pend count
+        pend = misc + 16 * 4;
+        queue = pend + 2 * 4;
+        prefix = queue + 2 * 4;
+        total = prefix + size_t(B + 1) * 4 + 1024 /* alignment slack */;
+    }
+};
+
+__device__ __forceinline__ uint32_t ld_u32(const __nv_bfloat16* p) {
+    return __ldg(reinterpret_cast<const unsigned int*>(p));
+}
+
+// Keeps the bf16 halves of x whose token (lo: t, hi: t + 1) lies below `valid`.
+__device__ __forceinline__ uint32_t keep_tokens(uint32_t x, int t, int valid) {
+    return x & ((t < valid ? 0x0000FFFFu : 0u) | (t + 1 < valid ? 0xFFFF0000u : 0u));
+}
+
+// Log-sum-exp merge of one query row of one segment from its partials (base-2 lse), by 16
+// lanes: lane l of the half-warp owns head-dims 4l..4l+3.  Pieces are taken 8 at a time with
+// all loads issued together and combined online.
+__device__ __forceinline__ void merge_row(const VerifyArgs& a, int b, int g, int r, long long slot0, int pieces,
+                                          int hl) {
+    constexpr int kChunk = 8;
+    const int R = a.R;
+    const float* lp = a.part_lse + slot0 * R + r;
+    const float* op = a.part_o + (slot0 * R + r) * kHeadDim + 4 * hl;
+    float M = kNegInf, sum = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c0 = 0; c0 < pieces; c0 += kChunk) {
+        float l[kChunk];
+        float4 v[kChunk];
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i) {
+            const bool in = c0 + i < pieces;
+            l[i] = in ? __ldcg(lp + (long long)(c0 + i) * R) : kNegInf;
+            v[i] = in ? __ldcg(reinterpret_cast<const float4*>(op + (long long)(c0 + i) * R * kHeadDim))
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float Mc = M;
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i) Mc = fmaxf(Mc, l[i]);
+        if (Mc == kNegInf) continue;
+        const float rs = M == kNegInf ? 0.f : exp2f(M - Mc);
+        sum *= rs;
+        o.x *= rs;
+        o.y *= rs;
+        o.z *= rs;
+        o.w *= rs;
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i) {
+            const float w = l[i] == kNegInf ? 0.f : exp2f(l[i] - Mc);
+            sum += w;
+            o.x += w * v[i].x;
+            o.y += w * v[i].y;
+            o.z += w * v[i].z;
+            o.w += w * v[i].w;
+        }
+        M = Mc;
+    }
+    const int i = r / a.G, h = g * a.G + r % a.G;
+    const long long row = ((long long)b * a.QL + i) * a.Hq + h;
+    uint2* dst = reinterpret_cast<uint2*>(a.out + row * kHeadDim) + hl;
+    if (M == kNegInf) {  // no live key and no finite sink in any piece
+        *dst = make_uint2(0u, 0u);
+        if (hl == 0 && a.lse) a.lse[row] = kNegInf;
+        return;
+    }
+    const float inv = 1.f / sum;
+    *dst = make_uint2(pack_bf16(o.x * inv, o.y * inv), pack_bf16(o.z * inv, o.w * inv));
+    if (hl == 0 && a.lse) a.lse[row] = (M + log2f(sum)) * kLn2;
+}
+
+// Resident CTAs per SM the launch bounds ask for: ~16 consumer warps per SM at <= 136 registers.
+template <int W>
+constexpr int min_blocks() { return W == 1 ? 8 : W == 2 ? 5 : W == 4 ? 3 : 2; }
+
+template <int W>  // W consumer warps = W groups of 8 query rows, plus one producer warp
+__global__ void __launch_bounds__((W + 1) * 32, min_blocks<W>())
+    verify_split_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                        const VerifyArgs a) {
+    constexpr int S = 3 * W + 1;  // ring stages: slack for consumers that drift apart
+    const Layout L(S, a.B);
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* ring = sm + L.ring;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm + L.full);
+    uint64_t* empty = reinterpret_cast<uint64_t*>(sm + L.empty);
+    int* bad = reinterpret_cast<int*>(sm + L.bad);
+    int* misc = reinterpret_cast<int*>(sm + L.misc);
+    int* pend = reinterpret_cast<int*>(sm + L.pend);    // segments of this share's partial pieces
+    int* queue = reinterpret_cast<int*>(sm + L.queue);  // segments this CTA completes and merges
+    int* prefix = reinterpret_cast<int*>(sm + L.prefix);  // [B + 1] exclusive prefix of pages per request
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int B = a.B, Hkv = a.Hkv, G = a.G, QL = a.QL, R = a.R, cap = a.max_pages * kPageSize;
+
+    // ---- 1. pages per request -> exclusive prefix sum (every CTA, in shared memory)
+    int running = 0;
+    for (int base = 0; base < B; base += (W + 1) * 32) {
+        const int b = base + tid;
+        int n = 0;
+        if (b < B) {
+            const int Lb = a.kv_lens[b];
+            if ((Lb < 0 || Lb > cap) && blockIdx.x == 0) atomicOr(a.err, kErrBadLength);
+            n = (clamp_len(Lb, cap) + kPageSize - 1) / kPageSize;
+        }
+        int incl = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (lane == 31) misc[warp] = incl;
+        __syncthreads();
+        int woff = 0, tot = 0;
+#pragma unroll
+        for (int w = 0; w <= W; ++w) {
+            const int v = misc[w];
+            woff += (w < warp) ? v : 0;
+            tot += v;
+        }
+        if (b < B) prefix[b] = running + woff + incl - n;
+        running += tot;
+        __syncthreads();
+    }
+    if (tid == 0) {
+        prefix[B] = running;
+        misc[12] = 0;
+    }
+    __syncthreads();
+
+    // ---- 2. requests with no cached token: every row's mass on the sink (out = 0, lse = sink)
+    {
+        const long long rows = (long long)B * QL * a.Hq;
+        for (long long r = (long long)blockIdx.x * blockDim.x + tid; r < rows; r += (long long)gridDim.x * blockDim.x) {
+            const int b = (int)(r / ((long long)QL * a.Hq));
+            if (prefix[b + 1] != prefix[b]) continue;
+            uint4* dst = reinterpret_cast<uint4*>(a.out + r * kHeadDim);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+            if (a.lse) a.lse[r] = __ldg(&a.sinks[r % a.Hq]);
+        }
+    }
+
+    const long long U = (long long)running * Hkv;
+    if (U == 0) return;
+    const long long C = effective_shares(a.workers, a.fixed_workers, a.min_pages_per_worker, U);
+    const long long cta = blockIdx.x;
+    if (cta >= C) return;
+    const long long x0 = cta * U / C, x1 = (cta + 1) * U / C;
+    const int total = (int)(x1 - x0);
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], W);  // every consumer warp releases every page
+        }
+        fence_mbar_init();
+        fence_proxy_async_smem();
+        tma_prefetch_desc(&tmap_k);
+        tma_prefetch_desc(&tmap_v);
+    }
+    __syncthreads();
+
+    // ---- 3. producer (warp W): walks the share's pages; lanes resolve 32 page ids at a time
+    SegPiece pp;
+    piece_first(pp, prefix, B, Hkv, x0, x1);
+    int pt = 0, win_base = -64, win_row = -1, issued = 0;
+    auto issue_next = [&]() {  // warp-uniform; the stage of page `issued` is free
+        if (pt >= pp.len()) {
+            piece_next(pp, prefix, B, Hkv, x1);
+            pt = 0;
+            win_base = -64;
+        }
+        if (pt - win_base >= 32) {
+            win_base = pt;
+            int row = -1;
+            if (pt + lane < pp.len()) {
+                const int pid = __ldg(&a.page_table[(long long)pp.b * a.max_pages + pp.page0() + pt + lane]);
+                if (pid >= 0 && pid < a.num_pages) row = (pid * Hkv + pp.g) * kPageSize;
+            }
+            win_row = row;
+        }
+        const int row = __shfl_sync(0xffffffffu, win_row, pt - win_base);
+        if (lane == 0) {
+            const int s = issued % S;
+            uint8_t* dst = ring + s * kStageBytes;
+            if (row >= 0) {
+                bad[s] = 0;
+                mbar_arrive_expect_tx(&full[s], kStageBytes);
+                tma_load_2d(dst, &tmap_k, 0, row, &full[s]);
+                tma_load_2d(dst + kSliceBytes, &tmap_v, 0, row, &full[s]);
+            } else {
+                bad[s] = 1;
+                atomicOr(a.err, kErrBadPage);
+                mbar_arrive(&full[s]);
+            }
+        }
+        ++pt;
+        ++issued;
+    };
+    if (warp == W) {
+        bool ok = true;
+        while (ok && issued < total) {
+            if (issued >= S) {  // the stage's previous page must be released by every consumer
+                int got = 0;
+                if (lane == 0) got = mbar_wait(&empty[issued % S], ((issued / S) - 1) & 1);
+                ok = __shfl_sync(0xffffffffu, got, 0) != 0;
+                if (!ok) break;
+            }
+            issue_next();
+        }
+        if (!ok && lane == 0) atomicOr(a.err, kErrTimeout);
+        // every copy it started has landed before the CTA can exit (bounded)
+        for (int j = issued > S ? issued - S : 0; j < issued; ++j) (void)mbar_wait(&full[j % S], (j / S) & 1);
+    }
+
+    // ---- 4. consumers (warps 0 .. W-1): piece by piece, page by page
+    const int gq = lane >> 2, tq = lane & 3;  // mma fragment coordinates
+    int consumed = 0;
+    bool failed = false;
+    int pend_n = 0;  // partial pieces of this share (at most its first and its last), thread 0 only
+    SegPiece cp;
+    piece_first(cp, prefix, B, Hkv, x0, x1);
+    for (; warp < W && cp.ps < x1; piece_next(cp, prefix, B, Hkv, x1)) {
+        const int kv_len = clamp_len(__ldg(&a.kv_lens[cp.b]), cap);
+        const int pos0 = kv_len - QL;  // cache position of drafted token 0 (negative for a short cache)
+        // This lane's two query rows (mma columns 2tq, 2tq+1): keys [0, lim) are visible.
+        int lim[2];
+        float sink2[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int r = 8 * warp + 2 * tq + e;
+            lim[e] = r < R ? pos0 + r / G + 1 : 0;
+            sink2[e] = r < R ? __ldg(&a.sinks[cp.g * G + r % G]) * kLog2e : kNegInf;
+        }
+        // smallest limit over the warp's rows (padding rows excluded): pages below it need no mask
+        int lim_lo = min(8 * warp + 2 * tq < R ? lim[0] : INT_MAX, 8 * warp + 2 * tq + 1 < R ? lim[1] : INT_MAX);
+#pragma unroll
+        for (int o = 1; o < 4; o <<= 1) lim_lo = min(lim_lo, __shfl_xor_sync(0xffffffffu, lim_lo, o));
+        // Q^T fragments of the row this lane loads (mma column gq)
+        uint32_t qf[4][2];
+        {
+            const int r = 8 * warp + gq;
+            const bool live = r < R;
+            const __nv_bfloat16* qb =
+                a.q + (((long long)cp.b * QL + (live ? r / G : 0)) * a.Hq + cp.g * G + (live ? r % G : 0)) * kHeadDim;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                qf[kk][0] = live ? ld_u32(qb + kk * 16 + 2 * tq) : 0u;
+                qf[kk][1] = live ? ld_u32(qb + kk * 16 + 8 + 2 * tq) : 0u;
+            }
+        }
+        const bool seeded = cp.page0() == 0;  // this piece holds token 0: it carries the sink
+        const int seg = cp.b * Hkv + cp.g;
+        const bool whole = seeded && (cp.pe == cp.seg_start + cp.n);
+        float m[2], d[2], O[4][4];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            m[e] = seeded ? sink2[e] : kNegInf;
+            d[e] = (seeded && lane < 4) ? 1.f : 0.f;  // the sink's own e^(sink-m)=1, once per row
+        }
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) O[mt][e] = 0.f;
+
+        const int npg = cp.len();
+        for (int t = 0; t < npg; ++t) {
+            const int s = consumed % S;
+            if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (consumed / S) & 1))) {
+                failed = true;
+                if (lane == 0) atomicOr(a.err, kErrTimeout);
+                break;
+            }
+            const int page = cp.page0() + t;
+            const int valid = bad[s] ? 0 : min(kPageSize, kv_len - page * kPageSize);
+            const uint32_t kb = smem_u32(ring + s * kStageBytes), vb = kb + kSliceBytes;
+
+            // S^T = K Q^T : 16 tokens x 8 rows
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const int row = ((lane >> 3) & 1) * 8 + (lane & 7);
+                const int chunk = 2 * kk + (lane >> 4);
+                uint32_t af[4];
+                ldmatrix_x4(af, kb + row * 128 + ((chunk ^ (row & 7)) << 4));
+                mma_bf16_16816(acc, af, qf[kk][0], qf[kk][1]);
+            }
+
+            // online softmax (base 2); this lane holds tokens gq, gq+8 of rows 2tq, 2tq+1.  Only the
+            // pages holding the draft or the cache end need the per-row limits.
+            float sc[4];
+            if (valid == kPageSize && (page + 1) * kPageSize <= lim_lo) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sc[e] = acc[e] * a.scale_log2;
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int slot_tok = gq + (e >= 2 ? 8 : 0);
+                    const bool live = slot_tok < valid && page * kPageSize + slot_tok < lim[e & 1];
+                    sc[e] = live ? acc[e] * a.scale_log2 : kNegInf;
+                }
+            }
+            float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+            }
+            const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+            const bool dead0 = (mn0 == kNegInf), dead1 = (mn1 == kNegInf);
+            const float al0 = dead0 ? 1.f : fast_exp2(m[0] - mn0);
+            const float al1 = dead1 ? 1.f : fast_exp2(m[1] - mn1);
+            const float p0 = dead0 ? 0.f : fast_exp2(sc[0] - mn0);
+            const float p2 = dead0 ? 0.f : fast_exp2(sc[2] - mn0);
+            const float p1 = dead1 ? 0.f : fast_exp2(sc[1] - mn1);
+            const float p3 = dead1 ? 0.f : fast_exp2(sc[3] - mn1);
+            d[0] = d[0] * al0 + (p0 + p2);
+            d[1] = d[1] * al1 + (p1 + p3);
+            m[0] = mn0;
+            m[1] = mn1;
+            if (!__all_sync(0xffffffffu, al0 == 1.f && al1 == 1.f)) {  // some row's max moved
+#pragma unroll
+                for (int mt = 0; mt < 4; ++mt) {
+                    O[mt][0] *= al0;
+                    O[mt][1] *= al1;
+                    O[mt][2] *= al0;
+                    O[mt][3] *= al1;
+                }
+            }
+            const uint32_t pb0 = movmatrix_trans(pack_bf16(p0, p1));  // tokens 0..7  -> B rows k = 2tq, 2tq+1
+            const uint32_t pb1 = movmatrix_trans(pack_bf16(p2, p3));  // tokens 8..15
+
+            // O^T += V^T P^T : 4 tiles of 16 head-dims.  Slots at or past the cache end (or of a
+            // skipped page) may hold anything; their value halves are zeroed in registers so
+            // that a 0 weight times garbage cannot produce NaN.
+#pragma unroll
+            for (int mt = 0; mt < 4; ++mt) {
+                const int j = lane >> 3;
+                const int row = (j >> 1) * 8 + (lane & 7);
+                const int chunk = 2 * mt + (j & 1);
+                uint32_t af[4];
+                ldmatrix_x4_trans(af, vb + row * 128 + ((chunk ^ (row & 7)) << 4));
+                if (valid < kPageSize) {
+                    af[0] = keep_tokens(af[0], 2 * tq, valid);
+                    af[1] = keep_tokens(af[1], 2 * tq, valid);
+                    af[2] = keep_tokens(af[2], 2 * tq + 8, valid);
+                    af[3] = keep_tokens(af[3], 2 * tq + 8, valid);
+                }
+                mma_bf16_16816(O[mt], af, pb0, pb1);
+            }
+
+            // release the stage to the producer
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+            ++consumed;
+        }
+        if (failed) break;
+
+        // ---- end of the piece: normaliser over the lanes, then this warp's rows
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) d[e] += __shfl_xor_sync(0xffffffffu, d[e], o);
+        const long long slot = cta + seg;  // partial slot of this piece
+        if (!whole && tid == 0) pend[pend_n++] = seg;
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int r = 8 * warp + 2 * tq + (e & 1);
+                if (r >= R) continue;
+                const int dim = mt * 16 + gq + (e >= 2 ? 8 : 0);
+                const float dt = d[e & 1];
+                const float v = dt > 0.f ? O[mt][e] / dt : 0.f;
+                if (whole)
+                    a.out[(((long long)cp.b * QL + r / G) * a.Hq + cp.g * G + r % G) * kHeadDim + dim] =
+                        __float2bfloat16_rn(v);
+                else
+                    a.part_o[(slot * R + r) * kHeadDim + dim] = v;
+            }
+        if (lane < 4) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int r = 8 * warp + 2 * tq + e;
+                if (r >= R) continue;
+                const float l2 = d[e] > 0.f ? m[e] + log2f(d[e]) : kNegInf;
+                if (whole) {
+                    if (a.lse) a.lse[((long long)cp.b * QL + r / G) * a.Hq + cp.g * G + r % G] = l2 * kLn2;
+                } else {
+                    a.part_lse[slot * R + r] = l2;
+                }
+            }
+        }
+    }
+
+    if (tid == 0) misc[13] = pend_n;
+
+    // ---- 5. count this share's partial pieces (at most two); merge the segments it completes
+    __syncthreads();  // every partial of this CTA is written (CTA scope) ...
+    if (tid < 2 && tid < misc[13]) {  // ... and the release CAS publishes them device-wide
+        const int seg = pend[tid];
+        const int b = seg / Hkv, g = seg - b * Hkv;
+        const int n = prefix[b + 1] - prefix[b];
+        long long c_first;
+        int pieces;
+        segment_pieces((long long)prefix[b] * Hkv + (long long)g * n, n, C, U, c_first, pieces);
+        if (arrive_last(&a.counters[seg], a.epoch, pieces)) queue[atomicAdd(&misc[12], 1)] = seg;
+    }
+    __syncthreads();
+    const int nq = misc[12];
+    // (segment, row) items over half-warps
+    for (int item = warp * 2 + (lane >> 4); item < nq * R; item += (W + 1) * 2) {
+        const int seg = queue[item / R], r = item % R;
+        const int b = seg / Hkv, g = seg - b * Hkv;
+        const int n = prefix[b + 1] - prefix[b];
+        long long c_first;
+        int pieces;
+        segment_pieces((long long)prefix[b] * Hkv + (long long)g * n, n, C, U, c_first, pieces);
+        merge_row(a, b, g, r, c_first + seg, pieces, lane & 15);
+    }
+}
+
+template <int W>
+cudaError_t ensure_smem_attr(size_t smem) {
+    static thread_local size_t set_to[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && set_to[dev] >= smem) return cudaSuccess;
+    e = cudaFuncSetAttribute(verify_split_kernel<W>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess && dev < 64) set_to[dev] = smem;
+    return e;
+}
+
+template <int W>
+cudaError_t occupancy(size_t smem, int* per_sm) {
+    cudaError_t e = ensure_smem_attr<W>(smem);
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, verify_split_kernel<W>, (W + 1) * 32, smem);
+}
+
+// Warps for R query rows: groups of 8 rows, rounded up to a power of two.
+int warps_for(int R) {
+    const int n = (R + 7) / 8;
+    return n <= 1 ? 1 : n <= 2 ? 2 : n <= 4 ? 4 : 8;
+}
+
+// Resident CTAs for (device, warps, shared memory), remembered so that repeated calls skip the query.
+cudaError_t resident(int W, size_t smem, long long* ctas) {
+    struct Entry {
+        int dev, W;
+        size_t smem;
+        long long ctas;
+    };
+    static thread_local Entry cache[8] = {};
+    static thread_local int next = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    for (const Entry& c : cache)
+        if (c.ctas > 0 && c.dev == dev && c.W == W && c.smem == smem) {
+            *ctas = c.ctas;
+            return cudaSuccess;
+        }
+    int sms = 0, per_sm = 0;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    switch (W) {
+        case 1: e = occupancy<1>(smem, &per_sm); break;
+        case 2: e = occupancy<2>(smem, &per_sm); break;
+        case 4: e = occupancy<4>(smem, &per_sm); break;
+        default: e = occupancy<8>(smem, &per_sm); break;
+    }
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    cache[next] = Entry{dev, W, smem, (long long)sms * per_sm};
+    next = (next + 1) % 8;
+    *ctas = (long long)sms * per_sm;
+    return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t verify_plan(int B, int QL, int Hq, int Hkv, int num_workers, VerifyPlan* plan) {
+    const int G = Hq / Hkv, R = QL * G;
+    const int W = warps_for(R);
+    const int S = 3 * W + 1;
+    const size_t smem = Layout(S, B).total;
+    long long res = 0;
+    cudaError_t e = resident(W, smem, &res);
+    if (e != cudaSuccess) return e;
+    const long long shares = num_workers > 0 ? num_workers : res;
+    plan->grid = (int)shares;
+    plan->warps = W;
+    plan->stages = S;
+    plan->smem = smem;
+    plan->slots = (size_t)shares + (size_t)B * Hkv;
+    size_t bytes = plan->slots * R * kHeadDim * 4;  // partial o
+    bytes += plan->slots * R * 4;                   // partial lse (base 2)
+    plan->counters_offset = (bytes + 255) & ~size_t(255);
+    plan->ws_bytes = plan->counters_offset + (size_t)B * Hkv * sizeof(unsigned long long);
+    return cudaSuccess;
+}
+
+cudaError_t verify_launch(const VerifyArgs& args, const VerifyPlan& plan, const CUtensorMap& tk, const CUtensorMap& tv,
+                          cudaStream_t stream) {
+    if (args.B == 0) return cudaSuccess;
+    VerifyArgs a = args;
+    a.min_pages_per_worker = kMinPages;
+    switch (plan.warps) {
+        case 1: verify_split_kernel<1><<<plan.grid, 64, plan.smem, stream>>>(tk, tv, a); break;
+        case 2: verify_split_kernel<2><<<plan.grid, 96, plan.smem, stream>>>(tk, tv, a); break;
+        case 4: verify_split_kernel<4><<<plan.grid, 160, plan.smem, stream>>>(tk, tv, a); break;
+        default: verify_split_kernel<8><<<plan.grid, 288, plan.smem, stream>>>(tk, tv, a); break;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace sinkattn

@@ -36,6 +36,11 @@ class DecodeDims(ctypes.Structure):
                                               "num_pages", "max_pages", "num_workers")]
 
 
+class VerifyDims(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("batch", "q_len", "num_q_heads", "num_kv_heads", "head_dim",
+                                              "page_size", "num_pages", "max_pages", "num_workers")]
+
+
 class PrefillDims(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("num_seqs", "total_tokens", "max_seqlen", "num_q_heads",
                                               "num_kv_heads", "head_dim")]
@@ -45,7 +50,8 @@ class MergeDims(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("num_splits", "num_rows", "num_heads", "head_dim")]
 
 
-EXPORTS = ("sinkattn_decode", "sinkattn_prefill", "sinkattn_merge", "sinkattn_decode_workspace_size",
+EXPORTS = ("sinkattn_decode", "sinkattn_prefill", "sinkattn_merge", "sinkattn_decode_workspace_size", "sinkattn_verify",
+           "sinkattn_verify_workspace_size",
            "sinkattn_get_error", "sinkattn_status_string", "sinkattn_version")
 
 
@@ -62,11 +68,14 @@ def _load():
     lib.sinkattn_decode_noalloc.restype = ctypes.c_int
     lib.sinkattn_decode_workspace_size.argtypes = [ctypes.POINTER(DecodeDims)]
     lib.sinkattn_decode_workspace_size.restype = sz
+    lib.sinkattn_verify.argtypes = [P, P, P, P, P, P, f32, P, P, ctypes.POINTER(VerifyDims), P, sz, P]
+    lib.sinkattn_verify_workspace_size.argtypes = [ctypes.POINTER(VerifyDims)]
+    lib.sinkattn_verify_workspace_size.restype = sz
     lib.sinkattn_get_error.argtypes = [P]
     lib.sinkattn_status_string.argtypes = [ctypes.c_int]
     lib.sinkattn_status_string.restype = ctypes.c_char_p
     lib.sinkattn_version.restype = i32
-    for fn in ("sinkattn_decode", "sinkattn_prefill", "sinkattn_merge", "sinkattn_get_error"):
+    for fn in ("sinkattn_decode", "sinkattn_prefill", "sinkattn_merge", "sinkattn_get_error", "sinkattn_verify"):
         getattr(lib, fn).restype = ctypes.c_int
     return lib
 
@@ -145,6 +154,51 @@ def sinkattn_decode(q, k_pages, v_pages, page_table, kv_lens, sinks, scale, out=
                               float(scale), _ptr(out), _ptr(lse), ctypes.byref(dims), _ptr(workspace),
                               workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "sinkattn_decode")
+    return out, lse
+
+
+def verify_dims(q, k_pages, page_table, num_workers=0) -> VerifyDims:
+    B, QL, Hq, D = q.shape
+    P, Hkv, PS, _ = k_pages.shape
+    return VerifyDims(B, QL, Hq, Hkv, D, PS, P, page_table.shape[1], num_workers)
+
+
+def sinkattn_verify_workspace_size(q, k_pages, page_table, num_workers=0) -> int:
+    return int(_lib.sinkattn_verify_workspace_size(ctypes.byref(verify_dims(q, k_pages, page_table, num_workers))))
+
+
+def sinkattn_verify(q, k_pages, v_pages, page_table, kv_lens, sinks, scale, out=None, lse=None, workspace=None,
+                    num_workers=0, return_lse=True, stream=None):
+    """Attention of q_len drafted tokens per request over the paged cache (their K/V already in it).
+
+    q [B, q_len, Hq, 64]; kv_lens counts the drafted tokens.  Shapes: see ``include/sinkattn.h``.
+    Returns (out [B, q_len, Hq, 64], lse [B, q_len, Hq]).
+    """
+    _need(q, "q", torch.bfloat16, 4)
+    _need(k_pages, "k_pages", torch.bfloat16, 4)
+    _need(v_pages, "v_pages", torch.bfloat16, 4)
+    _need(page_table, "page_table", torch.int32, 2)
+    _need(kv_lens, "kv_lens", torch.int32, 1)
+    _need(sinks, "sinks", torch.float32, 1)
+    if v_pages.shape != k_pages.shape:
+        raise ValueError("k_pages and v_pages must have the same shape")
+    B, QL, Hq, D = q.shape
+    if page_table.shape[0] != B or kv_lens.shape[0] != B or sinks.shape[0] != Hq or k_pages.shape[1] == 0:
+        raise ValueError("inconsistent verify shapes")
+    dims = verify_dims(q, k_pages, page_table, num_workers)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty(B, QL, Hq, device=q.device, dtype=torch.float32)
+    if workspace is None:
+        nbytes = int(_lib.sinkattn_verify_workspace_size(ctypes.byref(dims)))
+        if nbytes == 0:
+            raise SinkAttnError(ERR_INVALID_ARG, "sinkattn_verify_workspace_size")
+        workspace = torch.empty(nbytes, device=q.device, dtype=torch.uint8)
+    st = _lib.sinkattn_verify(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table), _ptr(kv_lens), _ptr(sinks),
+                              float(scale), _ptr(out), _ptr(lse), ctypes.byref(dims), _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "sinkattn_verify")
     return out, lse
 
 

@@ -125,6 +125,55 @@ sinkattn_status_t sinkattn_decode(const void *q, const void *k_pages, const void
                                   const sinkattn_decode_dims_t *dims, void *workspace,
                                   size_t workspace_bytes, void *stream);
 
+/* Shapes of a verification call. */
+typedef struct {
+    int32_t batch;             /* B requests, 0..32768                                     */
+    int32_t q_len;             /* drafted query tokens per request, 1..16, and
+                                  q_len * (num_q_heads / num_kv_heads) <= 64              */
+    int32_t num_q_heads;       /* Hq                                                      */
+    int32_t num_kv_heads;      /* Hkv, divides Hq                                         */
+    int32_t head_dim;          /* must be 64                                              */
+    int32_t page_size;         /* must be 16                                              */
+    int32_t num_pages;         /* P, pages in the K/V pools                               */
+    int32_t max_pages;         /* row length of page_table (>= 1)                         */
+    int32_t num_workers;       /* as in sinkattn_decode_dims_t (0 = automatic)            */
+} sinkattn_verify_dims_t;
+
+/* Bytes of device workspace sinkattn_verify needs for `dims`; 0 on invalid dims. */
+size_t sinkattn_verify_workspace_size(const sinkattn_verify_dims_t *dims);
+
+/*
+ * Attention of drafted tokens over the paged cache: the verification step of
+ * speculative decoding.  Source: "Accelerating Sonar through speculation",
+ * sections "Speculative decoding" (the target model runs over the drafted
+ * tokens and produces logits for each of them) and "Inference with
+ * speculative decoding" (verification batches over the paged KV cache); the
+ * attention of every token is the sink attention of sinkattn_decode.
+ *
+ * The q_len query tokens of request b are its last q_len cached tokens, whose
+ * K and V are already in the pages: token i sits at cache position
+ * kv_lens[b] - q_len + i and attends to cache tokens 0 .. that position
+ * (the whole prefix and the draft up to itself).  All q_len tokens of a
+ * request share one pass over its pages.  q_len = 1 is sinkattn_decode.
+ *
+ *   q          [B, q_len, Hq, 64]  bf16
+ *   k_pages, v_pages, page_table, sinks, scale: as sinkattn_decode
+ *   kv_lens    [B] int32   cached tokens per request, the q_len drafted ones included;
+ *                          a request shorter than q_len leaves its earliest tokens
+ *                          without keys (out = 0, lse = sink)
+ *   out        [B, q_len, Hq, 64]  bf16
+ *   lse        [B, q_len, Hq]      f32 natural log, or NULL
+ *   workspace  at least sinkattn_verify_workspace_size(dims) bytes, 256-byte aligned;
+ *              it needs no initialisation and must not be shared by overlapping calls.
+ *
+ * Errors and the handling of bad page ids and lengths are those of sinkattn_decode.
+ */
+sinkattn_status_t sinkattn_verify(const void *q, const void *k_pages, const void *v_pages,
+                                  const int32_t *page_table, const int32_t *kv_lens,
+                                  const float *sinks, float scale, void *out, float *lse,
+                                  const sinkattn_verify_dims_t *dims, void *workspace,
+                                  size_t workspace_bytes, void *stream);
+
 /*
  * Causal (or full) prefill over packed variable-length sequences.
  * Source: "GPT-OSS on day 0", section "Kernels for GPT-OSS / Sink Attention"

@@ -69,3 +69,19 @@ def test_host_validation_without_device(S):
     m = S.MergeDims(2, 4, 0, 64)
     assert lib.sinkattn_merge(None, None, None, None, None, ctypes.byref(m), None) == S.ERR_INVALID_ARG
     assert lib.sinkattn_merge(None, None, None, None, None, None, None) == S.ERR_INVALID_ARG
+
+
+def test_verify_host_validation_without_device(S):
+    lib = S._lib
+    nul = [None] * 6
+
+    def call(d):
+        return lib.sinkattn_verify(*nul, 0.125, None, None, ctypes.byref(d), None, 0, None)
+
+    assert call(S.VerifyDims(2, 0, 8, 2, 64, 16, 10, 4, 0)) == S.ERR_INVALID_ARG       # q_len 0
+    assert call(S.VerifyDims(2, 17, 8, 8, 64, 16, 10, 4, 0)) == S.ERR_UNSUPPORTED      # q_len 17
+    assert call(S.VerifyDims(2, 9, 64, 8, 64, 16, 10, 4, 0)) == S.ERR_UNSUPPORTED      # 9 x 8 = 72 rows
+    assert call(S.VerifyDims(2, 4, 8, 3, 64, 16, 10, 4, 0)) == S.ERR_INVALID_ARG       # Hq % Hkv != 0
+    assert call(S.VerifyDims(2, 4, 8, 2, 32, 16, 10, 4, 0)) == S.ERR_UNSUPPORTED       # head_dim 32
+    assert lib.sinkattn_verify_workspace_size(ctypes.byref(S.VerifyDims(2, 9, 64, 8, 64, 16, 10, 4, 0))) == 0
+    assert call(S.VerifyDims(0, 4, 8, 2, 64, 16, 10, 4, 0)) == 0                       # empty batch: nothing to do
