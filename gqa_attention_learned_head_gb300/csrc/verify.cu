@@ -14,16 +14,17 @@
 // shares of (request, KV head, page) units, pieces, merge in the same launch),
 // but the R = q_len x G query rows of a (request, KV head) go through ONE pass
 // over its pages, so the draft costs the cache bytes once:
-//  * consumer warp w < W owns rows 8w .. 8w+7 (row r = i * G + head within the
-//    group); all consumer warps read every page of the share from one CTA ring
+//  * consumer warp w < W owns rows 16w .. 16w+15 (row r = i * G + head within
+//    the group); all consumer warps read every page of the share from one CTA ring
 //    of 3W + 1 stages, which a producer warp (warp W) fills by TMA (K and V
 //    slices of one (page, KV head), 128-byte swizzle) as soon as every consumer
 //    has released a stage.  The producer is a warp of its own so that its
 //    waits -- for the slowest consumer, for page ids, for a TMA issue slot --
 //    never hold up the products;
-//  * per warp and page the products are the decode's: S^T[16 tokens x 8 rows]
-//    = K Q^T and O^T[64 x 8] += V^T P^T with mma.m16n8k16, online softmax in
-//    registers, each row masked at its own causal limit;
+//  * per warp and page: S[16 rows x 16 tokens] = Q K^T and O[16 x 64] += P V
+//    with mma.m16n8k16 (rows on M, so P goes from the accumulators straight
+//    into the next product), online softmax in registers, each row masked at
+//    its own causal limit;
 //  * no combine between warps (they own different rows); a piece that is not
 //    a whole segment writes fp32 partials per row and the CTA completing the
 //    segment merges them by log-sum-exp.
@@ -69,26 +70,29 @@ __device__ __forceinline__ uint32_t keep_tokens(uint32_t x, int t, int valid) {
     return x & ((t < valid ? 0x0000FFFFu : 0u) | (t + 1 < valid ? 0xFFFF0000u : 0u));
 }
 
-// Log-sum-exp merge of one query row of one segment from its partials (base-2 lse), by 16
-// lanes: lane l of the half-warp owns head-dims 4l..4l+3.  Pieces are taken 8 at a time with
-// all loads issued together and combined online.
+// Log-sum-exp merge of one query row of one segment from its partials (base-2 lse), by the 4
+// lanes of a quad: lane l owns head-dims 16l..16l+15.  Pieces are taken 4 at a time with all
+// loads issued together and combined online; a quad per row keeps many rows in flight at once.
 __device__ __forceinline__ void merge_row(const VerifyArgs& a, int b, int g, int r, long long slot0, int pieces,
                                           int hl) {
-    constexpr int kChunk = 8;
+    constexpr int kChunk = 4;
     const int R = a.R;
     const float* lp = a.part_lse + slot0 * R + r;
-    const float* op = a.part_o + (slot0 * R + r) * kHeadDim + 4 * hl;
+    const float* op = a.part_o + (slot0 * R + r) * kHeadDim + 16 * hl;
     float M = kNegInf, sum = 0.f;
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    float o[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) o[k] = 0.f;
     for (int c0 = 0; c0 < pieces; c0 += kChunk) {
         float l[kChunk];
-        float4 v[kChunk];
+        float4 v[kChunk][4];
 #pragma unroll
         for (int i = 0; i < kChunk; ++i) {
             const bool in = c0 + i < pieces;
+            const float4* src = reinterpret_cast<const float4*>(op + (long long)(c0 + i) * R * kHeadDim);
             l[i] = in ? __ldcg(lp + (long long)(c0 + i) * R) : kNegInf;
-            v[i] = in ? __ldcg(reinterpret_cast<const float4*>(op + (long long)(c0 + i) * R * kHeadDim))
-                      : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) v[i][k] = in ? __ldcg(src + k) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         float Mc = M;
 #pragma unroll
@@ -96,39 +100,44 @@ __device__ __forceinline__ void merge_row(const VerifyArgs& a, int b, int g, int
         if (Mc == kNegInf) continue;
         const float rs = M == kNegInf ? 0.f : exp2f(M - Mc);
         sum *= rs;
-        o.x *= rs;
-        o.y *= rs;
-        o.z *= rs;
-        o.w *= rs;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) o[k] *= rs;
 #pragma unroll
         for (int i = 0; i < kChunk; ++i) {
             const float w = l[i] == kNegInf ? 0.f : exp2f(l[i] - Mc);
             sum += w;
-            o.x += w * v[i].x;
-            o.y += w * v[i].y;
-            o.z += w * v[i].z;
-            o.w += w * v[i].w;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                o[4 * k + 0] += w * v[i][k].x;
+                o[4 * k + 1] += w * v[i][k].y;
+                o[4 * k + 2] += w * v[i][k].z;
+                o[4 * k + 3] += w * v[i][k].w;
+            }
         }
         M = Mc;
     }
     const int i = r / a.G, h = g * a.G + r % a.G;
     const long long row = ((long long)b * a.QL + i) * a.Hq + h;
-    uint2* dst = reinterpret_cast<uint2*>(a.out + row * kHeadDim) + hl;
+    uint4* dst = reinterpret_cast<uint4*>(a.out + row * kHeadDim + 16 * hl);
     if (M == kNegInf) {  // no live key and no finite sink in any piece
-        *dst = make_uint2(0u, 0u);
+        dst[0] = dst[1] = make_uint4(0u, 0u, 0u, 0u);
         if (hl == 0 && a.lse) a.lse[row] = kNegInf;
         return;
     }
     const float inv = 1.f / sum;
-    *dst = make_uint2(pack_bf16(o.x * inv, o.y * inv), pack_bf16(o.z * inv, o.w * inv));
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+        dst[k] = make_uint4(pack_bf16(o[8 * k + 0] * inv, o[8 * k + 1] * inv), pack_bf16(o[8 * k + 2] * inv, o[8 * k + 3] * inv),
+                            pack_bf16(o[8 * k + 4] * inv, o[8 * k + 5] * inv), pack_bf16(o[8 * k + 6] * inv, o[8 * k + 7] * inv));
     if (hl == 0 && a.lse) a.lse[row] = (M + log2f(sum)) * kLn2;
 }
 
-// Resident CTAs per SM the launch bounds ask for: ~16 consumer warps per SM at <= 136 registers.
+// Resident CTAs per SM the launch bounds ask for: a register cap of 128 (one consumer warp) or
+// 136 (two or four), which the consumers need without spilling.
 template <int W>
-constexpr int min_blocks() { return W == 1 ? 8 : W == 2 ? 5 : W == 4 ? 3 : 2; }
+constexpr int min_blocks() { return W == 1 ? 8 : W == 2 ? 5 : 3; }
 
-template <int W>  // W consumer warps = W groups of 8 query rows, plus one producer warp
+template <int W>  // W consumer warps = W groups of 16 query rows, plus one producer warp
 __global__ void __launch_bounds__((W + 1) * 32, min_blocks<W>())
     verify_split_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                         const VerifyArgs a) {
@@ -279,45 +288,49 @@ __global__ void __launch_bounds__((W + 1) * 32, min_blocks<W>())
     for (; warp < W && cp.ps < x1; piece_next(cp, prefix, B, Hkv, x1)) {
         const int kv_len = clamp_len(__ldg(&a.kv_lens[cp.b]), cap);
         const int pos0 = kv_len - QL;  // cache position of drafted token 0 (negative for a short cache)
-        // This lane's two query rows (mma columns 2tq, 2tq+1): keys [0, lim) are visible.
-        int lim[2];
+        // This lane's two query rows (mma rows gq and gq + 8 of the warp's 16): keys [0, lim) visible.
+        int rr[2], lim[2];
         float sink2[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-            const int r = 8 * warp + 2 * tq + e;
-            lim[e] = r < R ? pos0 + r / G + 1 : 0;
-            sink2[e] = r < R ? __ldg(&a.sinks[cp.g * G + r % G]) * kLog2e : kNegInf;
+            rr[e] = 16 * warp + gq + 8 * e;
+            lim[e] = rr[e] < R ? pos0 + rr[e] / G + 1 : 0;
+            sink2[e] = rr[e] < R ? __ldg(&a.sinks[cp.g * G + rr[e] % G]) * kLog2e : kNegInf;
         }
-        // smallest limit over the warp's rows (padding rows excluded): pages below it need no mask
-        int lim_lo = min(8 * warp + 2 * tq < R ? lim[0] : INT_MAX, 8 * warp + 2 * tq + 1 < R ? lim[1] : INT_MAX);
+        // smallest limit over the warp's live rows: pages below it need no mask
+        int lim_lo = min(rr[0] < R ? lim[0] : INT_MAX, rr[1] < R ? lim[1] : INT_MAX);
 #pragma unroll
-        for (int o = 1; o < 4; o <<= 1) lim_lo = min(lim_lo, __shfl_xor_sync(0xffffffffu, lim_lo, o));
-        // Q^T fragments of the row this lane loads (mma column gq)
-        uint32_t qf[4][2];
+        for (int o = 4; o < 32; o <<= 1) lim_lo = min(lim_lo, __shfl_xor_sync(0xffffffffu, lim_lo, o));
+        // A fragments of Q (rows gq, gq + 8; dims 2tq, 2tq+1 and +8 within each 16-dim step)
+        uint32_t qa[4][4];
         {
-            const int r = 8 * warp + gq;
-            const bool live = r < R;
-            const __nv_bfloat16* qb =
-                a.q + (((long long)cp.b * QL + (live ? r / G : 0)) * a.Hq + cp.g * G + (live ? r % G : 0)) * kHeadDim;
+            const __nv_bfloat16* qr[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int r = rr[e] < R ? rr[e] : 0;
+                qr[e] = a.q + (((long long)cp.b * QL + r / G) * a.Hq + cp.g * G + r % G) * kHeadDim;
+            }
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-                qf[kk][0] = live ? ld_u32(qb + kk * 16 + 2 * tq) : 0u;
-                qf[kk][1] = live ? ld_u32(qb + kk * 16 + 8 + 2 * tq) : 0u;
+                qa[kk][0] = rr[0] < R ? ld_u32(qr[0] + kk * 16 + 2 * tq) : 0u;
+                qa[kk][1] = rr[1] < R ? ld_u32(qr[1] + kk * 16 + 2 * tq) : 0u;
+                qa[kk][2] = rr[0] < R ? ld_u32(qr[0] + kk * 16 + 8 + 2 * tq) : 0u;
+                qa[kk][3] = rr[1] < R ? ld_u32(qr[1] + kk * 16 + 8 + 2 * tq) : 0u;
             }
         }
         const bool seeded = cp.page0() == 0;  // this piece holds token 0: it carries the sink
         const int seg = cp.b * Hkv + cp.g;
         const bool whole = seeded && (cp.pe == cp.seg_start + cp.n);
-        float m[2], d[2], O[4][4];
+        float m[2], d[2], O[8][4];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             m[e] = seeded ? sink2[e] : kNegInf;
-            d[e] = (seeded && lane < 4) ? 1.f : 0.f;  // the sink's own e^(sink-m)=1, once per row
+            d[e] = (seeded && tq == 0) ? 1.f : 0.f;  // the sink's own e^(sink-m)=1, once per row
         }
 #pragma unroll
-        for (int mt = 0; mt < 4; ++mt)
+        for (int n = 0; n < 8; ++n)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) O[mt][e] = 0.f;
+            for (int e = 0; e < 4; ++e) O[n][e] = 0.f;
 
         const int npg = cp.len();
         for (int t = 0; t < npg; ++t) {
@@ -331,78 +344,91 @@ __global__ void __launch_bounds__((W + 1) * 32, min_blocks<W>())
             const int valid = bad[s] ? 0 : min(kPageSize, kv_len - page * kPageSize);
             const uint32_t kb = smem_u32(ring + s * kStageBytes), vb = kb + kSliceBytes;
 
-            // S^T = K Q^T : 16 tokens x 8 rows
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            // S = Q K^T : 16 rows x 16 tokens (two n-tiles of 8 tokens); K rows give B fragments
+            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-                const int row = ((lane >> 3) & 1) * 8 + (lane & 7);
-                const int chunk = 2 * kk + (lane >> 4);
-                uint32_t af[4];
-                ldmatrix_x4(af, kb + row * 128 + ((chunk ^ (row & 7)) << 4));
-                mma_bf16_16816(acc, af, qf[kk][0], qf[kk][1]);
+                const int tok = ((lane >> 4) << 3) + (lane & 7);
+                const int chunk = 2 * kk + ((lane >> 3) & 1);
+                uint32_t kf[4];
+                ldmatrix_x4(kf, kb + tok * 128 + ((chunk ^ (tok & 7)) << 4));
+                mma_bf16_16816(acc[0], qa[kk], kf[0], kf[1]);
+                mma_bf16_16816(acc[1], qa[kk], kf[2], kf[3]);
             }
 
-            // online softmax (base 2); this lane holds tokens gq, gq+8 of rows 2tq, 2tq+1.  Only the
-            // pages holding the draft or the cache end need the per-row limits.
-            float sc[4];
+            // online softmax (base 2): element e of n-tile j is row rr[e >> 1], token 8j + 2tq + (e & 1).
+            // Only the pages holding the draft or the cache end need the per-row limits.
+            float sc[2][4];
             if (valid == kPageSize && (page + 1) * kPageSize <= lim_lo) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) sc[e] = acc[e] * a.scale_log2;
+                for (int j = 0; j < 2; ++j)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sc[j][e] = acc[j][e] * a.scale_log2;
             } else {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int slot_tok = gq + (e >= 2 ? 8 : 0);
-                    const bool live = slot_tok < valid && page * kPageSize + slot_tok < lim[e & 1];
-                    sc[e] = live ? acc[e] * a.scale_log2 : kNegInf;
+                for (int j = 0; j < 2; ++j)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int slot_tok = 8 * j + 2 * tq + (e & 1);
+                        const bool live = slot_tok < valid && page * kPageSize + slot_tok < lim[e >> 1];
+                        sc[j][e] = live ? acc[j][e] * a.scale_log2 : kNegInf;
+                    }
+            }
+            float mx[2];
+            mx[0] = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
+            mx[1] = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
+#pragma unroll
+            for (int o = 1; o < 4; o <<= 1) {
+                mx[0] = fmaxf(mx[0], __shfl_xor_sync(0xffffffffu, mx[0], o));
+                mx[1] = fmaxf(mx[1], __shfl_xor_sync(0xffffffffu, mx[1], o));
+            }
+            float al[2], p[2][4];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const float mn = fmaxf(m[e], mx[e]);
+                const bool dead = mn == kNegInf;
+                al[e] = dead ? 1.f : fast_exp2(m[e] - mn);
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    p[j][2 * e] = dead ? 0.f : fast_exp2(sc[j][2 * e] - mn);
+                    p[j][2 * e + 1] = dead ? 0.f : fast_exp2(sc[j][2 * e + 1] - mn);
+                }
+                d[e] = d[e] * al[e] + ((p[0][2 * e] + p[0][2 * e + 1]) + (p[1][2 * e] + p[1][2 * e + 1]));
+                m[e] = mn;
+            }
+            if (!__all_sync(0xffffffffu, al[0] == 1.f && al[1] == 1.f)) {  // some row's max moved
+#pragma unroll
+                for (int n = 0; n < 8; ++n) {
+                    O[n][0] *= al[0];
+                    O[n][1] *= al[0];
+                    O[n][2] *= al[1];
+                    O[n][3] *= al[1];
                 }
             }
-            float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
-#pragma unroll
-            for (int o = 4; o < 32; o <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-            }
-            const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
-            const bool dead0 = (mn0 == kNegInf), dead1 = (mn1 == kNegInf);
-            const float al0 = dead0 ? 1.f : fast_exp2(m[0] - mn0);
-            const float al1 = dead1 ? 1.f : fast_exp2(m[1] - mn1);
-            const float p0 = dead0 ? 0.f : fast_exp2(sc[0] - mn0);
-            const float p2 = dead0 ? 0.f : fast_exp2(sc[2] - mn0);
-            const float p1 = dead1 ? 0.f : fast_exp2(sc[1] - mn1);
-            const float p3 = dead1 ? 0.f : fast_exp2(sc[3] - mn1);
-            d[0] = d[0] * al0 + (p0 + p2);
-            d[1] = d[1] * al1 + (p1 + p3);
-            m[0] = mn0;
-            m[1] = mn1;
-            if (!__all_sync(0xffffffffu, al0 == 1.f && al1 == 1.f)) {  // some row's max moved
-#pragma unroll
-                for (int mt = 0; mt < 4; ++mt) {
-                    O[mt][0] *= al0;
-                    O[mt][1] *= al1;
-                    O[mt][2] *= al0;
-                    O[mt][3] *= al1;
-                }
-            }
-            const uint32_t pb0 = movmatrix_trans(pack_bf16(p0, p1));  // tokens 0..7  -> B rows k = 2tq, 2tq+1
-            const uint32_t pb1 = movmatrix_trans(pack_bf16(p2, p3));  // tokens 8..15
+            // P as the A operand: the accumulator layout is the A layout (no shuffle)
+            uint32_t pa[4];
+            pa[0] = pack_bf16(p[0][0], p[0][1]);  // row gq,     tokens 2tq, 2tq+1
+            pa[1] = pack_bf16(p[0][2], p[0][3]);  // row gq + 8, tokens 2tq, 2tq+1
+            pa[2] = pack_bf16(p[1][0], p[1][1]);  // row gq,     tokens 8+2tq, 9+2tq
+            pa[3] = pack_bf16(p[1][2], p[1][3]);  // row gq + 8, tokens 8+2tq, 9+2tq
 
-            // O^T += V^T P^T : 4 tiles of 16 head-dims.  Slots at or past the cache end (or of a
-            // skipped page) may hold anything; their value halves are zeroed in registers so
-            // that a 0 weight times garbage cannot produce NaN.
+            // O += P V : 8 n-tiles of 8 head-dims; V rows give B fragments through the transposing
+            // load.  Slots at or past the cache end (or of a skipped page) may hold anything; their
+            // value halves are zeroed in registers so that a 0 weight times garbage cannot make NaN.
 #pragma unroll
-            for (int mt = 0; mt < 4; ++mt) {
-                const int j = lane >> 3;
-                const int row = (j >> 1) * 8 + (lane & 7);
-                const int chunk = 2 * mt + (j & 1);
-                uint32_t af[4];
-                ldmatrix_x4_trans(af, vb + row * 128 + ((chunk ^ (row & 7)) << 4));
+            for (int nn = 0; nn < 4; ++nn) {
+                const int tok = ((lane >> 3) & 1) * 8 + (lane & 7);
+                const int chunk = 2 * nn + (lane >> 4);
+                uint32_t vf[4];
+                ldmatrix_x4_trans(vf, vb + tok * 128 + ((chunk ^ (tok & 7)) << 4));
                 if (valid < kPageSize) {
-                    af[0] = keep_tokens(af[0], 2 * tq, valid);
-                    af[1] = keep_tokens(af[1], 2 * tq, valid);
-                    af[2] = keep_tokens(af[2], 2 * tq + 8, valid);
-                    af[3] = keep_tokens(af[3], 2 * tq + 8, valid);
+                    vf[0] = keep_tokens(vf[0], 2 * tq, valid);
+                    vf[1] = keep_tokens(vf[1], 8 + 2 * tq, valid);
+                    vf[2] = keep_tokens(vf[2], 2 * tq, valid);
+                    vf[3] = keep_tokens(vf[3], 8 + 2 * tq, valid);
                 }
-                mma_bf16_16816(O[mt], af, pb0, pb1);
+                mma_bf16_16816(O[2 * nn], pa, vf[0], vf[1]);
+                mma_bf16_16816(O[2 * nn + 1], pa, vf[2], vf[3]);
             }
 
             // release the stage to the producer
@@ -413,33 +439,31 @@ __global__ void __launch_bounds__((W + 1) * 32, min_blocks<W>())
         }
         if (failed) break;
 
-        // ---- end of the piece: normaliser over the lanes, then this warp's rows
+        // ---- end of the piece: normaliser over the quad, then this warp's rows
 #pragma unroll
         for (int e = 0; e < 2; ++e)
 #pragma unroll
-            for (int o = 4; o < 32; o <<= 1) d[e] += __shfl_xor_sync(0xffffffffu, d[e], o);
+            for (int o = 1; o < 4; o <<= 1) d[e] += __shfl_xor_sync(0xffffffffu, d[e], o);
         const long long slot = cta + seg;  // partial slot of this piece
         if (!whole && tid == 0) pend[pend_n++] = seg;
 #pragma unroll
-        for (int mt = 0; mt < 4; ++mt)
+        for (int e = 0; e < 2; ++e) {
+            const int r = rr[e];
+            if (r >= R) continue;
+            const float inv = d[e] > 0.f ? 1.f / d[e] : 0.f;
+            if (whole) {
+                __nv_bfloat16* dst =
+                    a.out + (((long long)cp.b * QL + r / G) * a.Hq + cp.g * G + r % G) * kHeadDim + 2 * tq;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int r = 8 * warp + 2 * tq + (e & 1);
-                if (r >= R) continue;
-                const int dim = mt * 16 + gq + (e >= 2 ? 8 : 0);
-                const float dt = d[e & 1];
-                const float v = dt > 0.f ? O[mt][e] / dt : 0.f;
-                if (whole)
-                    a.out[(((long long)cp.b * QL + r / G) * a.Hq + cp.g * G + r % G) * kHeadDim + dim] =
-                        __float2bfloat16_rn(v);
-                else
-                    a.part_o[(slot * R + r) * kHeadDim + dim] = v;
+                for (int n = 0; n < 8; ++n)
+                    *reinterpret_cast<uint32_t*>(dst + 8 * n) = pack_bf16(O[n][2 * e] * inv, O[n][2 * e + 1] * inv);
+            } else {
+                float* dst = a.part_o + (slot * R + r) * kHeadDim + 2 * tq;
+#pragma unroll
+                for (int n = 0; n < 8; ++n)
+                    *reinterpret_cast<float2*>(dst + 8 * n) = make_float2(O[n][2 * e] * inv, O[n][2 * e + 1] * inv);
             }
-        if (lane < 4) {
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int r = 8 * warp + 2 * tq + e;
-                if (r >= R) continue;
+            if (tq == 0) {
                 const float l2 = d[e] > 0.f ? m[e] + log2f(d[e]) : kNegInf;
                 if (whole) {
                     if (a.lse) a.lse[((long long)cp.b * QL + r / G) * a.Hq + cp.g * G + r % G] = l2 * kLn2;
@@ -465,15 +489,15 @@ __global__ void __launch_bounds__((W + 1) * 32, min_blocks<W>())
     }
     __syncthreads();
     const int nq = misc[12];
-    // (segment, row) items over half-warps
-    for (int item = warp * 2 + (lane >> 4); item < nq * R; item += (W + 1) * 2) {
+    // (segment, row) items over quads of lanes: 8 per warp and pass
+    for (int item = warp * 8 + (lane >> 2); item < nq * R; item += (W + 1) * 8) {
         const int seg = queue[item / R], r = item % R;
         const int b = seg / Hkv, g = seg - b * Hkv;
         const int n = prefix[b + 1] - prefix[b];
         long long c_first;
         int pieces;
         segment_pieces((long long)prefix[b] * Hkv + (long long)g * n, n, C, U, c_first, pieces);
-        merge_row(a, b, g, r, c_first + seg, pieces, lane & 15);
+        merge_row(a, b, g, r, c_first + seg, pieces, lane & 3);
     }
 }
 
@@ -496,10 +520,10 @@ cudaError_t occupancy(size_t smem, int* per_sm) {
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, verify_split_kernel<W>, (W + 1) * 32, smem);
 }
 
-// Warps for R query rows: groups of 8 rows, rounded up to a power of two.
+// Consumer warps for R query rows: groups of 16 rows, rounded up to a power of two.
 int warps_for(int R) {
-    const int n = (R + 7) / 8;
-    return n <= 1 ? 1 : n <= 2 ? 2 : n <= 4 ? 4 : 8;
+    const int n = (R + 15) / 16;
+    return n <= 1 ? 1 : n <= 2 ? 2 : 4;
 }
 
 // Resident CTAs for (device, warps, shared memory), remembered so that repeated calls skip the query.
@@ -524,8 +548,7 @@ cudaError_t resident(int W, size_t smem, long long* ctas) {
     switch (W) {
         case 1: e = occupancy<1>(smem, &per_sm); break;
         case 2: e = occupancy<2>(smem, &per_sm); break;
-        case 4: e = occupancy<4>(smem, &per_sm); break;
-        default: e = occupancy<8>(smem, &per_sm); break;
+        default: e = occupancy<4>(smem, &per_sm); break;
     }
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
@@ -566,8 +589,7 @@ cudaError_t verify_launch(const VerifyArgs& args, const VerifyPlan& plan, const 
     switch (plan.warps) {
         case 1: verify_split_kernel<1><<<plan.grid, 64, plan.smem, stream>>>(tk, tv, a); break;
         case 2: verify_split_kernel<2><<<plan.grid, 96, plan.smem, stream>>>(tk, tv, a); break;
-        case 4: verify_split_kernel<4><<<plan.grid, 160, plan.smem, stream>>>(tk, tv, a); break;
-        default: verify_split_kernel<8><<<plan.grid, 288, plan.smem, stream>>>(tk, tv, a); break;
+        default: verify_split_kernel<4><<<plan.grid, 160, plan.smem, stream>>>(tk, tv, a); break;
     }
     return cudaGetLastError();
 }
