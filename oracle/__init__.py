@@ -53,7 +53,8 @@ def _load():
         _lib.oracle_decode_partials.argtypes = [i, i, i, i, i, i, i, P, P, P, P, P, P, f, i, i, i, P, P]
         _lib.oracle_merge.argtypes = [i, i, i, i, P, P, P, P, P]
         _lib.oracle_verify.argtypes = [i, i, i, i, i, i, i, i, P, P, P, P, P, P, f, i, P, P, P]
-        for fn in ("oracle_decode", "oracle_prefill", "oracle_decode_partials", "oracle_merge", "oracle_verify",
+        _lib.oracle_prefill_paged.argtypes = [i, P, P, i, i, i, i, i, i, i, P, P, P, P, P, f, i, P, P, P]
+        for fn in ("oracle_decode", "oracle_prefill", "oracle_decode_partials", "oracle_merge", "oracle_verify", "oracle_prefill_paged",
                    "oracle_num_threads"):
             getattr(_lib, fn).restype = ctypes.c_int
     return _lib
@@ -164,6 +165,56 @@ def prefill(q, k, v, cu_seqlens, sinks, scale, causal=True, rows=None):
                                 _ptr(sk), float(scale), int(bool(causal)), n, _ptr(rows),
                                 _ptr(out), _ptr(lse))
     _check(rc, "oracle.prefill")
+    return out, lse
+
+
+def kv_append(k, v, cu_seqlens, start_pos, page_table, k_pages, v_pages):
+    """Writing new tokens into their requests' pages, by definition (returns new pool arrays).
+
+    k/v [T,Hkv,D] bf16: the new tokens of N sequences packed by cu_seqlens [N+1]; new token i of
+    sequence n goes to cache position start_pos[n] + i, i.e. page page_table[n][pos // PS], slot
+    pos % PS.  k_pages/v_pages [P,Hkv,PS,D] bf16 are not modified.  Returns (k_pages, v_pages) as
+    bf16 bit patterns (uint16), every other slot unchanged.
+    """
+    kb, vb = _bf16_bits(k), _bf16_bits(v)
+    kp, vp = _bf16_bits(k_pages).copy(), _bf16_bits(v_pages).copy()
+    cu, sp, pt = _np(cu_seqlens, np.int32), _np(start_pos, np.int32), _np(page_table, np.int32)
+    PS = kp.shape[2]
+    for n in range(len(cu) - 1):
+        for i in range(int(cu[n + 1] - cu[n])):
+            pos = int(sp[n]) + i
+            page = int(pt[n, pos // PS])
+            if not 0 <= page < kp.shape[0]:
+                raise IndexError("oracle.kv_append: page id out of range")
+            kp[page, :, pos % PS] = kb[cu[n] + i]
+            vp[page, :, pos % PS] = vb[cu[n] + i]
+    return kp, vp
+
+
+def prefill_paged(q, k_pages, v_pages, page_table, cu_seqlens, start_pos, sinks, scale, rows=None):
+    """Chunked prefill over a paged cache by definition.
+
+    q [T,Hq,D] bf16: the new tokens of N sequences packed by cu_seqlens [N+1]; new token i of
+    sequence n sits at cache position start_pos[n] + i (its K/V already in the pages) and sees
+    cache tokens 0..that position.  k_pages/v_pages [P,Hkv,PS,D] (bf16 tensors or uint16 bit
+    arrays), page_table [N,max_pages].  rows: optional (t, h) pairs.  Returns (out, lse) float64.
+    """
+    q, kp, vp = _bf16_bits(q), _bf16_bits(k_pages), _bf16_bits(v_pages)
+    pt, cu, sp, sk = (_np(page_table, np.int32), _np(cu_seqlens, np.int32), _np(start_pos, np.int32),
+                      _np(sinks, np.float32))
+    T, Hq, D = q.shape
+    P, Hkv, PS, _ = kp.shape
+    if rows is not None:
+        rows = _np(rows, np.int32).reshape(-1, 2)
+        n = rows.shape[0]
+        out, lse = np.empty((n, D)), np.empty(n)
+    else:
+        n = T * Hq
+        out, lse = np.empty((T, Hq, D)), np.empty((T, Hq))
+    rc = _load().oracle_prefill_paged(len(cu) - 1, _ptr(cu), _ptr(sp), T, Hq, Hkv, D, PS, pt.shape[1], P, _ptr(q),
+                                      _ptr(kp), _ptr(vp), _ptr(pt), _ptr(sk), float(scale), n, _ptr(rows),
+                                      _ptr(out), _ptr(lse))
+    _check(rc, "oracle.prefill_paged")
     return out, lse
 
 

@@ -264,6 +264,71 @@ int oracle_prefill(int N, const int32_t *cu_seqlens, int T, int Hq, int Hkv, int
 }
 
 /*
+ * Chunked prefill over a paged cache.  Source: "Accelerating Sonar through
+ * speculation" (Perplexity), section "Inference with speculative decoding":
+ * input tokens are batched, slots for them are allocated in the per-request KV
+ * pages, the page metadata goes to the GPU and the batch runs as prefill,
+ * decode or verification over those pages.  Reading where the page is silent:
+ * the new tokens of sequence n (len_n = cu_seqlens[n+1] - cu_seqlens[n]) are
+ * already in its pages at cache positions start_pos[n] .. start_pos[n] + len_n - 1;
+ * new token i sees cache tokens 0 .. start_pos[n] + i (the cached prefix and the
+ * new tokens up to itself).
+ *   q [T, Hq, D] packed new tokens; k_pages, v_pages [num_pages, Hkv, PS, D];
+ *   page_table [N, max_pages]; start_pos [N]; sinks [Hq].
+ * rows: n_rows (t, h) pairs, or NULL for every (t, h) in order.
+ */
+int oracle_prefill_paged(int N, const int32_t *cu_seqlens, const int32_t *start_pos, int T, int Hq, int Hkv,
+                         int D, int PS, int max_pages, int num_pages, const uint16_t *q,
+                         const uint16_t *k_pages, const uint16_t *v_pages, const int32_t *page_table,
+                         const float *sinks, float scale, int n_rows, const int32_t *rows, double *out,
+                         double *lse) {
+    if (N < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || D <= 0 || PS <= 0) return ORACLE_BAD_ARG;
+    if (cu_seqlens[0] != 0 || cu_seqlens[N] != T) return ORACLE_BAD_ARG;
+    for (int n = 0; n < N; ++n)
+        if (cu_seqlens[n + 1] < cu_seqlens[n] || start_pos[n] < 0) return ORACLE_BAD_ARG;
+    const int G = Hq / Hkv;
+    const long total = rows ? n_rows : (long)T * Hq;
+    int status = ORACLE_OK;
+#pragma omp parallel
+    {
+        long cap = 0;
+        double *s = NULL;
+        const uint16_t **kp = NULL, **vp = NULL;
+#pragma omp for schedule(dynamic, 16)
+        for (long r = 0; r < total; ++r) {
+            long t = rows ? rows[2 * r] : r / Hq;
+            int h = rows ? rows[2 * r + 1] : (int)(r % Hq);
+            int n = 0;
+            while (cu_seqlens[n + 1] <= t) ++n; /* sequence holding token t */
+            long J = (long)start_pos[n] + (t - cu_seqlens[n]) + 1; /* cache tokens 0 .. its position */
+            if (J > cap) {
+                cap = J;
+                s = realloc(s, sizeof(double) * cap);
+                kp = realloc((void *)kp, sizeof(void *) * cap);
+                vp = realloc((void *)vp, sizeof(void *) * cap);
+            }
+            int bad = 0;
+            for (long j = 0; j < J; ++j) {
+                kp[j] = paged_row(k_pages, page_table, max_pages, num_pages, Hkv, PS, D, n, h / G, j);
+                vp[j] = paged_row(v_pages, page_table, max_pages, num_pages, Hkv, PS, D, n, h / G, j);
+                if (!kp[j]) bad = 1;
+            }
+            if (bad) {
+#pragma omp atomic write
+                status = ORACLE_BAD_PAGE;
+                continue;
+            }
+            sink_row(q + (t * Hq + h) * D, kp, vp, J, D, (double)sinks[h], 1, (double)scale, s, out + r * D,
+                     lse + r);
+        }
+        free(s);
+        free((void *)kp);
+        free((void *)vp);
+    }
+    return status;
+}
+
+/*
  * Split-KV partial results of decode: chunk c covers tokens
  * [c*chunk_tokens, (c+1)*chunk_tokens) of each request (possibly empty).
  *   sink_mode 0: the chunk holding token 0 (chunk 0) also holds the sink --

@@ -395,3 +395,77 @@ def test_verify_row_selection_matches_full_result():
     so, sl = oracle.verify(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens, inp.sinks, inp.scale, rows=rows)
     for n, (b, i, h) in enumerate(rows):
         assert np.array_equal(so[n], out[b, i, h]) and sl[n] == lse[b, i, h]
+
+
+# ---- chunked prefill over a paged cache, and writing new tokens into pages
+
+def _pool_from_sequences(seqs, Hkv, extra_tokens, seed):
+    """A permuted page pool holding each sequence's K/V [L, Hkv, 64] at positions 0..L-1, with room for
+    `extra_tokens` more tokens per sequence; returns (k_pages, v_pages, page_table)."""
+    g = torch.Generator().manual_seed(seed)
+    npg = [(k.shape[0] + extra + 15) // 16 for (k, _), extra in zip(seqs, extra_tokens)]
+    P = sum(npg)
+    perm = torch.randperm(P, generator=g)
+    pt = torch.full((len(seqs), max(npg)), -1, dtype=torch.int32)
+    kp = torch.randn(P, Hkv, 16, 64, generator=g).to(torch.bfloat16)  # unused slots hold noise
+    vp = torch.randn(P, Hkv, 16, 64, generator=g).to(torch.bfloat16)
+    off = 0
+    for n, ((k, v), m) in enumerate(zip(seqs, npg)):
+        pt[n, :m] = perm[off:off + m].to(torch.int32)
+        off += m
+        for t in range(k.shape[0]):
+            kp[pt[n, t // 16], :, t % 16] = k[t]
+            vp[pt[n, t // 16], :, t % 16] = v[t]
+    return kp, vp, pt
+
+
+def test_append_then_paged_prefill_equals_causal_prefill():
+    """Prefix in pages + new tokens appended into pages + paged prefill of the new tokens == the causal
+    prefill of the whole sequences (an independent causal rule and contiguous K/V)."""
+    Hq, Hkv = 8, 2
+    full = W.make_prefill(Hq, Hkv, [40, 23, 70], seed=41)
+    prefix = [17, 0, 64]  # cached tokens of each sequence; the rest is new
+    cu = full.cu_seqlens.tolist()
+    seqs = [(full.k[cu[n]:cu[n] + prefix[n]], full.v[cu[n]:cu[n] + prefix[n]]) for n in range(3)]
+    new_len = [cu[n + 1] - cu[n] - prefix[n] for n in range(3)]
+    kp, vp, pt = _pool_from_sequences(seqs, Hkv, new_len, seed=42)
+    sel = torch.cat([torch.arange(cu[n] + prefix[n], cu[n + 1]) for n in range(3)])
+    cu_new = torch.tensor([0] + list(np.cumsum(new_len)), dtype=torch.int32)
+    sp = torch.tensor(prefix, dtype=torch.int32)
+    kb, vb = oracle.kv_append(full.k[sel], full.v[sel], cu_new, sp, pt, kp, vp)
+    out, lse = oracle.prefill_paged(full.q[sel], kb, vb, pt, cu_new, sp, full.sinks, full.scale)
+    ro, rl = oracle.prefill(full.q, full.k, full.v, full.cu_seqlens, full.sinks, full.scale, True)
+    assert np.abs(out - ro[sel.numpy()]).max() <= TOL
+    assert np.abs(lse - rl[sel.numpy()]).max() <= TOL
+
+
+def test_kv_append_writes_only_its_slots():
+    inp = W.make_decode(2, 8, 2, [20, 5], seed=43, extra_pages=3, max_pages=4)
+    k = bf16(torch.randn(7, 2, 64))
+    v = bf16(torch.randn(7, 2, 64))
+    cu, sp = torch.tensor([0, 4, 7], dtype=torch.int32), torch.tensor([20, 5], dtype=torch.int32)
+    pt = inp.page_table.clone()
+    used = set(int(x) for x in inp.page_table.flatten() if x >= 0)
+    pt[0, 1] = min(set(range(inp.k_pages.shape[0])) - used)  # request 0's positions 16.. go to a spare page
+    kb, vb = oracle.kv_append(k, v, cu, sp, pt, inp.k_pages, inp.v_pages)
+    before = oracle._bf16_bits(inp.k_pages)
+    changed = np.argwhere(np.any(kb != before, axis=-1))
+    written = {(int(pt[n, (int(sp[n]) + i) // 16]), h, (int(sp[n]) + i) % 16)
+               for n in range(2) for i in range(int(cu[n + 1] - cu[n])) for h in range(2)}
+    assert {tuple(int(x) for x in c) for c in changed} <= written
+    for n in range(2):
+        for i in range(int(cu[n + 1] - cu[n])):
+            pos = int(sp[n]) + i
+            assert np.array_equal(kb[pt[n, pos // 16], :, pos % 16], oracle._bf16_bits(k)[cu[n] + i])
+            assert np.array_equal(vb[pt[n, pos // 16], :, pos % 16], oracle._bf16_bits(v)[cu[n] + i])
+
+
+def test_paged_prefill_with_uniform_chunks_is_verification():
+    QL = 3
+    inp = W.make_decode(3, 8, 2, [9, 40, 33], seed=44, q_len=QL)
+    vo, vl = oracle.verify(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens, inp.sinks, inp.scale)
+    cu = torch.arange(0, 3 * QL + 1, QL, dtype=torch.int32)
+    po, pl = oracle.prefill_paged(inp.q.reshape(3 * QL, 8, 64), inp.k_pages, inp.v_pages, inp.page_table, cu,
+                                  inp.kv_lens - QL, inp.sinks, inp.scale)
+    assert np.abs(po - vo.reshape(3 * QL, 8, 64)).max() <= TOL
+    assert np.abs(pl - vl.reshape(3 * QL, 8)).max() <= TOL
