@@ -135,6 +135,19 @@ sinkattn_status_t check_verify_dims(const sinkattn_verify_dims_t* d) {
     return SINKATTN_OK;
 }
 
+sinkattn_status_t check_paged_dims(const sinkattn_paged_dims_t* d, bool need_q_heads) {
+    if (!d) return SINKATTN_ERR_INVALID_ARG;
+    if (d->num_seqs < 0 || d->total_tokens < 0 || d->max_seqlen < 0 || d->num_kv_heads <= 0 || d->num_pages < 0 ||
+        d->max_pages < 1)
+        return SINKATTN_ERR_INVALID_ARG;
+    if (need_q_heads && (d->num_q_heads <= 0 || d->num_q_heads % d->num_kv_heads)) return SINKATTN_ERR_INVALID_ARG;
+    if (d->head_dim != kHeadDim || d->page_size != kPageSize) return SINKATTN_ERR_UNSUPPORTED;
+    if (d->num_seqs > 16384 || d->max_seqlen > (1 << 20)) return SINKATTN_ERR_UNSUPPORTED;
+    if ((long long)d->num_pages * d->num_kv_heads * kPageSize >= (1ll << 31)) return SINKATTN_ERR_UNSUPPORTED;
+    if ((long long)d->max_pages * kPageSize >= (1ll << 31)) return SINKATTN_ERR_UNSUPPORTED;
+    return SINKATTN_OK;
+}
+
 }  // namespace
 }  // namespace sinkattn
 
@@ -294,6 +307,87 @@ sinkattn_status_t sinkattn_verify(const void* q, const void* k_pages, const void
                                                                                             : SINKATTN_ERR_CUDA;
 }
 
+sinkattn_status_t sinkattn_kv_append(const void* k, const void* v, const int32_t* cu_seqlens, const int32_t* start_pos,
+                                     const int32_t* page_table, void* k_pages, void* v_pages,
+                                     const sinkattn_paged_dims_t* dims, void* stream) {
+    sinkattn_status_t st = check_paged_dims(dims, false);
+    if (st != SINKATTN_OK) return st;
+    if (dims->num_seqs == 0 || dims->total_tokens == 0) return SINKATTN_OK;
+    if (!k || !v || !cu_seqlens || !start_pos || !page_table || !k_pages || !v_pages) return SINKATTN_ERR_INVALID_ARG;
+    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) ||
+        !aligned(cu_seqlens, 4) || !aligned(start_pos, 4) || !aligned(page_table, 4))
+        return SINKATTN_ERR_INVALID_ARG;
+    DeviceState* ds = nullptr;
+    if ((st = device_state(&ds)) != SINKATTN_OK) return st;
+    AppendArgs a;
+    a.k = static_cast<const __nv_bfloat16*>(k);
+    a.v = static_cast<const __nv_bfloat16*>(v);
+    a.cu_seqlens = cu_seqlens;
+    a.start_pos = start_pos;
+    a.page_table = page_table;
+    a.k_pages = static_cast<__nv_bfloat16*>(k_pages);
+    a.v_pages = static_cast<__nv_bfloat16*>(v_pages);
+    a.err = ds->err;
+    a.N = dims->num_seqs;
+    a.T = dims->total_tokens;
+    a.Hkv = dims->num_kv_heads;
+    a.num_pages = dims->num_pages;
+    a.max_pages = dims->max_pages;
+    return kv_append_launch(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SINKATTN_OK : SINKATTN_ERR_CUDA;
+}
+
+sinkattn_status_t sinkattn_prefill_paged(const void* q, const void* k_pages, const void* v_pages,
+                                         const int32_t* page_table, const int32_t* cu_seqlens, const int32_t* start_pos,
+                                         const float* sinks, float scale, void* out, float* lse,
+                                         const sinkattn_paged_dims_t* dims, void* stream) {
+    sinkattn_status_t st = check_paged_dims(dims, true);
+    if (st != SINKATTN_OK) return st;
+    const sinkattn_paged_dims_t& d = *dims;
+    if (d.num_seqs == 0 || d.total_tokens == 0 || d.max_seqlen == 0) return SINKATTN_OK;
+    if (!q || !page_table || !cu_seqlens || !start_pos || !sinks || !out) return SINKATTN_ERR_INVALID_ARG;
+    if (d.num_pages > 0 && (!k_pages || !v_pages)) return SINKATTN_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(out, 16) ||
+        !aligned(page_table, 4) || !aligned(cu_seqlens, 4) || !aligned(start_pos, 4) || !aligned(sinks, 4) ||
+        (lse && !aligned(lse, 4)))
+        return SINKATTN_ERR_INVALID_ARG;
+    if (!(scale == scale)) return SINKATTN_ERR_INVALID_ARG;
+    DeviceState* ds = nullptr;
+    if ((st = device_state(&ds)) != SINKATTN_OK) return st;
+    CUtensorMap tq, tk, tv;
+    std::memset(&tk, 0, sizeof tk);
+    std::memset(&tv, 0, sizeof tv);
+    if (!encode_thd(&tq, q, d.total_tokens, d.num_q_heads, 128)) return SINKATTN_ERR_INVALID_ARG;
+    // With an empty pool every page reads as out of range (zero-filled copies from a map over one
+    // row would still need a pool), so an empty pool is only accepted without cached tokens.
+    const unsigned long long rows = (unsigned long long)d.num_pages * d.num_kv_heads * kPageSize;
+    if (rows == 0) return SINKATTN_ERR_INVALID_ARG;
+    if (!encode_rows(&tk, k_pages, rows, 128, kPageSize) || !encode_rows(&tv, v_pages, rows, 128, kPageSize))
+        return SINKATTN_ERR_INVALID_ARG;
+    PrefillArgs a;
+    a.q = static_cast<const __nv_bfloat16*>(q);
+    a.k = static_cast<const __nv_bfloat16*>(k_pages);
+    a.v = static_cast<const __nv_bfloat16*>(v_pages);
+    a.cu_seqlens = cu_seqlens;
+    a.sinks = sinks;
+    a.out = static_cast<__nv_bfloat16*>(out);
+    a.lse = lse;
+    a.err = ds->err;
+    a.N = d.num_seqs;
+    a.T = d.total_tokens;
+    a.max_seqlen = d.max_seqlen;
+    a.Hq = d.num_q_heads;
+    a.Hkv = d.num_kv_heads;
+    a.G = d.num_q_heads / d.num_kv_heads;
+    a.causal = 1;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.page_table = page_table;
+    a.start_pos = start_pos;
+    a.num_pages = d.num_pages;
+    a.max_pages = d.max_pages;
+    const cudaError_t e = prefill_paged_launch(a, tq, tk, tv, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SINKATTN_OK : SINKATTN_ERR_CUDA;
+}
+
 sinkattn_status_t sinkattn_prefill(const void* q, const void* k, const void* v, const int32_t* cu_seqlens,
                                    const float* sinks, float scale, int32_t causal, void* out, float* lse,
                                    const sinkattn_prefill_dims_t* dims, void* stream) {
@@ -330,6 +424,9 @@ sinkattn_status_t sinkattn_prefill(const void* q, const void* k, const void* v, 
     a.G = d.num_q_heads / d.num_kv_heads;
     a.causal = causal ? 1 : 0;
     a.scale_log2 = scale * 1.4426950408889634f;
+    a.page_table = nullptr;
+    a.start_pos = nullptr;
+    a.num_pages = a.max_pages = 0;
     cudaError_t e;
     const PrefillKernel which = prefill_kernel_choice();
     if (which == PrefillKernel::kLegacy) {

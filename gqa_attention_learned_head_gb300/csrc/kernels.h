@@ -73,6 +73,20 @@ cudaError_t verify_plan(int B, int QL, int Hq, int Hkv, int num_workers, VerifyP
 cudaError_t verify_launch(const VerifyArgs& args, const VerifyPlan& plan, const CUtensorMap& tmap_k,
                           const CUtensorMap& tmap_v, cudaStream_t stream);
 
+// ------------------------------------------------------------------ paged cache: append
+struct AppendArgs {
+    const __nv_bfloat16* k;     // [T, Hkv, 64] new tokens, packed by cu_seqlens
+    const __nv_bfloat16* v;     // [T, Hkv, 64]
+    const int32_t* cu_seqlens;  // [N+1]
+    const int32_t* start_pos;   // [N] cache position of each sequence's first new token
+    const int32_t* page_table;  // [N, max_pages]
+    __nv_bfloat16* k_pages;     // [P, Hkv, 16, 64]
+    __nv_bfloat16* v_pages;
+    unsigned* err;
+    int N, T, Hkv, num_pages, max_pages;
+};
+cudaError_t kv_append_launch(const AppendArgs& args, cudaStream_t stream);
+
 // ------------------------------------------------------------------ merge
 struct MergeArgs {
     const float* part_o;    // [S, R, H, 64]
@@ -96,6 +110,10 @@ struct PrefillArgs {
     unsigned* err;
     int N, T, max_seqlen, Hq, Hkv, G, causal;
     float scale_log2;
+    // paged cache (sinkattn_prefill_paged only): k / v come from [P, Hkv, 16, 64] pools
+    const int32_t* page_table;  // [N, max_pages]
+    const int32_t* start_pos;   // [N] cache position of each sequence's first new token
+    int num_pages, max_pages;
 };
 // Tensor-core (tcgen05) prefill; the tensor maps are built by the caller.
 cudaError_t prefill_tc_launch(const PrefillArgs& args, const CUtensorMap& tmap_q, const CUtensorMap& tmap_k,
@@ -103,6 +121,9 @@ cudaError_t prefill_tc_launch(const PrefillArgs& args, const CUtensorMap& tmap_q
 // tcgen05 prefill over two query heads of one KV group per CTA (group size must be even).
 cudaError_t prefill_pp_launch(const PrefillArgs& args, const CUtensorMap& tmap_q, const CUtensorMap& tmap_k,
                               const CUtensorMap& tmap_v, cudaStream_t stream);
+// Chunked prefill over a paged cache (one-head tcgen05 kernel, K / V gathered page by page).
+cudaError_t prefill_paged_launch(const PrefillArgs& args, const CUtensorMap& tmap_q, const CUtensorMap& tmap_k,
+                                 const CUtensorMap& tmap_v, cudaStream_t stream);
 // Warp-level mma.sync prefill, kept as the legacy-tensor-path baseline.
 cudaError_t prefill_mma_launch(const PrefillArgs& args, cudaStream_t stream);
 

@@ -41,6 +41,11 @@ class VerifyDims(ctypes.Structure):
                                               "page_size", "num_pages", "max_pages", "num_workers")]
 
 
+class PagedDims(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("num_seqs", "total_tokens", "max_seqlen", "num_q_heads", "num_kv_heads",
+                                              "head_dim", "page_size", "num_pages", "max_pages")]
+
+
 class PrefillDims(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("num_seqs", "total_tokens", "max_seqlen", "num_q_heads",
                                               "num_kv_heads", "head_dim")]
@@ -51,7 +56,7 @@ class MergeDims(ctypes.Structure):
 
 
 EXPORTS = ("sinkattn_decode", "sinkattn_prefill", "sinkattn_merge", "sinkattn_decode_workspace_size", "sinkattn_verify",
-           "sinkattn_verify_workspace_size",
+           "sinkattn_verify_workspace_size", "sinkattn_kv_append", "sinkattn_prefill_paged",
            "sinkattn_get_error", "sinkattn_status_string", "sinkattn_version")
 
 
@@ -71,11 +76,14 @@ def _load():
     lib.sinkattn_verify.argtypes = [P, P, P, P, P, P, f32, P, P, ctypes.POINTER(VerifyDims), P, sz, P]
     lib.sinkattn_verify_workspace_size.argtypes = [ctypes.POINTER(VerifyDims)]
     lib.sinkattn_verify_workspace_size.restype = sz
+    lib.sinkattn_kv_append.argtypes = [P, P, P, P, P, P, P, ctypes.POINTER(PagedDims), P]
+    lib.sinkattn_prefill_paged.argtypes = [P, P, P, P, P, P, P, f32, P, P, ctypes.POINTER(PagedDims), P]
     lib.sinkattn_get_error.argtypes = [P]
     lib.sinkattn_status_string.argtypes = [ctypes.c_int]
     lib.sinkattn_status_string.restype = ctypes.c_char_p
     lib.sinkattn_version.restype = i32
-    for fn in ("sinkattn_decode", "sinkattn_prefill", "sinkattn_merge", "sinkattn_get_error", "sinkattn_verify"):
+    for fn in ("sinkattn_decode", "sinkattn_prefill", "sinkattn_merge", "sinkattn_get_error", "sinkattn_verify",
+               "sinkattn_kv_append", "sinkattn_prefill_paged"):
         getattr(lib, fn).restype = ctypes.c_int
     return lib
 
@@ -199,6 +207,55 @@ def sinkattn_verify(q, k_pages, v_pages, page_table, kv_lens, sinks, scale, out=
                               float(scale), _ptr(out), _ptr(lse), ctypes.byref(dims), _ptr(workspace),
                               workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "sinkattn_verify")
+    return out, lse
+
+
+def paged_dims(k_pages, page_table, cu_seqlens, total_tokens, max_seqlen, num_q_heads=0) -> PagedDims:
+    P, Hkv, PS, D = k_pages.shape
+    return PagedDims(cu_seqlens.shape[0] - 1, total_tokens, max_seqlen, num_q_heads, Hkv, D, PS, P,
+                     page_table.shape[1])
+
+
+def sinkattn_kv_append(k, v, cu_seqlens, start_pos, page_table, k_pages, v_pages, max_seqlen=0, stream=None):
+    """Writes new tokens' k / v [T, Hkv, 64] into the pages, in place, at cache positions start_pos[n] + i."""
+    _need(k, "k", torch.bfloat16, 3)
+    _need(v, "v", torch.bfloat16, 3)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    _need(start_pos, "start_pos", torch.int32, 1)
+    _need(page_table, "page_table", torch.int32, 2)
+    _need(k_pages, "k_pages", torch.bfloat16, 4)
+    _need(v_pages, "v_pages", torch.bfloat16, 4)
+    if v.shape != k.shape or v_pages.shape != k_pages.shape or k.shape[1] != k_pages.shape[1]:
+        raise ValueError("inconsistent append shapes")
+    dims = paged_dims(k_pages, page_table, cu_seqlens, k.shape[0], max_seqlen)
+    st = _lib.sinkattn_kv_append(_ptr(k), _ptr(v), _ptr(cu_seqlens), _ptr(start_pos), _ptr(page_table),
+                                 _ptr(k_pages), _ptr(v_pages), ctypes.byref(dims), _stream(stream))
+    _check(st, "sinkattn_kv_append")
+
+
+def sinkattn_prefill_paged(q, k_pages, v_pages, page_table, cu_seqlens, start_pos, sinks, scale, max_seqlen=None,
+                           out=None, lse=None, return_lse=True, stream=None):
+    """Chunked prefill of new tokens q [T, Hq, 64] over the paged cache (their K/V already appended):
+    new token i of sequence n sees cache tokens 0 .. start_pos[n] + i.  Returns (out, lse)."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_pages, "k_pages", torch.bfloat16, 4)
+    _need(v_pages, "v_pages", torch.bfloat16, 4)
+    _need(page_table, "page_table", torch.int32, 2)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    _need(start_pos, "start_pos", torch.int32, 1)
+    _need(sinks, "sinks", torch.float32, 1)
+    if max_seqlen is None:
+        raise ValueError("max_seqlen is required (an upper bound of the new tokens per sequence)")
+    T, Hq, D = q.shape
+    dims = paged_dims(k_pages, page_table, cu_seqlens, T, max_seqlen, Hq)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty(T, Hq, device=q.device, dtype=torch.float32)
+    st = _lib.sinkattn_prefill_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table), _ptr(cu_seqlens),
+                                     _ptr(start_pos), _ptr(sinks), float(scale), _ptr(out), _ptr(lse),
+                                     ctypes.byref(dims), _stream(stream))
+    _check(st, "sinkattn_prefill_paged")
     return out, lse
 
 

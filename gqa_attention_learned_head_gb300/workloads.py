@@ -135,6 +135,73 @@ def make_decode(B, Hq, Hkv, kv_lens, seed=0, sink_std=1.0, contiguous=False,
                         sinks, 1.0 / math.sqrt(D))
 
 
+@dataclass
+class PagedPrefillInputs:
+    q: torch.Tensor           # [T, Hq, D] bf16   new tokens packed by cu_seqlens
+    k_new: torch.Tensor       # [T, Hkv, D] bf16  their keys, to be appended to the pages
+    v_new: torch.Tensor       # [T, Hkv, D] bf16
+    k_pages: torch.Tensor     # [P, Hkv, PS, D] bf16  holds the cached prefixes
+    v_pages: torch.Tensor
+    page_table: torch.Tensor  # [N, max_pages] int32, room for prefix + new tokens
+    cu_seqlens: torch.Tensor  # [N+1] int32 over the new tokens
+    start_pos: torch.Tensor   # [N] int32 cached tokens of each sequence
+    sinks: torch.Tensor       # [Hq] f32
+    scale: float
+    new_lens: list = field(default_factory=list)
+
+    def to(self, device):
+        return PagedPrefillInputs(*(t.to(device) for t in (self.q, self.k_new, self.v_new, self.k_pages,
+                                                           self.v_pages, self.page_table, self.cu_seqlens,
+                                                           self.start_pos, self.sinks)),
+                                  self.scale, list(self.new_lens))
+
+    @property
+    def max_seqlen(self) -> int:
+        return max(self.new_lens) if self.new_lens else 0
+
+    def visible_pairs(self) -> int:
+        """(new token, visible cached token) pairs per head."""
+        return sum(L * s + L * (L + 1) // 2 for L, s in zip(self.new_lens, self.start_pos.tolist()))
+
+
+def make_paged_prefill(Hq, Hkv, prefix_lens, new_lens, seed=0, device="cpu", D=HEAD_DIM, PS=PAGE_SIZE):
+    """Chunked prefill inputs over a paged cache.
+
+    prefix_lens / new_lens: lists of N ints, or (lo, hi) tuples for inclusive-uniform lengths (N from
+    the other argument, or 8).  Each sequence gets the pages for prefix + new tokens, randomly
+    permuted in the pool; the pool is drawn whole (the prefix slots hold the cached K/V, the others
+    noise that the appended tokens overwrite).  Draw order: lengths -> page permutation -> q ->
+    k_pages -> v_pages -> k_new -> v_new -> sinks.
+    """
+    g = _generator(seed, device)
+    N = len(prefix_lens) if isinstance(prefix_lens, list) else (len(new_lens) if isinstance(new_lens, list) else 8)
+
+    def draw(spec):
+        if isinstance(spec, tuple):
+            return torch.randint(spec[0], spec[1] + 1, (N,), generator=g, device=device).cpu().tolist()
+        return [int(x) for x in spec]
+
+    pre, new = draw(prefix_lens), draw(new_lens)
+    npages = [(p + n + PS - 1) // PS for p, n in zip(pre, new)]
+    P = max(sum(npages), 1)
+    perm = torch.randperm(P, generator=g, device=device).cpu()
+    pt = torch.full((N, max(max(npages, default=0), 1)), -1, dtype=torch.int32)
+    off = 0
+    for b, n in enumerate(npages):
+        pt[b, :n] = perm[off:off + n].to(torch.int32)
+        off += n
+    T = sum(new)
+    q = _normal_bf16(g, (T, Hq, D), device)
+    kp = _normal_bf16(g, (P, Hkv, PS, D), device)
+    vp = _normal_bf16(g, (P, Hkv, PS, D), device)
+    kn = _normal_bf16(g, (T, Hkv, D), device)
+    vn = _normal_bf16(g, (T, Hkv, D), device)
+    sinks = torch.randn(Hq, generator=g, device=device, dtype=torch.float32)
+    cu = torch.tensor([0] + list(torch.tensor(new).cumsum(0).tolist()), dtype=torch.int32, device=device)
+    return PagedPrefillInputs(q, kn, vn, kp, vp, pt.to(device), cu, torch.tensor(pre, dtype=torch.int32, device=device),
+                              sinks, 1.0 / math.sqrt(D), new)
+
+
 def make_prefill(Hq, Hkv, seqlens, seed=0, causal=True, device="cpu", D=HEAD_DIM,
                  sink_std=1.0) -> PrefillInputs:
     """Packed varlen prefill inputs; seqlens: list, or (N, lo, hi) for inclusive-uniform."""
@@ -185,6 +252,12 @@ LONG_CONTEXT_CHUNKS = 32  # the long-context workload splits each request into 3
 def causal_prefill(device="cpu", seed=0):
     """Two sequences of 8192 tokens, 64 q / 8 KV heads, causal."""
     return make_prefill(64, 8, [8192, 8192], seed=seed, device=device)
+
+
+def chunked_prefill(device="cpu", seed=0):
+    """Chunked prefill over the paged cache: 8 sequences with U[1024, 8192] cached tokens each taking
+    U[256, 2048] new tokens, 64 q / 8 KV heads."""
+    return make_paged_prefill(64, 8, (1024, 8192), (256, 2048), seed=seed, device=device)
 
 
 def mixed_serving_prefill(device="cpu", seed=0):

@@ -174,6 +174,72 @@ sinkattn_status_t sinkattn_verify(const void *q, const void *k_pages, const void
                                   const sinkattn_verify_dims_t *dims, void *workspace,
                                   size_t workspace_bytes, void *stream);
 
+/* Shapes of the calls over a paged cache that take new tokens packed by cu_seqlens. */
+typedef struct {
+    int32_t num_seqs;          /* N sequences (requests), 0..16384                        */
+    int32_t total_tokens;      /* T new tokens, packed by cu_seqlens                      */
+    int32_t max_seqlen;        /* >= the largest number of new tokens of one sequence     */
+    int32_t num_q_heads;       /* Hq (read by sinkattn_prefill_paged only)                */
+    int32_t num_kv_heads;      /* Hkv, divides Hq                                         */
+    int32_t head_dim;          /* must be 64                                              */
+    int32_t page_size;         /* must be 16                                              */
+    int32_t num_pages;         /* P, pages in the K/V pools                               */
+    int32_t max_pages;         /* row length of page_table (>= 1)                         */
+} sinkattn_paged_dims_t;
+
+/*
+ * Writes the keys and values of new tokens into their requests' pages.
+ * Source: "Accelerating Sonar through speculation", section "Inference with
+ * speculative decoding": slots for the next tokens are allocated in the
+ * per-request KV pages before the batch runs.
+ *
+ *   k, v        [T, Hkv, 64]     bf16   new tokens of N sequences, packed by cu_seqlens
+ *   cu_seqlens  [N + 1]          int32  cu_seqlens[0] = 0, non-decreasing, cu_seqlens[N] = T
+ *   start_pos   [N]              int32  cache position of each sequence's first new token
+ *                                       (the number of tokens already cached)
+ *   page_table  [N, max_pages]   int32  token at cache position p of sequence n goes to page
+ *                                       page_table[n][p / 16], slot p % 16
+ *   k_pages, v_pages [P, Hkv, 16, 64] bf16, written in place (only the new tokens' slots)
+ *
+ * A page id outside [0, P) skips its tokens and raises SINKATTN_ERR_BAD_PAGE; a
+ * position past max_pages * 16 skips the token and raises SINKATTN_ERR_BAD_LENGTH.
+ */
+sinkattn_status_t sinkattn_kv_append(const void *k, const void *v, const int32_t *cu_seqlens,
+                                     const int32_t *start_pos, const int32_t *page_table,
+                                     void *k_pages, void *v_pages, const sinkattn_paged_dims_t *dims,
+                                     void *stream);
+
+/*
+ * Chunked prefill over the paged cache: new tokens of N sequences attend to
+ * everything cached before them and to the new tokens up to themselves.
+ * Source: "Accelerating Sonar through speculation", section "Inference with
+ * speculative decoding" (batches of prefill, decode or verification run over
+ * the per-request KV pages); the attention is the sink attention of
+ * sinkattn_prefill ("GPT-OSS on day 0", section "Kernels for GPT-OSS / Sink
+ * Attention").
+ *
+ * The new tokens' keys and values must already be in the pages
+ * (sinkattn_kv_append): new token i of sequence n sits at cache position
+ * start_pos[n] + i and sees cache tokens 0 .. start_pos[n] + i.
+ *
+ *   q           [T, Hq, 64]   bf16   new tokens packed by cu_seqlens
+ *   k_pages, v_pages [P, Hkv, 16, 64] bf16 (P >= 1), page_table [N, max_pages] int32,
+ *   cu_seqlens [N + 1], start_pos [N]: as sinkattn_kv_append
+ *   sinks [Hq] f32, scale: as sinkattn_prefill
+ *   out         [T, Hq, 64]   bf16;  lse [T, Hq] f32 natural log, or NULL
+ *
+ * dims->max_seqlen bounds the new tokens of one sequence (a longer one is cut and
+ * raises SINKATTN_ERR_BAD_LENGTH, as does start_pos[n] + len_n > max_pages * 16).
+ * A page id outside [0, P) raises SINKATTN_ERR_BAD_PAGE; its tokens then read as
+ * zero vectors and that sequence's result is not meaningful.  Slots past a
+ * sequence's last cached token may hold anything.
+ */
+sinkattn_status_t sinkattn_prefill_paged(const void *q, const void *k_pages, const void *v_pages,
+                                         const int32_t *page_table, const int32_t *cu_seqlens,
+                                         const int32_t *start_pos, const float *sinks, float scale,
+                                         void *out, float *lse, const sinkattn_paged_dims_t *dims,
+                                         void *stream);
+
 /*
  * Causal (or full) prefill over packed variable-length sequences.
  * Source: "GPT-OSS on day 0", section "Kernels for GPT-OSS / Sink Attention"

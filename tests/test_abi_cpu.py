@@ -85,3 +85,17 @@ def test_verify_host_validation_without_device(S):
     assert call(S.VerifyDims(2, 4, 8, 2, 32, 16, 10, 4, 0)) == S.ERR_UNSUPPORTED       # head_dim 32
     assert lib.sinkattn_verify_workspace_size(ctypes.byref(S.VerifyDims(2, 9, 64, 8, 64, 16, 10, 4, 0))) == 0
     assert call(S.VerifyDims(0, 4, 8, 2, 64, 16, 10, 4, 0)) == 0                       # empty batch: nothing to do
+
+
+def test_paged_host_validation_without_device(S):
+    lib = S._lib
+    d = S.PagedDims(2, 10, 8, 8, 2, 32, 16, 10, 4)  # head_dim 32
+    assert lib.sinkattn_kv_append(*([None] * 7), ctypes.byref(d), None) == S.ERR_UNSUPPORTED
+    assert lib.sinkattn_prefill_paged(*([None] * 7), 0.125, None, None, ctypes.byref(d), None) == S.ERR_UNSUPPORTED
+    d = S.PagedDims(2, 10, 8, 8, 3, 64, 16, 10, 4)  # Hq % Hkv != 0
+    assert lib.sinkattn_prefill_paged(*([None] * 7), 0.125, None, None, ctypes.byref(d), None) == S.ERR_INVALID_ARG
+    d = S.PagedDims(2, 10, 8, 8, 2, 64, 16, 10, 0)  # max_pages 0
+    assert lib.sinkattn_kv_append(*([None] * 7), ctypes.byref(d), None) == S.ERR_INVALID_ARG
+    d = S.PagedDims(0, 0, 0, 8, 2, 64, 16, 10, 4)  # nothing to do
+    assert lib.sinkattn_kv_append(*([None] * 7), ctypes.byref(d), None) == 0
+    assert lib.sinkattn_prefill_paged(*([None] * 7), 0.125, None, None, ctypes.byref(d), None) == 0
