@@ -2,7 +2,8 @@
 """Benchmark of libsinkattn (sink attention, GQA, paged split-KV decode + causal prefill).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload batched_paged_decode|long_context_decode|speculative_verify|causal_prefill]
+                    [--workload batched_paged_decode|long_context_decode|speculative_verify|causal_prefill|
+                                chunked_prefill]
 
 Headline: decode KV GB/s on the batched paged decode workload (batch 32,
 64 q / 8 KV heads, head_dim 64, kv_len uniform in [512, 4096], 16-token pages
@@ -10,7 +11,8 @@ randomly permuted in the pool).  One step = one sinkattn_decode call (split
 pass + merge), i.e. the whole decode hot path, on inputs resident in HBM.
 The L2 is flushed (256 MiB write, then a 512 MiB read) before every timed step.  Secondary lines
 for the long-context split-KV decode, the verification of drafted tokens (4 per request), the
-causal prefill and the mixed serving batch ride in the same JSON object under "secondary".
+causal prefill, the chunked prefill over the paged cache and the mixed serving batch ride in the
+same JSON object under "secondary".
 
 Prints ONE JSON line on rank 0.  Under torchrun every rank runs its own
 independent batch (weak scaling, no collective on the data path); the
@@ -47,6 +49,9 @@ WORKLOAD_TEXT = {
     "long_context_decode": "long-context split-KV decode: batch 4, 64 q / 8 KV heads, head_dim 64, kv_len 131072, "
                            "32 chunks per request merged by LSE",
     "causal_prefill": "causal prefill: 2 x 8192 tokens (varlen), 64 q / 8 KV heads, head_dim 64",
+    "chunked_prefill": "chunked prefill over the paged cache: 8 sequences, U[1024,8192] cached + U[256,2048] new "
+                       "tokens each, 64 q / 8 KV heads, head_dim 64; one step = append the new K/V into the pages "
+                       "+ paged prefill",
     "speculative_verify": "verification of drafts: batch 32, 4 query tokens per request over the paged cache, "
                           "64 q / 8 KV heads, head_dim 64, kv_len U[512,4096] (drafts included), permuted pages",
     "mixed_serving": "mixed serving batch: 8 causal prefills L~U[256,4096] + 256 paged decodes kv_len~U[1024,32768], "
@@ -271,6 +276,27 @@ def bench_verify(S, W, rank, K, warmup, flush, stream):
     return inp, step, times, decode_bytes(inp.kv_lens, Hkv, D)
 
 
+def bench_chunked(S, W, rank, K, warmup, flush, stream):
+    """One step = the serving step of a chunked prefill: append the new tokens' K/V into the pages,
+    then the paged prefill over prefix + new tokens.  Returns the attention flops per step."""
+    inp = W.chunked_prefill(device="cuda", seed=rank)
+    out = torch.empty_like(inp.q)
+    lse = torch.empty(inp.q.shape[0], inp.q.shape[1], dtype=torch.float32, device="cuda")
+
+    def step():
+        S.sinkattn_kv_append(inp.k_new, inp.v_new, inp.cu_seqlens, inp.start_pos, inp.page_table, inp.k_pages,
+                             inp.v_pages, stream=stream)
+        S.sinkattn_prefill_paged(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.cu_seqlens, inp.start_pos,
+                                 inp.sinks, inp.scale, max_seqlen=inp.max_seqlen, out=out, lse=lse, stream=stream)
+
+    with torch.cuda.stream(stream):
+        times = timed_steps(step, K, warmup, flush, stream)
+    err = S.sinkattn_get_error(stream)
+    if err:
+        raise RuntimeError(f"device error {S.status_string(err)}")
+    return inp, step, times, 4 * 64 * inp.q.shape[1] * inp.visible_pairs()
+
+
 def bench_prefill(S, W, name, rank, K, warmup, flush, stream):
     inp = (W.mixed_serving_prefill if name == "mixed_serving" else W.causal_prefill)(device="cuda", seed=rank)
     out = torch.empty_like(inp.q)
@@ -314,6 +340,32 @@ def cpu_baseline_decode(inp, budget_s=12.0):
     dt = time.perf_counter() - t0
     return {"value": done_bytes / dt / 1e9, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"{reqs} whole requests (all {QL} x {Hq} query rows) of the same workload, fp64, {dt:.1f} s"}
+
+
+def cpu_baseline_chunked(inp, budget_s=8.0):
+    """The fp64 oracle (append, then paged prefill of random rows) on the host cores."""
+    import numpy as np
+
+    import oracle
+
+    kb, vb = oracle.kv_append(inp.k_new, inp.v_new, inp.cu_seqlens, inp.start_pos, inp.page_table, inp.k_pages,
+                              inp.v_pages)
+    q, pt, cu, sp, sk = inp.q.cpu(), inp.page_table.cpu(), inp.cu_seqlens.cpu(), inp.start_pos.cpu(), inp.sinks.cpu()
+    T, Hq, _ = q.shape
+    rng = np.random.default_rng(0)
+    cul, spl = cu.tolist(), sp.tolist()
+    pairs, n = 0, 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < budget_s:
+        t = int(rng.integers(0, T))
+        rows = np.stack([np.full(Hq, t), np.arange(Hq)], 1).astype(np.int32)
+        oracle.prefill_paged(q, kb, vb, pt, cu, sp, sk, inp.scale, rows=rows)
+        s = max(i for i in range(len(cul) - 1) if cul[i] <= t)
+        pairs += (spl[s] + t - cul[s] + 1) * Hq
+        n += 1
+    dt = time.perf_counter() - t0
+    return {"value": 4 * 64 * pairs / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{n} random new-token rows (all {Hq} heads) of the workload after the append, fp64, {dt:.1f} s"}
 
 
 def cpu_baseline_prefill(inp, budget_s=8.0):
@@ -427,6 +479,25 @@ def run_ours(args):
                 "traffic": profiled_traffic(kname, name, [ksrc, "ptx.cuh", "kernels.h", "split_kv.cuh"])}
         launches = K  # one split kernel per step
         cfg_extra = {"kv_tokens": int(inp.kv_lens.sum()), "kv_bytes_per_step": nbytes}
+    elif name == "chunked_prefill":
+        inp, step, times, flops = bench_chunked(S, W, rank, K, Wu, flush, stream)
+        total_flops = sum_over_ranks(float(flops), world)
+        ms = statistics.mean(times)
+        torch.cuda.synchronize()
+        barrier(world)
+        ms_max = max_over_ranks(ms, world)
+        value = total_flops / (ms_max * 1e-3) / 1e12
+        unit = "TFLOP/s"
+        achieved = flops / (ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "kernel": "prefill_tc_kernel<paged> + kv_append_kernel (the two kernels of a "
+                                             "step); achieved over the whole step",
+                "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s", "frac": achieved / tc_peak,
+                "peak_source": f"{peak_src} bf16_tflops",
+                "traffic": profiled_traffic("prefill_tc_kernel_paged", name,
+                                            ["prefill_tc.cu", "ptx.cuh", "kernels.h", "tile_order.cuh"])}
+        launches = 2 * K  # append + paged prefill per step
+        cfg_extra = {"new_tokens": int(inp.q.shape[0]), "cached_tokens": int(inp.start_pos.sum()),
+                     "flops_per_step": flops}
     else:
         inp, step, times, flops = bench_prefill(S, W, name, rank, K, Wu, flush, stream)
         total_flops = sum_over_ranks(float(flops), world)
@@ -459,6 +530,33 @@ def run_ours(args):
     e2e = None
     if args.kernels_only:
         pass
+    elif name == "chunked_prefill":
+        srcs = (inp.q, inp.k_new, inp.v_new, inp.cu_seqlens, inp.start_pos, inp.page_table)
+        h_in = [t.cpu().pin_memory() for t in srcs]
+        d_in = [torch.empty_like(t) for t in srcs]
+        h_out = torch.empty(inp.q.shape, dtype=torch.bfloat16).pin_memory()
+        h_lse = torch.empty(inp.q.shape[:2], dtype=torch.float32).pin_memory()
+        d_out = torch.empty_like(inp.q)
+        d_lse = torch.empty(inp.q.shape[:2], dtype=torch.float32, device="cuda")
+
+        def e2e_step():
+            for h, d in zip(h_in, d_in):
+                d.copy_(h, non_blocking=True)
+            q, kn, vn, cu, sp, pt = d_in
+            S.sinkattn_kv_append(kn, vn, cu, sp, pt, inp.k_pages, inp.v_pages, stream=stream)
+            S.sinkattn_prefill_paged(q, inp.k_pages, inp.v_pages, pt, cu, sp, inp.sinks, inp.scale,
+                                     max_seqlen=inp.max_seqlen, out=d_out, lse=d_lse, stream=stream)
+            h_out.copy_(d_out, non_blocking=True)
+            h_lse.copy_(d_lse, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            et = timed_steps(e2e_step, K, Wu, flush, stream)
+        e_ms = max_over_ranks(statistics.mean(et), world)
+        e2e = {"value": total_flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e_ms,
+               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in h_in),
+               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in (h_out, h_lse)),
+               "note": "the page pools stay resident (they are the cache); new tokens' q/k/v and the metadata "
+                       "come from pinned host memory every step and the output + lse are read back"}
     elif name == "causal_prefill":
         h_in = [t.cpu().pin_memory() for t in (inp.q, inp.k, inp.v, inp.cu_seqlens)]
         d_in = [torch.empty_like(t) for t in (inp.q, inp.k, inp.v, inp.cu_seqlens)]
@@ -540,13 +638,20 @@ def run_ours(args):
                               "unit": "TFLOP/s", "ms_per_step": pms,
                               "frac_of_bf16_peak": pf / (pms * 1e-3) / 1e12 / tc_peak})
             del pi
+            ci, _, ct, cf = bench_chunked(S, W, rank, Ks, Wu, flush, stream)
+            cms = statistics.mean(ct)
+            secondary.append({"workload": WORKLOAD_TEXT["chunked_prefill"], "value": cf / (cms * 1e-3) / 1e12,
+                              "unit": "TFLOP/s", "ms_per_step": cms,
+                              "frac_of_bf16_peak": cf / (cms * 1e-3) / 1e12 / tc_peak})
+            del ci
             secondary.append(bench_mixed(S, W, rank, Ks, Wu, flush, hbm_peak, tc_peak))
         except Exception as e:  # report, never hide
             secondary.append({"error": f"{type(e).__name__}: {e}"})
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline_decode(inp) if unit == "GB/s" else cpu_baseline_prefill(inp)
+        cpu = (cpu_baseline_decode(inp) if unit == "GB/s" else
+               cpu_baseline_chunked(inp) if name == "chunked_prefill" else cpu_baseline_prefill(inp))
 
     clocks = None
     if sampler:
@@ -608,7 +713,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="batched_paged_decode",
                     choices=["batched_paged_decode", "long_context_decode", "tiny_decode", "speculative_verify",
-                             "causal_prefill"])
+                             "causal_prefill", "chunked_prefill"])
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernels-only", action="store_true",
