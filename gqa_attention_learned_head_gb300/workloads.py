@@ -235,6 +235,30 @@ def batched_paged_decode(device="cpu", seed=0):
     return make_decode(32, 64, 8, (512, 4096), seed=seed, device=device)
 
 
+def tree_masks(parents) -> list:
+    """Attention masks of a draft tree given by parent indices (-1 for the root, parents before
+    children): bit j of mask i is set iff draft token j is token i or one of its ancestors."""
+    masks = []
+    for i, p in enumerate(parents):
+        assert p < i, "parents must come before their children"
+        masks.append((masks[p] if p >= 0 else 0) | (1 << i))
+    return masks
+
+
+# An EAGLE-style draft tree of 8 tokens, depth 4: the last accepted token (0) with two candidate
+# continuations, the first of them expanded twice, then one more level on two branches.
+DRAFT_TREE_PARENTS = [-1, 0, 0, 1, 1, 2, 3, 5]
+
+
+def tree_verify(device="cpu", seed=0):
+    """Verification of a draft tree: the batched paged decode's lengths and pool with 8 drafted
+    tokens per request (the tree DRAFT_TREE_PARENTS, same for every request), 64 q / 8 KV heads.
+    Returns (inputs, tree_mask [B, 8] int64)."""
+    inp = make_decode(32, 64, 8, (512, 4096), seed=seed, device=device, q_len=len(DRAFT_TREE_PARENTS))
+    m = torch.tensor(tree_masks(DRAFT_TREE_PARENTS), dtype=torch.int64, device=device)
+    return inp, m.expand(32, -1).contiguous()
+
+
 def speculative_verify(device="cpu", seed=0):
     """Verification of drafts: batch 32, 4 query tokens per request (3 drafted + the last
     accepted one), 64 q / 8 KV heads, kv_len U[512, 4096] including the 4, permuted pages."""

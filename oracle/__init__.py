@@ -54,7 +54,8 @@ def _load():
         _lib.oracle_merge.argtypes = [i, i, i, i, P, P, P, P, P]
         _lib.oracle_verify.argtypes = [i, i, i, i, i, i, i, i, P, P, P, P, P, P, f, i, P, P, P]
         _lib.oracle_prefill_paged.argtypes = [i, P, P, i, i, i, i, i, i, i, P, P, P, P, P, f, i, P, P, P]
-        for fn in ("oracle_decode", "oracle_prefill", "oracle_decode_partials", "oracle_merge", "oracle_verify", "oracle_prefill_paged",
+        _lib.oracle_verify_tree.argtypes = [i, i, i, i, i, i, i, i, P, P, P, P, P, P, P, f, i, P, P, P]
+        for fn in ("oracle_decode", "oracle_prefill", "oracle_decode_partials", "oracle_merge", "oracle_verify", "oracle_prefill_paged", "oracle_verify_tree",
                    "oracle_num_threads"):
             getattr(_lib, fn).restype = ctypes.c_int
     return _lib
@@ -141,6 +142,31 @@ def verify(q, k_pages, v_pages, page_table, kv_lens, sinks, scale, rows=None):
                                _ptr(pt), _ptr(kl), _ptr(sk), float(scale), n, _ptr(rows),
                                _ptr(out), _ptr(lse))
     _check(rc, "oracle.verify")
+    return out, lse
+
+
+def verify_tree(q, k_pages, v_pages, page_table, kv_lens, tree_mask, sinks, scale, rows=None):
+    """Verification of a tree of drafted tokens by definition.
+
+    As verify, but drafted token i sees drafted token j iff bit j of tree_mask[b, i] is set
+    (tree_mask [B, q_len] integers, q_len <= 64); every cache token before the draft is seen.
+    """
+    q, kp, vp = _bf16_bits(q), _bf16_bits(k_pages), _bf16_bits(v_pages)
+    pt, kl, sk = _np(page_table, np.int32), _np(kv_lens, np.int32), _np(sinks, np.float32)
+    tm = np.ascontiguousarray(np.asarray(tree_mask.cpu() if hasattr(tree_mask, "cpu") else tree_mask,
+                                         dtype=np.int64).view(np.uint64))
+    B, QL, Hq, D = q.shape
+    P, Hkv, PS, _ = kp.shape
+    if rows is not None:
+        rows = _np(rows, np.int32).reshape(-1, 3)
+        n = rows.shape[0]
+        out, lse = np.empty((n, D)), np.empty(n)
+    else:
+        n = B * QL * Hq
+        out, lse = np.empty((B, QL, Hq, D)), np.empty((B, QL, Hq))
+    rc = _load().oracle_verify_tree(B, QL, Hq, Hkv, D, PS, pt.shape[1], P, _ptr(q), _ptr(kp), _ptr(vp), _ptr(pt),
+                                    _ptr(kl), _ptr(tm), _ptr(sk), float(scale), n, _ptr(rows), _ptr(out), _ptr(lse))
+    _check(rc, "oracle.verify_tree")
     return out, lse
 
 

@@ -264,6 +264,71 @@ int oracle_prefill(int N, const int32_t *cu_seqlens, int T, int Hq, int Hkv, int
 }
 
 /*
+ * Verification of a TREE of drafted tokens.  Source: "Accelerating Sonar
+ * through speculation" (Perplexity), section "EAGLE": the drafts form a tree
+ * explored by the drafter, and the target model checks the tree with a custom
+ * attention mask.  Reading where the page is silent: the q_len drafted tokens
+ * of request b are the last q_len cache tokens, in the order given (position
+ * kv_lens[b] - q_len + i for token i); token i sees every cache token before
+ * the draft, and drafted token j iff bit j of tree_mask[b * q_len + i] is set
+ * (its ancestors in the tree and itself).  A chain mask (bits 0..i) is the
+ * linear verification above.
+ *   tree_mask [B, q_len] uint64 (q_len <= 64); other arguments as oracle_verify.
+ */
+int oracle_verify_tree(int B, int q_len, int Hq, int Hkv, int D, int PS, int max_pages, int num_pages,
+                       const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
+                       const int32_t *page_table, const int32_t *kv_lens, const uint64_t *tree_mask,
+                       const float *sinks, float scale, int n_rows, const int32_t *rows, double *out,
+                       double *lse) {
+    if (B < 0 || q_len <= 0 || q_len > 64 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || D <= 0 || PS <= 0)
+        return ORACLE_BAD_ARG;
+    const int G = Hq / Hkv;
+    const long total = rows ? n_rows : (long)B * q_len * Hq;
+    int status = ORACLE_OK;
+#pragma omp parallel
+    {
+        long cap = 0;
+        double *s = NULL;
+        const uint16_t **kp = NULL, **vp = NULL;
+#pragma omp for schedule(dynamic, 1)
+        for (long r = 0; r < total; ++r) {
+            int b = rows ? rows[3 * r] : (int)(r / ((long)q_len * Hq));
+            int i = rows ? rows[3 * r + 1] : (int)((r / Hq) % q_len);
+            int h = rows ? rows[3 * r + 2] : (int)(r % Hq);
+            long L = kv_lens[b];
+            long base = L - q_len; /* first drafted position */
+            if (L > cap) {
+                cap = L;
+                s = realloc(s, sizeof(double) * cap);
+                kp = realloc((void *)kp, sizeof(void *) * cap);
+                vp = realloc((void *)vp, sizeof(void *) * cap);
+            }
+            const uint64_t bits = tree_mask[(long)b * q_len + i];
+            long J = 0;
+            int bad = 0;
+            for (long t = 0; t < L; ++t) {
+                if (t >= base && !((bits >> (t - base)) & 1ull)) continue; /* a draft token off its path */
+                kp[J] = paged_row(k_pages, page_table, max_pages, num_pages, Hkv, PS, D, b, h / G, t);
+                vp[J] = paged_row(v_pages, page_table, max_pages, num_pages, Hkv, PS, D, b, h / G, t);
+                if (!kp[J]) bad = 1;
+                ++J;
+            }
+            if (bad) {
+#pragma omp atomic write
+                status = ORACLE_BAD_PAGE;
+                continue;
+            }
+            sink_row(q + (((long)b * q_len + i) * Hq + h) * D, kp, vp, J, D, (double)sinks[h], 1,
+                     (double)scale, s, out + r * D, lse + r);
+        }
+        free(s);
+        free((void *)kp);
+        free((void *)vp);
+    }
+    return status;
+}
+
+/*
  * Chunked prefill over a paged cache.  Source: "Accelerating Sonar through
  * speculation" (Perplexity), section "Inference with speculative decoding":
  * input tokens are batched, slots for them are allocated in the per-request KV

@@ -469,3 +469,56 @@ def test_paged_prefill_with_uniform_chunks_is_verification():
                                   inp.kv_lens - QL, inp.sinks, inp.scale)
     assert np.abs(po - vo.reshape(3 * QL, 8, 64)).max() <= TOL
     assert np.abs(pl - vl.reshape(3 * QL, 8)).max() <= TOL
+
+
+# ---- verification of a draft tree (EAGLE-style masks)
+
+def test_tree_masks_from_parents():
+    assert W.tree_masks([-1, 0, 0, 1]) == [0b1, 0b11, 0b101, 0b1011]
+    assert W.tree_masks(W.DRAFT_TREE_PARENTS)[7] == (1 << 7) | (1 << 5) | (1 << 2) | 1
+
+
+def test_chain_tree_is_linear_verification():
+    QL = 4
+    inp = W.make_decode(3, 8, 2, [9, 40, 33], seed=61, q_len=QL)
+    chain = torch.tensor([W.tree_masks([-1, 0, 1, 2])] * 3, dtype=torch.int64)
+    to, tl = oracle.verify_tree(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens, chain, inp.sinks,
+                                inp.scale)
+    vo, vl = oracle.verify(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens, inp.sinks, inp.scale)
+    assert np.abs(to - vo).max() <= TOL and np.abs(tl - vl).max() <= TOL
+
+
+def test_tree_brute_force_tiny():
+    """A 4-token tree over a 6-token cache (2 tokens before the draft), by explicit key sets."""
+    parents = [-1, 0, 0, 2]
+    inp = W.make_decode(1, 2, 1, [6], seed=62, q_len=4)
+    masks = W.tree_masks(parents)
+    out, lse = oracle.verify_tree(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens,
+                                  torch.tensor([masks], dtype=torch.int64), inp.sinks, inp.scale)
+    k, v = gather_kv(inp, 0, 0)
+    for i in range(4):
+        keys = [0, 1] + [2 + j for j in range(4) if (masks[i] >> j) & 1]  # prefix + path to the root
+        for h in range(2):
+            qv = inp.q[0, i, h].double()
+            logits = [inp.scale * float(qv @ k[j]) for j in keys] + [float(inp.sinks[h])]
+            m = max(logits)
+            w = [math.exp(x - m) for x in logits]
+            z = sum(w)
+            ref = sum(w[n] / z * v[j].numpy() for n, j in enumerate(keys))
+            assert np.abs(out[0, i, h] - ref).max() <= TOL
+            assert abs(lse[0, i, h] - (m + math.log(z))) <= TOL
+
+
+def test_tree_siblings_do_not_see_each_other():
+    """Two children of the same parent: each result is independent of the other's key and value."""
+    parents = [-1, 0, 0]
+    inp = W.make_decode(1, 4, 2, [30], seed=63, q_len=3)
+    m = torch.tensor([W.tree_masks(parents)], dtype=torch.int64)
+    base, _ = oracle.verify_tree(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens, m, inp.sinks, inp.scale)
+    kp, vp = inp.k_pages.clone(), inp.v_pages.clone()
+    sib = 30 - 3 + 2  # cache position of draft token 2
+    kp[inp.page_table[0, sib // 16], :, sib % 16] = 7.0
+    vp[inp.page_table[0, sib // 16], :, sib % 16] = -7.0
+    moved, _ = oracle.verify_tree(inp.q, kp, vp, inp.page_table, inp.kv_lens, m, inp.sinks, inp.scale)
+    assert np.array_equal(moved[0, :2], base[0, :2])  # tokens 0 and 1 never look at token 2
+    assert not np.array_equal(moved[0, 2], base[0, 2])
