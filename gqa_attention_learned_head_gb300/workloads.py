@@ -236,8 +236,8 @@ def batched_paged_decode(device="cpu", seed=0):
 
 
 def tree_masks(parents) -> list:
-    """Attention masks of a draft tree given by parent indices (-1 for the root, parents before
-    children): bit j of mask i is set iff draft token j is token i or one of its ancestors."""
+    """Attention masks of a draft tree (or forest) given by parent indices (-1 for a root, parents
+    before children): bit j of mask i is set iff draft token j is token i or one of its ancestors."""
     masks = []
     for i, p in enumerate(parents):
         assert p < i, "parents must come before their children"

@@ -522,3 +522,25 @@ def test_tree_siblings_do_not_see_each_other():
     moved, _ = oracle.verify_tree(inp.q, kp, vp, inp.page_table, inp.kv_lens, m, inp.sinks, inp.scale)
     assert np.array_equal(moved[0, :2], base[0, :2])  # tokens 0 and 1 never look at token 2
     assert not np.array_equal(moved[0, 2], base[0, 2])
+
+
+def test_forest_brute_force():
+    """Two roots: token 1's path does not contain token 0, token 3 hangs under token 1."""
+    parents = [-1, -1, 0, 1]
+    inp = W.make_decode(1, 2, 1, [7], seed=64, q_len=4)
+    masks = W.tree_masks(parents)
+    assert masks[1] == 0b10 and masks[3] == 0b1010
+    out, lse = oracle.verify_tree(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens,
+                                  torch.tensor([masks], dtype=torch.int64), inp.sinks, inp.scale)
+    k, v = gather_kv(inp, 0, 0)
+    for i in range(4):
+        keys = [0, 1, 2] + [3 + j for j in range(4) if (masks[i] >> j) & 1]
+        for h in range(2):
+            qv = inp.q[0, i, h].double()
+            logits = [inp.scale * float(qv @ k[j]) for j in keys] + [float(inp.sinks[h])]
+            m = max(logits)
+            w = [math.exp(x - m) for x in logits]
+            z = sum(w)
+            ref = sum(w[n] / z * v[j].numpy() for n, j in enumerate(keys))
+            assert np.abs(out[0, i, h] - ref).max() <= TOL
+            assert abs(lse[0, i, h] - (m + math.log(z))) <= TOL
