@@ -10,8 +10,8 @@ Headline: decode KV GB/s on the batched paged decode workload (batch 32,
 randomly permuted in the pool).  One step = one sinkattn_decode call (split
 pass + merge), i.e. the whole decode hot path, on inputs resident in HBM.
 The L2 is flushed (256 MiB write, then a 512 MiB read) before every timed step.  Secondary lines
-for the long-context split-KV decode, the verification of drafted tokens (4 per request), the
-causal prefill, the chunked prefill over the paged cache and the mixed serving batch ride in the
+for the long-context split-KV decode, the verification of drafted tokens (4 per request, and a
+draft tree of 8), the causal prefill, the chunked prefill over the paged cache and the mixed serving batch ride in the
 same JSON object under "secondary".
 
 Prints ONE JSON line on rank 0.  Under torchrun every rank runs its own
@@ -52,6 +52,8 @@ WORKLOAD_TEXT = {
     "chunked_prefill": "chunked prefill over the paged cache: 8 sequences, U[1024,8192] cached + U[256,2048] new "
                        "tokens each, 64 q / 8 KV heads, head_dim 64; one step = append the new K/V into the pages "
                        "+ paged prefill",
+    "tree_verify": "verification of a draft tree: batch 32, an EAGLE-style tree of 8 drafted tokens per request "
+                   "(depth 4) over the paged cache, 64 q / 8 KV heads, kv_len U[512,4096] (drafts included)",
     "speculative_verify": "verification of drafts: batch 32, 4 query tokens per request over the paged cache, "
                           "64 q / 8 KV heads, head_dim 64, kv_len U[512,4096] (drafts included), permuted pages",
     "mixed_serving": "mixed serving batch: 8 causal prefills L~U[256,4096] + 256 paged decodes kv_len~U[1024,32768], "
@@ -267,6 +269,27 @@ def bench_verify(S, W, rank, K, warmup, flush, stream):
     def step():
         S.sinkattn_verify(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens, inp.sinks, inp.scale,
                           out=out, lse=lse, workspace=ws, stream=stream)
+
+    with torch.cuda.stream(stream):
+        times = timed_steps(step, K, warmup, flush, stream)
+    err = S.sinkattn_get_error(stream)
+    if err:
+        raise RuntimeError(f"device error {S.status_string(err)}")
+    return inp, step, times, decode_bytes(inp.kv_lens, Hkv, D)
+
+
+def bench_tree_verify(S, W, rank, K, warmup, flush, stream):
+    inp, masks = W.tree_verify(device="cuda", seed=rank)
+    B, QL, Hq, D = inp.q.shape
+    Hkv = inp.k_pages.shape[1]
+    ws = torch.empty(S.sinkattn_verify_workspace_size(inp.q, inp.k_pages, inp.page_table), dtype=torch.uint8,
+                     device="cuda")
+    out = torch.empty_like(inp.q)
+    lse = torch.empty(B, QL, Hq, dtype=torch.float32, device="cuda")
+
+    def step():
+        S.sinkattn_verify_tree(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens, masks, inp.sinks,
+                               inp.scale, out=out, lse=lse, workspace=ws, stream=stream)
 
     with torch.cuda.stream(stream):
         times = timed_steps(step, K, warmup, flush, stream)
@@ -632,6 +655,11 @@ def run_ours(args):
                               "traffic": profiled_traffic("verify_split_kernel", "speculative_verify",
                                                           ["verify.cu", "ptx.cuh", "kernels.h", "split_kv.cuh"])})
             del vi
+            ti, _, tt, tb = bench_tree_verify(S, W, rank, Ks, Wu, flush, stream)
+            tms = statistics.mean(tt)
+            secondary.append({"workload": WORKLOAD_TEXT["tree_verify"], "value": tb / (tms * 1e-3) / 1e9,
+                              "unit": "GB/s", "ms_per_step": tms, "frac_of_hbm_peak": tb / (tms * 1e-3) / 1e9 / hbm_peak})
+            del ti
             pi, _, pt_, pf = bench_prefill(S, W, "causal_prefill", rank, Ks, Wu, flush, stream)
             pms = statistics.mean(pt_)
             secondary.append({"workload": WORKLOAD_TEXT["causal_prefill"], "value": pf / (pms * 1e-3) / 1e12,

@@ -246,17 +246,48 @@ size_t sinkattn_verify_workspace_size(const sinkattn_verify_dims_t* dims) {
     return plan.ws_bytes;
 }
 
+namespace sinkattn {
+namespace {
+sinkattn_status_t verify_common(const void* q, const void* k_pages, const void* v_pages, const int32_t* page_table,
+                                const int32_t* kv_lens, const uint64_t* tree_mask, const float* sinks, float scale,
+                                void* out, float* lse, const sinkattn_verify_dims_t* dims, void* workspace,
+                                size_t workspace_bytes, void* stream);
+}  // namespace
+}  // namespace sinkattn
+
 sinkattn_status_t sinkattn_verify(const void* q, const void* k_pages, const void* v_pages, const int32_t* page_table,
                                   const int32_t* kv_lens, const float* sinks, float scale, void* out, float* lse,
                                   const sinkattn_verify_dims_t* dims, void* workspace, size_t workspace_bytes,
                                   void* stream) {
+    return verify_common(q, k_pages, v_pages, page_table, kv_lens, nullptr, sinks, scale, out, lse, dims, workspace,
+                         workspace_bytes, stream);
+}
+
+sinkattn_status_t sinkattn_verify_tree(const void* q, const void* k_pages, const void* v_pages,
+                                       const int32_t* page_table, const int32_t* kv_lens, const uint64_t* tree_mask,
+                                       const float* sinks, float scale, void* out, float* lse,
+                                       const sinkattn_verify_dims_t* dims, void* workspace, size_t workspace_bytes,
+                                       void* stream) {
+    if (!tree_mask) return SINKATTN_ERR_INVALID_ARG;
+    if (dims && dims->q_len > 64) return SINKATTN_ERR_UNSUPPORTED;
+    return verify_common(q, k_pages, v_pages, page_table, kv_lens, tree_mask, sinks, scale, out, lse, dims, workspace,
+                         workspace_bytes, stream);
+}
+
+namespace sinkattn {
+namespace {
+sinkattn_status_t verify_common(const void* q, const void* k_pages, const void* v_pages, const int32_t* page_table,
+                                const int32_t* kv_lens, const uint64_t* tree_mask, const float* sinks, float scale,
+                                void* out, float* lse, const sinkattn_verify_dims_t* dims, void* workspace,
+                                size_t workspace_bytes, void* stream) {
     sinkattn_status_t st = check_verify_dims(dims);
     if (st != SINKATTN_OK) return st;
     if (dims->batch == 0) return SINKATTN_OK;
     if (!q || !page_table || !kv_lens || !sinks || !out) return SINKATTN_ERR_INVALID_ARG;
     if (dims->num_pages > 0 && (!k_pages || !v_pages)) return SINKATTN_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(out, 16) ||
-        !aligned(page_table, 4) || !aligned(kv_lens, 4) || !aligned(sinks, 4) || (lse && !aligned(lse, 4)))
+        !aligned(page_table, 4) || !aligned(kv_lens, 4) || !aligned(sinks, 4) || (lse && !aligned(lse, 4)) ||
+        (tree_mask && !aligned(tree_mask, 8)))
         return SINKATTN_ERR_INVALID_ARG;
     if (!(scale == scale)) return SINKATTN_ERR_INVALID_ARG;
     DeviceState* ds = nullptr;
@@ -283,6 +314,7 @@ sinkattn_status_t sinkattn_verify(const void* q, const void* k_pages, const void
     a.page_table = page_table;
     a.kv_lens = kv_lens;
     a.sinks = sinks;
+    a.tree_mask = reinterpret_cast<const unsigned long long*>(tree_mask);
     a.out = static_cast<__nv_bfloat16*>(out);
     a.lse = lse;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -306,6 +338,8 @@ sinkattn_status_t sinkattn_verify(const void* q, const void* k_pages, const void
     return verify_launch(a, plan, tk, tv, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SINKATTN_OK
                                                                                             : SINKATTN_ERR_CUDA;
 }
+}  // namespace
+}  // namespace sinkattn
 
 sinkattn_status_t sinkattn_kv_append(const void* k, const void* v, const int32_t* cu_seqlens, const int32_t* start_pos,
                                      const int32_t* page_table, void* k_pages, void* v_pages,

@@ -54,6 +54,7 @@ struct VerifyArgs {
     const int32_t* page_table;  // [B, max_pages]
     const int32_t* kv_lens;     // [B], counting the QL drafted tokens
     const float* sinks;         // [Hq]
+    const unsigned long long* tree_mask;  // [B, QL] draft tree masks, or null for a linear draft
     __nv_bfloat16* out;         // [B, QL, Hq, 64]
     float* lse;                 // [B, QL, Hq] or null
     float* part_o;              // [slots, R, 64]

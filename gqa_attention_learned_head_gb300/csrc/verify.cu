@@ -8,7 +8,10 @@
 // the paged KV cache); the attention itself is the sink attention of "GPT-OSS
 // on day 0", section "Kernels for GPT-OSS / Sink Attention".  Query token i of
 // request b is the cache token at position kv_len - q_len + i (its K and V are
-// already in the pages) and sees cache tokens 0 .. that position.
+// already in the pages) and sees cache tokens 0 .. that position -- or, for a
+// tree of drafts (section "EAGLE": the target checks the drafted tree with a
+// custom attention mask), every token before the draft and the drafted tokens
+// on its own path, given as a bit mask per token.
 //
 // GB300 design: the decode's work split (split_kv.cuh: contiguous per-CTA
 // shares of (request, KV head, page) units, pieces, merge in the same launch),
@@ -288,17 +291,24 @@ __global__ void __launch_bounds__((W + 1) * 32, min_blocks<W>())
     for (; warp < W && cp.ps < x1; piece_next(cp, prefix, B, Hkv, x1)) {
         const int kv_len = clamp_len(__ldg(&a.kv_lens[cp.b]), cap);
         const int pos0 = kv_len - QL;  // cache position of drafted token 0 (negative for a short cache)
-        // This lane's two query rows (mma rows gq and gq + 8 of the warp's 16): keys [0, lim) visible.
+        // This lane's two query rows (mma rows gq and gq + 8 of the warp's 16): keys [0, lim) visible;
+        // with a draft tree, a drafted key j (position pos0 + j) only if bit j of the row's mask is set.
+        const bool tree = a.tree_mask != nullptr;
         int rr[2], lim[2];
         float sink2[2];
+        unsigned long long bits[2] = {0ull, 0ull};
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             rr[e] = 16 * warp + gq + 8 * e;
-            lim[e] = rr[e] < R ? pos0 + rr[e] / G + 1 : 0;
-            sink2[e] = rr[e] < R ? __ldg(&a.sinks[cp.g * G + rr[e] % G]) * kLog2e : kNegInf;
+            const bool live = rr[e] < R;
+            lim[e] = !live ? 0 : tree ? kv_len : pos0 + rr[e] / G + 1;
+            sink2[e] = live ? __ldg(&a.sinks[cp.g * G + rr[e] % G]) * kLog2e : kNegInf;
+            if (tree && live) bits[e] = __ldg(&a.tree_mask[(long long)cp.b * QL + rr[e] / G]);
         }
-        // smallest limit over the warp's live rows: pages below it need no mask
-        int lim_lo = min(rr[0] < R ? lim[0] : INT_MAX, rr[1] < R ? lim[1] : INT_MAX);
+        // smallest limit over the warp's live rows (for a tree: the draft's start): pages below it
+        // need no mask
+        const int first_masked = tree ? max(pos0, 0) : INT_MAX;
+        int lim_lo = min(rr[0] < R ? min(lim[0], first_masked) : INT_MAX, rr[1] < R ? min(lim[1], first_masked) : INT_MAX);
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) lim_lo = min(lim_lo, __shfl_xor_sync(0xffffffffu, lim_lo, o));
         // A fragments of Q (rows gq, gq + 8; dims 2tq, 2tq+1 and +8 within each 16-dim step)
@@ -370,7 +380,9 @@ __global__ void __launch_bounds__((W + 1) * 32, min_blocks<W>())
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int slot_tok = 8 * j + 2 * tq + (e & 1);
-                        const bool live = slot_tok < valid && page * kPageSize + slot_tok < lim[e >> 1];
+                        const int tok = page * kPageSize + slot_tok;
+                        const bool live = slot_tok < valid && tok < lim[e >> 1] &&
+                                          (tok < pos0 || !tree || ((bits[e >> 1] >> (tok - pos0)) & 1ull));
                         sc[j][e] = live ? acc[j][e] * a.scale_log2 : kNegInf;
                     }
             }

@@ -56,7 +56,7 @@ class MergeDims(ctypes.Structure):
 
 
 EXPORTS = ("sinkattn_decode", "sinkattn_prefill", "sinkattn_merge", "sinkattn_decode_workspace_size", "sinkattn_verify",
-           "sinkattn_verify_workspace_size", "sinkattn_kv_append", "sinkattn_prefill_paged",
+           "sinkattn_verify_workspace_size", "sinkattn_kv_append", "sinkattn_prefill_paged", "sinkattn_verify_tree",
            "sinkattn_get_error", "sinkattn_status_string", "sinkattn_version")
 
 
@@ -76,6 +76,7 @@ def _load():
     lib.sinkattn_verify.argtypes = [P, P, P, P, P, P, f32, P, P, ctypes.POINTER(VerifyDims), P, sz, P]
     lib.sinkattn_verify_workspace_size.argtypes = [ctypes.POINTER(VerifyDims)]
     lib.sinkattn_verify_workspace_size.restype = sz
+    lib.sinkattn_verify_tree.argtypes = [P, P, P, P, P, P, P, f32, P, P, ctypes.POINTER(VerifyDims), P, sz, P]
     lib.sinkattn_kv_append.argtypes = [P, P, P, P, P, P, P, ctypes.POINTER(PagedDims), P]
     lib.sinkattn_prefill_paged.argtypes = [P, P, P, P, P, P, P, f32, P, P, ctypes.POINTER(PagedDims), P]
     lib.sinkattn_get_error.argtypes = [P]
@@ -83,7 +84,7 @@ def _load():
     lib.sinkattn_status_string.restype = ctypes.c_char_p
     lib.sinkattn_version.restype = i32
     for fn in ("sinkattn_decode", "sinkattn_prefill", "sinkattn_merge", "sinkattn_get_error", "sinkattn_verify",
-               "sinkattn_kv_append", "sinkattn_prefill_paged"):
+               "sinkattn_kv_append", "sinkattn_prefill_paged", "sinkattn_verify_tree"):
         getattr(lib, fn).restype = ctypes.c_int
     return lib
 
@@ -207,6 +208,38 @@ def sinkattn_verify(q, k_pages, v_pages, page_table, kv_lens, sinks, scale, out=
                               float(scale), _ptr(out), _ptr(lse), ctypes.byref(dims), _ptr(workspace),
                               workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "sinkattn_verify")
+    return out, lse
+
+
+def sinkattn_verify_tree(q, k_pages, v_pages, page_table, kv_lens, tree_mask, sinks, scale, out=None, lse=None,
+                         workspace=None, num_workers=0, return_lse=True, stream=None):
+    """sinkattn_verify for a draft tree: tree_mask [B, q_len] int64 on the device, bit j of mask i = drafted
+    token i sees drafted token j (its ancestors and itself).  Returns (out, lse)."""
+    _need(tree_mask, "tree_mask", torch.int64, 2)
+    B, QL = q.shape[0], q.shape[1]
+    if tuple(tree_mask.shape) != (B, QL):
+        raise ValueError("tree_mask must be [batch, q_len]")
+    _need(q, "q", torch.bfloat16, 4)
+    _need(k_pages, "k_pages", torch.bfloat16, 4)
+    _need(v_pages, "v_pages", torch.bfloat16, 4)
+    _need(page_table, "page_table", torch.int32, 2)
+    _need(kv_lens, "kv_lens", torch.int32, 1)
+    _need(sinks, "sinks", torch.float32, 1)
+    Hq = q.shape[2]
+    dims = verify_dims(q, k_pages, page_table, num_workers)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty(B, QL, Hq, device=q.device, dtype=torch.float32)
+    if workspace is None:
+        nbytes = int(_lib.sinkattn_verify_workspace_size(ctypes.byref(dims)))
+        if nbytes == 0:
+            raise SinkAttnError(ERR_INVALID_ARG, "sinkattn_verify_workspace_size")
+        workspace = torch.empty(nbytes, device=q.device, dtype=torch.uint8)
+    st = _lib.sinkattn_verify_tree(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table), _ptr(kv_lens),
+                                   _ptr(tree_mask), _ptr(sinks), float(scale), _ptr(out), _ptr(lse), ctypes.byref(dims),
+                                   _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "sinkattn_verify_tree")
     return out, lse
 
 

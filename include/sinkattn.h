@@ -174,6 +174,28 @@ sinkattn_status_t sinkattn_verify(const void *q, const void *k_pages, const void
                                   const sinkattn_verify_dims_t *dims, void *workspace,
                                   size_t workspace_bytes, void *stream);
 
+/*
+ * sinkattn_verify for a TREE of drafted tokens.  Source: "Accelerating Sonar
+ * through speculation", section "EAGLE": the drafter explores a tree of
+ * candidate continuations and the target checks the whole tree at once with a
+ * custom attention mask.
+ *
+ * The q_len drafted tokens of request b are its last q_len cached tokens, in
+ * any order that puts parents before children: token i sits at cache position
+ * kv_lens[b] - q_len + i, sees every cache token before the draft, and sees
+ * drafted token j iff bit j of tree_mask[b][i] is set (its ancestors and
+ * itself).  A mask with bits 0..i for token i is the linear draft of
+ * sinkattn_verify.
+ *
+ *   tree_mask  [B, q_len] uint64, 8-byte aligned, device memory (q_len <= 64)
+ *   everything else as sinkattn_verify (same workspace size).
+ */
+sinkattn_status_t sinkattn_verify_tree(const void *q, const void *k_pages, const void *v_pages,
+                                       const int32_t *page_table, const int32_t *kv_lens,
+                                       const uint64_t *tree_mask, const float *sinks, float scale,
+                                       void *out, float *lse, const sinkattn_verify_dims_t *dims,
+                                       void *workspace, size_t workspace_bytes, void *stream);
+
 /* Shapes of the calls over a paged cache that take new tokens packed by cu_seqlens. */
 typedef struct {
     int32_t num_seqs;          /* N sequences (requests), 0..16384                        */

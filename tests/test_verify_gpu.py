@@ -123,3 +123,69 @@ def test_garbage_past_the_cache_end_is_ignored(S):
     out, lse, err = run(S, inp)
     assert err == 0
     assert_parity(out, lse, ro, rl, "NaN past the end")
+
+
+# ---- draft trees (EAGLE-style masks)
+
+def run_tree(S, inp, masks, **kw):
+    g = inp.to("cuda")
+    m = torch.as_tensor(masks, dtype=torch.int64).cuda()
+    out, lse = S.sinkattn_verify_tree(g.q, g.k_pages, g.v_pages, g.page_table, g.kv_lens, m, g.sinks, g.scale, **kw)
+    err = S.sinkattn_get_error()
+    return out.float().cpu().numpy(), lse.cpu().numpy(), err
+
+
+def ref_tree(inp, masks, rows=None):
+    return oracle.verify_tree(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens,
+                              torch.as_tensor(masks, dtype=torch.int64), inp.sinks, inp.scale, rows=rows)
+
+
+@pytest.mark.parametrize("parents", [W.DRAFT_TREE_PARENTS, [-1, -1, 0, 1], [-1, 0, 1, 2, 3], [-1, 0, 0, 0, 0, 0]])
+@pytest.mark.parametrize("Hq,Hkv", [(64, 8), (8, 2), (4, 4)])
+def test_tree_shapes(S, parents, Hq, Hkv):
+    QL = len(parents)
+    if QL * Hq // Hkv > 64:
+        pytest.skip("more than 64 query rows per (request, KV head)")
+    lens = [QL, 17, 300, 1000, QL + 16]
+    inp = W.make_decode(len(lens), Hq, Hkv, lens, seed=QL + Hq, q_len=QL)
+    masks = [W.tree_masks(parents)] * len(lens)
+    out, lse, err = run_tree(S, inp, masks)
+    assert err == 0
+    assert_parity(out, lse, *ref_tree(inp, masks), f"parents={parents} Hq={Hq} Hkv={Hkv}")
+
+
+def test_tree_per_request_masks_and_splits(S):
+    """Different trees per request, forced splits so that drafts land in merged pieces."""
+    rng = np.random.default_rng(5)
+    QL, B = 6, 5
+    masks = []
+    for _ in range(B):
+        parents = [-1] + [int(rng.integers(-1, i)) for i in range(1, QL)]
+        masks.append(W.tree_masks(parents))
+    inp = W.make_decode(B, 16, 2, (20, 400), seed=71, q_len=QL)
+    for workers in (0, 7, 40):
+        out, lse, err = run_tree(S, inp, masks, num_workers=workers)
+        assert err == 0
+        assert_parity(out, lse, *ref_tree(inp, masks), f"workers={workers}")
+
+
+def test_chain_tree_matches_linear_kernel(S):
+    inp = W.make_decode(4, 64, 8, (100, 900), seed=72, q_len=4)
+    masks = [W.tree_masks([-1, 0, 1, 2])] * 4
+    out, lse, err = run_tree(S, inp, masks)
+    lo, ll, lerr = run(S, inp)
+    assert err == 0 and lerr == 0
+    ro, rl = ref(inp)
+    assert_parity(out, lse, ro, rl, "chain tree")
+    assert_parity(lo, ll, ro, rl, "linear")
+
+
+def test_tree_verify_full_size_sampled(S):
+    inp, masks = W.tree_verify()
+    out, lse, err = run_tree(S, inp, masks)
+    assert err == 0
+    rng = np.random.default_rng(3)
+    rows = np.stack([rng.integers(0, 32, 96), rng.integers(0, 8, 96), rng.integers(0, 64, 96)], 1).astype(np.int32)
+    ro, rl = ref_tree(inp, masks, rows)
+    assert_parity(out[rows[:, 0], rows[:, 1], rows[:, 2]], lse[rows[:, 0], rows[:, 1], rows[:, 2]], ro, rl, "tree")
+    assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
