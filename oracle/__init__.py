@@ -13,6 +13,7 @@ learned sink logit that enters the softmax normaliser and has no value row.
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 import subprocess
 from pathlib import Path
@@ -242,6 +243,76 @@ def prefill_paged(q, k_pages, v_pages, page_table, cu_seqlens, start_pos, sinks,
                                       _ptr(out), _ptr(lse))
     _check(rc, "oracle.prefill_paged")
     return out, lse
+
+
+# ---------------------------------------------------------------------------- pre-attention prologue
+# "GPT-OSS on day 0", section "Attention: GQA with attention sinks": the QKV projections carry a bias
+# and positions are encoded with YaRN rotary embeddings (as in DeepSeek-V3).  The page gives no
+# formulas; these follow the YaRN method as published ("YaRN: Efficient Context Window Extension of
+# Large Language Models"): rotary frequency theta_d = theta^(-2d/D); wavelength lambda_d = 2 pi /
+# theta_d; ratio r_d = L / lambda_d for the original context L; ramp gamma(r) = 0 for r < beta_slow,
+# 1 for r > beta_fast, linear between; new frequency (1 - gamma) theta_d / s + gamma theta_d; and the
+# attention temperature 1/t with sqrt(1/t) = 0.1 ln s + 1, applied by scaling q and k.
+
+def yarn_inv_freq(D, theta, factor, original_max_position, beta_fast, beta_slow) -> np.ndarray:
+    """Rotary angle per position of each of the D/2 dimension pairs, float64."""
+    d = np.arange(D // 2, dtype=np.float64)
+    theta_d = np.power(float(theta), -2.0 * d / D)
+    r = float(original_max_position) * theta_d / (2.0 * np.pi)  # L / wavelength
+    gamma = np.clip((r - beta_slow) / (beta_fast - beta_slow), 0.0, 1.0)
+    return (1.0 - gamma) * theta_d / float(factor) + gamma * theta_d
+
+
+def yarn_mscale(factor, attn_factor=0.0) -> float:
+    """Multiplier of q and k after the rotation: the given one, else 0.1 ln(s) + 1 (1 for s <= 1)."""
+    if attn_factor:
+        return float(attn_factor)
+    return 0.1 * math.log(factor) + 1.0 if factor > 1.0 else 1.0
+
+
+def rope(x, positions, inv_freq, mscale, interleaved=False):
+    """Rotates the last axis (D) of x [..., T, H, D] (float64) by positions [T] x inv_freq [D/2].
+
+    Pairs are (d, d + D/2) (interleaved=False) or (2d, 2d + 1); the result is scaled by mscale."""
+    x = np.asarray(x, dtype=np.float64)
+    D = x.shape[-1]
+    ang = np.asarray(positions, dtype=np.float64)[:, None] * inv_freq[None, :]  # [T, D/2]
+    c, s = np.cos(ang)[:, None, :], np.sin(ang)[:, None, :]
+    if interleaved:
+        a, b = x[..., 0::2], x[..., 1::2]
+    else:
+        a, b = x[..., : D // 2], x[..., D // 2:]
+    ra, rb = a * c - b * s, b * c + a * s
+    out = np.empty_like(x)
+    if interleaved:
+        out[..., 0::2], out[..., 1::2] = ra, rb
+    else:
+        out[..., : D // 2], out[..., D // 2:] = ra, rb
+    return out * mscale
+
+
+def qkv_prologue(qkv, bias, cu_seqlens, start_pos, Hq, Hkv, theta, factor, original_max_position, beta_fast,
+                 beta_slow, attn_factor=0.0, interleaved=False):
+    """Bias + YaRN rotary embedding of new tokens, by definition.
+
+    qkv [T, (Hq + 2 Hkv) * D] bf16 (q heads, then k heads, then v heads), bias [(Hq + 2 Hkv) * D]
+    bf16; new token i of sequence n is at position start_pos[n] + i.  Returns float64 q [T, Hq, D],
+    k [T, Hkv, D] (both rotated and scaled) and v [T, Hkv, D] (bias only)."""
+    x = _bf16_bits(qkv)
+    T = x.shape[0]
+    D = x.shape[1] // (Hq + 2 * Hkv)
+    xf = _bits_to_f64(x).reshape(T, Hq + 2 * Hkv, D) + _bits_to_f64(_bf16_bits(bias)).reshape(1, Hq + 2 * Hkv, D)
+    cu, sp = _np(cu_seqlens, np.int32), _np(start_pos, np.int32)
+    pos = np.concatenate([sp[n] + np.arange(cu[n + 1] - cu[n]) for n in range(len(cu) - 1)]).astype(np.float64)
+    inv = yarn_inv_freq(D, theta, factor, original_max_position, beta_fast, beta_slow)
+    ms = yarn_mscale(factor, attn_factor)
+    q = rope(xf[:, :Hq], pos, inv, ms, interleaved)
+    k = rope(xf[:, Hq:Hq + Hkv], pos, inv, ms, interleaved)
+    return q, k, xf[:, Hq + Hkv:]
+
+
+def _bits_to_f64(bits) -> np.ndarray:
+    return (np.asarray(bits, dtype=np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
 SINK_IN_FIRST_CHUNK = 0

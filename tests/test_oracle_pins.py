@@ -544,3 +544,87 @@ def test_forest_brute_force():
             ref = sum(w[n] / z * v[j].numpy() for n, j in enumerate(keys))
             assert np.abs(out[0, i, h] - ref).max() <= TOL
             assert abs(lse[0, i, h] - (m + math.log(z))) <= TOL
+
+
+# ---- pre-attention prologue: QKV bias + YaRN rotary embedding
+
+YARN = dict(theta=150000.0, factor=32.0, original_max_position=4096, beta_fast=32.0, beta_slow=1.0)
+
+
+def test_yarn_without_extension_is_plain_rope():
+    inv = oracle.yarn_inv_freq(64, 10000.0, 1.0, 4096, 32.0, 1.0)
+    assert np.allclose(inv, 10000.0 ** (-np.arange(32) / 32.0), rtol=1e-15, atol=0)
+    assert oracle.yarn_mscale(1.0) == 1.0
+
+
+def test_yarn_ramp_orientation():
+    """Dimensions that turn many times within the original context keep their frequency; those that
+    turn less than once are slowed down by the factor; the ramp between is monotone."""
+    D, th, s, L = 64, 150000.0, 32.0, 4096
+    base = th ** (-np.arange(32) / 32.0)
+    turns = L * base / (2 * np.pi)  # full turns over the original context
+    inv = oracle.yarn_inv_freq(D, th, s, L, 32.0, 1.0)
+    fast, slow = turns > 32.0, turns < 1.0
+    assert fast.any() and slow.any()
+    assert np.allclose(inv[fast], base[fast], rtol=1e-15, atol=0)
+    assert np.allclose(inv[slow], base[slow] / s, rtol=1e-15, atol=0)
+    ratio = inv / base  # 1 for fast dims, 1/s for slow ones
+    assert np.all(np.diff(ratio) <= 1e-15)
+    assert abs(oracle.yarn_mscale(32.0) - (0.1 * math.log(32.0) + 1.0)) < 1e-15
+
+
+@pytest.mark.parametrize("interleaved", [False, True])
+def test_rope_invariants(interleaved):
+    rng = np.random.default_rng(81)
+    inv = oracle.yarn_inv_freq(64, **YARN)
+    ms = oracle.yarn_mscale(YARN["factor"])
+    q, k = rng.standard_normal((1, 1, 64)), rng.standard_normal((1, 1, 64))
+    rq = lambda p: oracle.rope(q, [p], inv, ms, interleaved)[0, 0]
+    rk = lambda p: oracle.rope(k, [p], inv, ms, interleaved)[0, 0]
+    assert np.allclose(rq(0), ms * q[0, 0], rtol=1e-15, atol=0)  # position 0: no turn
+    for p in (1, 777, 131071):
+        assert abs(np.linalg.norm(rq(p)) - ms * np.linalg.norm(q)) < 1e-12  # a rotation
+    for m, n, delta in ((5, 2, 100), (4000, 17, 60000), (9, 9, 3)):  # only m - n matters
+        assert abs(rq(m) @ rk(n) - rq(m + delta) @ rk(n + delta)) < 1e-9
+
+
+def test_rope_pairs_by_hand():
+    """One unit vector per convention, rotated by hand: (1, 0) -> (cos a, sin a) in its pair."""
+    inv = oracle.yarn_inv_freq(64, **YARN)
+    p, d = 1234, 5
+    a = p * inv[d]
+    x = np.zeros((1, 1, 64))
+    x[0, 0, d] = 1.0
+    y = oracle.rope(x, [p], inv, 1.0, False)[0, 0]
+    assert abs(y[d] - math.cos(a)) < 1e-12 and abs(y[d + 32] - math.sin(a)) < 1e-12
+    assert np.count_nonzero(np.abs(y) > 1e-15) == 2
+    x = np.zeros((1, 1, 64))
+    x[0, 0, 2 * d] = 1.0
+    y = oracle.rope(x, [p], inv, 1.0, True)[0, 0]
+    assert abs(y[2 * d] - math.cos(a)) < 1e-12 and abs(y[2 * d + 1] - math.sin(a)) < 1e-12
+
+
+def test_conventions_are_a_permutation_apart():
+    rng = np.random.default_rng(82)
+    inv = oracle.yarn_inv_freq(64, **YARN)
+    x = rng.standard_normal((3, 2, 64))
+    perm = np.empty(64, dtype=int)
+    perm[0::2], perm[1::2] = np.arange(32), np.arange(32, 64)  # interleaved slot -> halves slot
+    a = oracle.rope(x[..., perm], [3, 50, 999], inv, 1.3, True)
+    b = oracle.rope(x, [3, 50, 999], inv, 1.3, False)[..., perm]
+    assert np.allclose(a, b, rtol=0, atol=1e-13)
+
+
+def test_prologue_adds_bias_before_rotating_and_uses_cache_positions():
+    Hq, Hkv = 4, 2
+    g = torch.Generator().manual_seed(83)
+    qkv = bf16(torch.randn(7, (Hq + 2 * Hkv) * 64, generator=g))
+    bias = bf16(torch.randn((Hq + 2 * Hkv) * 64, generator=g))
+    cu, sp = torch.tensor([0, 3, 7], dtype=torch.int32), torch.tensor([10, 0], dtype=torch.int32)
+    q, k, v = oracle.qkv_prologue(qkv, bias, cu, sp, Hq, Hkv, **YARN)
+    x = (qkv.double() + bias.double()).reshape(7, Hq + 2 * Hkv, 64).numpy()
+    pos = [10, 11, 12, 0, 1, 2, 3]
+    inv, ms = oracle.yarn_inv_freq(64, **YARN), oracle.yarn_mscale(32.0)
+    assert np.allclose(q, oracle.rope(x[:, :Hq], pos, inv, ms), rtol=0, atol=1e-12)
+    assert np.allclose(k, oracle.rope(x[:, Hq:Hq + Hkv], pos, inv, ms), rtol=0, atol=1e-12)
+    assert np.array_equal(v, x[:, Hq + Hkv:])
