@@ -8,6 +8,7 @@
 #include <atomic>
 #include <chrono>
 #include <cstdlib>
+#include <cmath>
 #include <cstring>
 #include <mutex>
 
@@ -420,6 +421,57 @@ sinkattn_status_t sinkattn_prefill_paged(const void* q, const void* k_pages, con
     a.max_pages = d.max_pages;
     const cudaError_t e = prefill_paged_launch(a, tq, tk, tv, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? SINKATTN_OK : SINKATTN_ERR_CUDA;
+}
+
+sinkattn_status_t sinkattn_qkv_prologue(const void* qkv, const void* bias, const int32_t* cu_seqlens,
+                                        const int32_t* start_pos, const int32_t* page_table, const sinkattn_rope_t* rope,
+                                        void* q_out, void* k_pages, void* v_pages, const sinkattn_paged_dims_t* dims,
+                                        void* stream) {
+    sinkattn_status_t st = check_paged_dims(dims, true);
+    if (st != SINKATTN_OK) return st;
+    if (!rope) return SINKATTN_ERR_INVALID_ARG;
+    const sinkattn_rope_t& r = *rope;
+    if (!(r.theta > 1.f) || !(r.factor >= 1.f) || r.original_max_position <= 0 || !(r.beta_slow > 0.f) ||
+        !(r.beta_fast > r.beta_slow) || !(r.attn_factor >= 0.f))
+        return SINKATTN_ERR_INVALID_ARG;
+    const sinkattn_paged_dims_t& d = *dims;
+    if (d.num_seqs == 0 || d.total_tokens == 0) return SINKATTN_OK;
+    if (!qkv || !cu_seqlens || !start_pos || !page_table || !q_out || !k_pages || !v_pages)
+        return SINKATTN_ERR_INVALID_ARG;
+    if (!aligned(qkv, 2) || (bias && !aligned(bias, 2)) || !aligned(q_out, 2) || !aligned(k_pages, 2) ||
+        !aligned(v_pages, 2) || !aligned(cu_seqlens, 4) || !aligned(start_pos, 4) || !aligned(page_table, 4))
+        return SINKATTN_ERR_INVALID_ARG;
+    DeviceState* ds = nullptr;
+    if ((st = device_state(&ds)) != SINKATTN_OK) return st;
+    PrologueArgs a;
+    a.qkv = static_cast<const __nv_bfloat16*>(qkv);
+    a.bias = static_cast<const __nv_bfloat16*>(bias);
+    a.cu_seqlens = cu_seqlens;
+    a.start_pos = start_pos;
+    a.page_table = page_table;
+    a.q_out = static_cast<__nv_bfloat16*>(q_out);
+    a.k_pages = static_cast<__nv_bfloat16*>(k_pages);
+    a.v_pages = static_cast<__nv_bfloat16*>(v_pages);
+    a.err = ds->err;
+    a.N = d.num_seqs;
+    a.T = d.total_tokens;
+    a.Hq = d.num_q_heads;
+    a.Hkv = d.num_kv_heads;
+    a.num_pages = d.num_pages;
+    a.max_pages = d.max_pages;
+    a.interleaved = r.interleaved ? 1 : 0;
+    // YaRN: pairs that turn often over the original context keep their frequency, slow ones are
+    // stretched by the factor, with a linear ramp in the number of turns between.
+    const double s = r.factor, pi = 3.14159265358979323846;
+    for (int i = 0; i < kHeadDim / 2; ++i) {
+        const double th = std::pow((double)r.theta, -2.0 * i / kHeadDim);
+        const double turns = (double)r.original_max_position * th / (2.0 * pi);
+        double gamma = (turns - r.beta_slow) / ((double)r.beta_fast - r.beta_slow);
+        gamma = gamma < 0.0 ? 0.0 : (gamma > 1.0 ? 1.0 : gamma);
+        a.inv_freq[i] = (1.0 - gamma) * th / s + gamma * th;
+    }
+    a.mscale = r.attn_factor > 0.f ? r.attn_factor : (s > 1.0 ? (float)(0.1 * std::log(s) + 1.0) : 1.f);
+    return qkv_prologue_launch(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SINKATTN_OK : SINKATTN_ERR_CUDA;
 }
 
 sinkattn_status_t sinkattn_prefill(const void* q, const void* k, const void* v, const int32_t* cu_seqlens,

@@ -88,6 +88,23 @@ struct AppendArgs {
 };
 cudaError_t kv_append_launch(const AppendArgs& args, cudaStream_t stream);
 
+// ------------------------------------------------------------------ pre-attention prologue
+struct PrologueArgs {
+    const __nv_bfloat16* qkv;   // [T, (Hq + 2 Hkv) * 64]: q heads, k heads, v heads
+    const __nv_bfloat16* bias;  // [(Hq + 2 Hkv) * 64] or null
+    const int32_t* cu_seqlens;  // [N+1] new tokens
+    const int32_t* start_pos;   // [N]
+    const int32_t* page_table;  // [N, max_pages]
+    __nv_bfloat16* q_out;       // [T, Hq, 64]
+    __nv_bfloat16* k_pages;     // [P, Hkv, 16, 64]
+    __nv_bfloat16* v_pages;
+    unsigned* err;
+    int N, T, Hq, Hkv, num_pages, max_pages, interleaved;
+    float mscale;                   // multiplier of rotated q and k
+    double inv_freq[kHeadDim / 2];  // rotation angle per position of each pair
+};
+cudaError_t qkv_prologue_launch(const PrologueArgs& args, cudaStream_t stream);
+
 // ------------------------------------------------------------------ merge
 struct MergeArgs {
     const float* part_o;    // [S, R, H, 64]

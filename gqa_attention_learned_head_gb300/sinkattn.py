@@ -46,6 +46,12 @@ class PagedDims(ctypes.Structure):
                                               "head_dim", "page_size", "num_pages", "max_pages")]
 
 
+class RopeParams(ctypes.Structure):
+    _fields_ = [("theta", ctypes.c_float), ("factor", ctypes.c_float), ("original_max_position", ctypes.c_int32),
+                ("beta_fast", ctypes.c_float), ("beta_slow", ctypes.c_float), ("attn_factor", ctypes.c_float),
+                ("interleaved", ctypes.c_int32)]
+
+
 class PrefillDims(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("num_seqs", "total_tokens", "max_seqlen", "num_q_heads",
                                               "num_kv_heads", "head_dim")]
@@ -56,7 +62,7 @@ class MergeDims(ctypes.Structure):
 
 
 EXPORTS = ("sinkattn_decode", "sinkattn_prefill", "sinkattn_merge", "sinkattn_decode_workspace_size", "sinkattn_verify",
-           "sinkattn_verify_workspace_size", "sinkattn_kv_append", "sinkattn_prefill_paged", "sinkattn_verify_tree",
+           "sinkattn_verify_workspace_size", "sinkattn_kv_append", "sinkattn_prefill_paged", "sinkattn_verify_tree", "sinkattn_qkv_prologue",
            "sinkattn_get_error", "sinkattn_status_string", "sinkattn_version")
 
 
@@ -78,13 +84,15 @@ def _load():
     lib.sinkattn_verify_workspace_size.restype = sz
     lib.sinkattn_verify_tree.argtypes = [P, P, P, P, P, P, P, f32, P, P, ctypes.POINTER(VerifyDims), P, sz, P]
     lib.sinkattn_kv_append.argtypes = [P, P, P, P, P, P, P, ctypes.POINTER(PagedDims), P]
+    lib.sinkattn_qkv_prologue.argtypes = [P, P, P, P, P, ctypes.POINTER(RopeParams), P, P, P,
+                                          ctypes.POINTER(PagedDims), P]
     lib.sinkattn_prefill_paged.argtypes = [P, P, P, P, P, P, P, f32, P, P, ctypes.POINTER(PagedDims), P]
     lib.sinkattn_get_error.argtypes = [P]
     lib.sinkattn_status_string.argtypes = [ctypes.c_int]
     lib.sinkattn_status_string.restype = ctypes.c_char_p
     lib.sinkattn_version.restype = i32
     for fn in ("sinkattn_decode", "sinkattn_prefill", "sinkattn_merge", "sinkattn_get_error", "sinkattn_verify",
-               "sinkattn_kv_append", "sinkattn_prefill_paged", "sinkattn_verify_tree"):
+               "sinkattn_kv_append", "sinkattn_prefill_paged", "sinkattn_verify_tree", "sinkattn_qkv_prologue", "sinkattn_qkv_prologue"):
         getattr(lib, fn).restype = ctypes.c_int
     return lib
 
@@ -264,6 +272,34 @@ def sinkattn_kv_append(k, v, cu_seqlens, start_pos, page_table, k_pages, v_pages
     st = _lib.sinkattn_kv_append(_ptr(k), _ptr(v), _ptr(cu_seqlens), _ptr(start_pos), _ptr(page_table),
                                  _ptr(k_pages), _ptr(v_pages), ctypes.byref(dims), _stream(stream))
     _check(st, "sinkattn_kv_append")
+
+
+def sinkattn_qkv_prologue(qkv, bias, cu_seqlens, start_pos, page_table, k_pages, v_pages, num_q_heads, theta,
+                          factor, original_max_position, beta_fast, beta_slow, attn_factor=0.0, interleaved=False,
+                          q_out=None, stream=None):
+    """QKV bias + YaRN rotary embedding of new tokens qkv [T, (Hq + 2 Hkv) * 64]; returns q [T, Hq, 64] and
+    writes the rotated k and the v into the pages at positions start_pos[n] + i (in place)."""
+    _need(qkv, "qkv", torch.bfloat16, 2)
+    if bias is not None:
+        _need(bias, "bias", torch.bfloat16, 1)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    _need(start_pos, "start_pos", torch.int32, 1)
+    _need(page_table, "page_table", torch.int32, 2)
+    _need(k_pages, "k_pages", torch.bfloat16, 4)
+    _need(v_pages, "v_pages", torch.bfloat16, 4)
+    T = qkv.shape[0]
+    Hkv = k_pages.shape[1]
+    if qkv.shape[1] != (num_q_heads + 2 * Hkv) * 64 or (bias is not None and bias.shape[0] != qkv.shape[1]):
+        raise ValueError("qkv must be [T, (Hq + 2 Hkv) * 64] and bias [(Hq + 2 Hkv) * 64]")
+    if q_out is None:
+        q_out = torch.empty(T, num_q_heads, 64, device=qkv.device, dtype=torch.bfloat16)
+    dims = paged_dims(k_pages, page_table, cu_seqlens, T, 0, num_q_heads)
+    rope = RopeParams(theta, factor, original_max_position, beta_fast, beta_slow, attn_factor, int(bool(interleaved)))
+    st = _lib.sinkattn_qkv_prologue(_ptr(qkv), _ptr(bias), _ptr(cu_seqlens), _ptr(start_pos), _ptr(page_table),
+                                    ctypes.byref(rope), _ptr(q_out), _ptr(k_pages), _ptr(v_pages), ctypes.byref(dims),
+                                    _stream(stream))
+    _check(st, "sinkattn_qkv_prologue")
+    return q_out
 
 
 def sinkattn_prefill_paged(q, k_pages, v_pages, page_table, cu_seqlens, start_pos, sinks, scale, max_seqlen=None,

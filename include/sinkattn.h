@@ -262,6 +262,48 @@ sinkattn_status_t sinkattn_prefill_paged(const void *q, const void *k_pages, con
                                          void *out, float *lse, const sinkattn_paged_dims_t *dims,
                                          void *stream);
 
+/* YaRN rotary embedding parameters (sinkattn_qkv_prologue). */
+typedef struct {
+    float theta;                    /* base of the rotary frequencies: theta^(-2d/64) for pair d  */
+    float factor;                   /* context extension factor s (>= 1; 1 = plain rotary)        */
+    int32_t original_max_position;  /* context length L the model was trained with               */
+    float beta_fast;                /* pairs turning more than beta_fast times over L keep their
+                                       frequency ...                                             */
+    float beta_slow;                /* ... pairs turning fewer than beta_slow times are slowed by s;
+                                       linear in between (beta_fast > beta_slow > 0)              */
+    float attn_factor;              /* multiplier of rotated q and k; 0 = 0.1 ln(s) + 1 (1 if s = 1) */
+    int32_t interleaved;            /* 0: pairs (d, d + 32); 1: pairs (2d, 2d + 1)                */
+} sinkattn_rope_t;
+
+/*
+ * The pre-attention step of new tokens, fused: QKV bias, YaRN rotary embedding
+ * of q and k, q to `q_out`, and k / v written straight into the tokens' page
+ * slots (what sinkattn_kv_append does for ready keys and values).  Source:
+ * "GPT-OSS on day 0", section "Attention: GQA with attention sinks" (QKV
+ * projections with a bias; YaRN positional encoding as in DeepSeek-V3).  The
+ * page gives no formulas; these follow the published YaRN method: for pair d,
+ * theta_d = theta^(-2d/64) and r_d = L theta_d / (2 pi) (turns over the
+ * original context); gamma = clamp((r_d - beta_slow) / (beta_fast - beta_slow),
+ * 0, 1); the angle per position is ((1 - gamma) / s + gamma) theta_d; rotated q
+ * and k are multiplied by attn_factor.
+ *
+ *   qkv        [T, (Hq + 2 Hkv) * 64] bf16  projected new tokens: Hq q heads, then Hkv k
+ *                                           heads, then Hkv v heads
+ *   bias       [(Hq + 2 Hkv) * 64]    bf16  added before the rotation, or NULL
+ *   cu_seqlens [N + 1], start_pos [N], page_table [N, max_pages]: as sinkattn_kv_append
+ *                                           (new token i of sequence n is at position
+ *                                           start_pos[n] + i)
+ *   q_out      [T, Hq, 64]            bf16
+ *   k_pages, v_pages [P, Hkv, 16, 64] bf16  the new tokens' slots are written
+ *
+ * Bad page ids and positions are reported as in sinkattn_kv_append (q_out is
+ * still written).
+ */
+sinkattn_status_t sinkattn_qkv_prologue(const void *qkv, const void *bias, const int32_t *cu_seqlens,
+                                        const int32_t *start_pos, const int32_t *page_table,
+                                        const sinkattn_rope_t *rope, void *q_out, void *k_pages,
+                                        void *v_pages, const sinkattn_paged_dims_t *dims, void *stream);
+
 /*
  * Causal (or full) prefill over packed variable-length sequences.
  * Source: "GPT-OSS on day 0", section "Kernels for GPT-OSS / Sink Attention"

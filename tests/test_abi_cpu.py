@@ -99,3 +99,16 @@ def test_paged_host_validation_without_device(S):
     d = S.PagedDims(0, 0, 0, 8, 2, 64, 16, 10, 4)  # nothing to do
     assert lib.sinkattn_kv_append(*([None] * 7), ctypes.byref(d), None) == 0
     assert lib.sinkattn_prefill_paged(*([None] * 7), 0.125, None, None, ctypes.byref(d), None) == 0
+
+
+def test_prologue_host_validation_without_device(S):
+    lib = S._lib
+    d = S.PagedDims(1, 4, 4, 8, 2, 64, 16, 10, 4)
+    ok = S.RopeParams(150000.0, 32.0, 4096, 32.0, 1.0, 0.0, 0)
+    call = lambda r, dd=d: lib.sinkattn_qkv_prologue(*([None] * 5), ctypes.byref(r) if r else None, None, None, None,
+                                                      ctypes.byref(dd), None)
+    assert call(None) == S.ERR_INVALID_ARG
+    assert call(S.RopeParams(150000.0, 0.5, 4096, 32.0, 1.0, 0.0, 0)) == S.ERR_INVALID_ARG   # factor < 1
+    assert call(S.RopeParams(150000.0, 32.0, 4096, 1.0, 32.0, 0.0, 0)) == S.ERR_INVALID_ARG  # beta_fast <= beta_slow
+    assert call(ok) == S.ERR_INVALID_ARG  # null buffers
+    assert call(ok, S.PagedDims(0, 0, 0, 8, 2, 64, 16, 10, 4)) == 0  # nothing to do
