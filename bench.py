@@ -299,6 +299,42 @@ def bench_tree_verify(S, W, rank, K, warmup, flush, stream):
     return inp, step, times, decode_bytes(inp.kv_lens, Hkv, D)
 
 
+YARN_GPT_OSS = dict(theta=150000.0, factor=32.0, original_max_position=4096, beta_fast=32.0, beta_slow=1.0)
+
+
+def bench_prologue_chunked(S, W, rank, K, warmup, flush, stream):
+    """The chunked prefill with the fused prologue in front: QKV bias + YaRN rotary of the new tokens
+    (q out, k/v into the pages), then the paged prefill.  Returns (ms list, prologue ms list, flops)."""
+    inp = W.chunked_prefill(device="cuda", seed=rank)
+    T, Hq, D = inp.q.shape
+    Hkv = inp.k_pages.shape[1]
+    g = torch.Generator(device="cuda")
+    g.manual_seed(1000 + rank)
+    qkv = torch.randn(T, (Hq + 2 * Hkv) * D, generator=g, device="cuda").to(torch.bfloat16)
+    bias = torch.randn((Hq + 2 * Hkv) * D, generator=g, device="cuda").to(torch.bfloat16)
+    q = torch.empty_like(inp.q)
+    out = torch.empty_like(inp.q)
+    lse = torch.empty(T, Hq, dtype=torch.float32, device="cuda")
+
+    def prologue():
+        S.sinkattn_qkv_prologue(qkv, bias, inp.cu_seqlens, inp.start_pos, inp.page_table, inp.k_pages, inp.v_pages,
+                                Hq, q_out=q, stream=stream, **YARN_GPT_OSS)
+
+    def step():
+        prologue()
+        S.sinkattn_prefill_paged(q, inp.k_pages, inp.v_pages, inp.page_table, inp.cu_seqlens, inp.start_pos,
+                                 inp.sinks, inp.scale, max_seqlen=inp.max_seqlen, out=out, lse=lse, stream=stream)
+
+    with torch.cuda.stream(stream):
+        times = timed_steps(step, K, warmup, flush, stream)
+        ptimes = timed_steps(prologue, K, warmup, flush, stream)
+    err = S.sinkattn_get_error(stream)
+    if err:
+        raise RuntimeError(f"device error {S.status_string(err)}")
+    moved = (qkv.numel() + q.numel() + 2 * T * Hkv * D) * 2 + bias.numel() * 2  # bytes read + written
+    return times, ptimes, 4 * D * Hq * inp.visible_pairs(), moved
+
+
 def bench_chunked(S, W, rank, K, warmup, flush, stream):
     """One step = the serving step of a chunked prefill: append the new tokens' K/V into the pages,
     then the paged prefill over prefix + new tokens.  Returns the attention flops per step."""
@@ -672,6 +708,14 @@ def run_ours(args):
                               "unit": "TFLOP/s", "ms_per_step": cms,
                               "frac_of_bf16_peak": cf / (cms * 1e-3) / 1e12 / tc_peak})
             del ci
+            st_, pt2, sf, moved = bench_prologue_chunked(S, W, rank, Ks, Wu, flush, stream)
+            sms, pms2 = statistics.mean(st_), statistics.mean(pt2)
+            secondary.append({"workload": "serving step of the chunked prefill: fused prologue (QKV bias + YaRN "
+                                          "rotary, k/v into the pages) + paged prefill, same sequences",
+                              "value": sf / (sms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": sms,
+                              "frac_of_bf16_peak": sf / (sms * 1e-3) / 1e12 / tc_peak,
+                              "prologue_ms": pms2, "prologue_GB/s": moved / (pms2 * 1e-3) / 1e9,
+                              "prologue_frac_of_hbm_peak": moved / (pms2 * 1e-3) / 1e9 / hbm_peak})
             secondary.append(bench_mixed(S, W, rank, Ks, Wu, flush, hbm_peak, tc_peak))
         except Exception as e:  # report, never hide
             secondary.append({"error": f"{type(e).__name__}: {e}"})
