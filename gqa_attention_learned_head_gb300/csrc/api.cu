@@ -438,8 +438,8 @@ sinkattn_status_t sinkattn_qkv_prologue(const void* qkv, const void* bias, const
     if (d.num_seqs == 0 || d.total_tokens == 0) return SINKATTN_OK;
     if (!qkv || !cu_seqlens || !start_pos || !page_table || !q_out || !k_pages || !v_pages)
         return SINKATTN_ERR_INVALID_ARG;
-    if (!aligned(qkv, 2) || (bias && !aligned(bias, 2)) || !aligned(q_out, 2) || !aligned(k_pages, 2) ||
-        !aligned(v_pages, 2) || !aligned(cu_seqlens, 4) || !aligned(start_pos, 4) || !aligned(page_table, 4))
+    if (!aligned(qkv, 16) || (bias && !aligned(bias, 16)) || !aligned(q_out, 16) || !aligned(k_pages, 16) ||
+        !aligned(v_pages, 16) || !aligned(cu_seqlens, 4) || !aligned(start_pos, 4) || !aligned(page_table, 4))
         return SINKATTN_ERR_INVALID_ARG;
     DeviceState* ds = nullptr;
     if ((st = device_state(&ds)) != SINKATTN_OK) return st;

@@ -296,8 +296,8 @@ typedef struct {
  *   q_out      [T, Hq, 64]            bf16
  *   k_pages, v_pages [P, Hkv, 16, 64] bf16  the new tokens' slots are written
  *
- * Bad page ids and positions are reported as in sinkattn_kv_append (q_out is
- * still written).
+ * bf16 buffers 16-byte aligned.  Bad page ids and positions are reported as in
+ * sinkattn_kv_append (q_out is still written).
  */
 sinkattn_status_t sinkattn_qkv_prologue(const void *qkv, const void *bias, const int32_t *cu_seqlens,
                                         const int32_t *start_pos, const int32_t *page_table,
