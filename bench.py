@@ -74,6 +74,16 @@ def peaks():
     return HBM_FALLBACK_GBS, BF16_FALLBACK_TFLOPS, 1700.0, "fallback"
 
 
+# Sources each profiled kernel is compiled from (its own file, the headers it includes).
+KERNEL_SOURCES = {
+    "decode_split_kernel": ["decode.cu", "ptx.cuh", "split_kv.cuh", "args_decode.h", "args_common.h"],
+    "verify_split_kernel": ["verify.cu", "ptx.cuh", "split_kv.cuh", "args_verify.h", "args_common.h"],
+    "prefill_pp_kernel": ["prefill_pp.cu", "ptx.cuh", "tile_order.cuh", "args_prefill.h", "args_common.h"],
+    "prefill_tc_kernel": ["prefill_tc.cu", "ptx.cuh", "tile_order.cuh", "args_prefill.h", "args_common.h"],
+    "prefill_tc_kernel_paged": ["prefill_tc.cu", "ptx.cuh", "tile_order.cuh", "args_prefill.h", "args_common.h"],
+}
+
+
 def kernel_source_hash(names):
     h = hashlib.sha256()
     for n in names:
@@ -530,12 +540,12 @@ def run_ours(args):
         value = total_bytes / (ms_max * 1e-3) / 1e9
         unit = "GB/s"
         achieved = nbytes / (ms * 1e-3) / 1e9
-        kname, ksrc, call = (("verify_split_kernel", "verify.cu", "sinkattn_verify") if name == "speculative_verify"
-                             else ("decode_split_kernel", "decode.cu", "sinkattn_decode"))
+        kname, call = (("verify_split_kernel", "sinkattn_verify") if name == "speculative_verify"
+                       else ("decode_split_kernel", "sinkattn_decode"))
         roof = {"bound": "hbm", "kernel": f"{kname} (the only kernel of a {call} call)",
                 "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                 "peak_source": f"{peak_src} hbm_gbs",
-                "traffic": profiled_traffic(kname, name, [ksrc, "ptx.cuh", "kernels.h", "split_kv.cuh"])}
+                "traffic": profiled_traffic(kname, name, KERNEL_SOURCES[kname])}
         launches = K  # one split kernel per step
         cfg_extra = {"kv_tokens": int(inp.kv_lens.sum()), "kv_bytes_per_step": nbytes}
     elif name == "chunked_prefill":
@@ -552,8 +562,7 @@ def run_ours(args):
                                              "step); achieved over the whole step",
                 "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s", "frac": achieved / tc_peak,
                 "peak_source": f"{peak_src} bf16_tflops",
-                "traffic": profiled_traffic("prefill_tc_kernel_paged", name,
-                                            ["prefill_tc.cu", "ptx.cuh", "kernels.h", "tile_order.cuh"])}
+                "traffic": profiled_traffic("prefill_tc_kernel_paged", name, KERNEL_SOURCES["prefill_tc_kernel_paged"])}
         launches = 2 * K  # append + paged prefill per step
         cfg_extra = {"new_tokens": int(inp.q.shape[0]), "cached_tokens": int(inp.start_pos.sum()),
                      "flops_per_step": flops}
@@ -568,12 +577,11 @@ def run_ours(args):
         unit = "TFLOP/s"
         achieved = flops / (ms * 1e-3) / 1e12
         # an even query-head group runs the two-head kernel, an odd one the one-head kernel
-        kname, ksrc = (("prefill_pp_kernel", "prefill_pp.cu") if (inp.q.shape[1] // inp.k.shape[1]) % 2 == 0
-                       else ("prefill_tc_kernel", "prefill_tc.cu"))
+        kname = "prefill_pp_kernel" if (inp.q.shape[1] // inp.k.shape[1]) % 2 == 0 else "prefill_tc_kernel"
         roof = {"bound": "tensor", "kernel": f"{kname} (the only kernel of a sinkattn_prefill call)",
                 "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s", "frac": achieved / tc_peak,
                 "peak_source": f"{peak_src} bf16_tflops",
-                "traffic": profiled_traffic(kname, name, [ksrc, "ptx.cuh", "kernels.h", "tile_order.cuh"])}
+                "traffic": profiled_traffic(kname, name, KERNEL_SOURCES[kname])}
         launches = K
         cfg_extra = {"tokens": int(inp.q.shape[0]), "flops_per_step": flops}
     # keep the GPU under the same load for >= 1.5 s of clock samples (not timed)
@@ -682,14 +690,14 @@ def run_ours(args):
             secondary.append({"workload": WORKLOAD_TEXT["long_context_decode"], "value": lb / (lms * 1e-3) / 1e9,
                               "unit": "GB/s", "ms_per_step": lms, "frac_of_hbm_peak": lb / (lms * 1e-3) / 1e9 / hbm_peak,
                               "traffic": profiled_traffic("decode_split_kernel", "long_context_decode",
-                                                          ["decode.cu", "ptx.cuh", "kernels.h", "split_kv.cuh"])})
+                                                          KERNEL_SOURCES["decode_split_kernel"])})
             del li
             vi, _, vt, vb = bench_verify(S, W, rank, Ks, Wu, flush, stream)
             vms = statistics.mean(vt)
             secondary.append({"workload": WORKLOAD_TEXT["speculative_verify"], "value": vb / (vms * 1e-3) / 1e9,
                               "unit": "GB/s", "ms_per_step": vms, "frac_of_hbm_peak": vb / (vms * 1e-3) / 1e9 / hbm_peak,
                               "traffic": profiled_traffic("verify_split_kernel", "speculative_verify",
-                                                          ["verify.cu", "ptx.cuh", "kernels.h", "split_kv.cuh"])})
+                                                          KERNEL_SOURCES["verify_split_kernel"])})
             del vi
             ti, _, tt, tb = bench_tree_verify(S, W, rank, Ks, Wu, flush, stream)
             tms = statistics.mean(tt)

@@ -37,7 +37,7 @@
 //    mma.m16n8k16 (no padding: M = a page, N = the group); the row max per
 //    head is a 3-step shuffle; P^T is re-laid out for the next MMA with
 //    movmatrix; O^T[64 x 8] += V^T * P^T.  Everything stays in registers.
-#include "kernels.h"
+#include "args_decode.h"
 #include "ptx.cuh"
 #include "split_kv.cuh"
 

@@ -11,7 +11,7 @@
 // Hkv x 64 bf16 keys and values in 16-byte pieces (a (page, KV head, slot) row
 // of 128 B is contiguous in the pool).  Page ids outside the pool and
 // positions past the page-table row are skipped and flagged.
-#include "kernels.h"
+#include "args_paged.h"
 #include "ptx.cuh"
 
 namespace sinkattn {

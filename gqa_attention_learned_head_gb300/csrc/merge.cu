@@ -10,7 +10,7 @@
 // fp32 partial rows are read with coalesced 8-byte loads and the bf16 output
 // row is written as one 128-byte line.  HBM-bound and tiny next to the decode
 // pass that produces the partials.
-#include "kernels.h"
+#include "args_merge.h"
 #include "ptx.cuh"
 
 namespace sinkattn {

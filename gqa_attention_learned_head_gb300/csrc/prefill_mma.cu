@@ -9,7 +9,7 @@
 // written for sm_103a: 4 warps x 16 query rows, 64-key tiles double-buffered
 // with cp.async, scores and P.V on mma.sync, P kept in registers.  It is the
 // baseline the tcgen05 kernel (prefill_tc.cu) is measured against.
-#include "kernels.h"
+#include "args_prefill.h"
 #include "ptx.cuh"
 #include "tile_order.cuh"
 

@@ -24,7 +24,7 @@
 // TMEM columns: S_w at 128 w, O_w at 256 + 64 w, P_w (bf16 pairs) at 384 + 64 w.
 // Every wait is bounded; a wait that gives up sets the device error word and
 // the kernel winds down (the other waits then give up too).
-#include "kernels.h"
+#include "args_prefill.h"
 #include "ptx.cuh"
 #include "tile_order.cuh"
 

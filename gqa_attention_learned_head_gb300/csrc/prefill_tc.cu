@@ -24,7 +24,7 @@
 //               O / d -- d including the sink term -- and the log-sum-exp.
 // TMEM columns: [0,128) S fp32, [128,192) O fp32, [192,256) P bf16 pairs.
 // Every wait is bounded; a wait that gives up sets the device error word.
-#include "kernels.h"
+#include "args_prefill.h"
 #include "ptx.cuh"
 #include "tile_order.cuh"
 

@@ -17,7 +17,7 @@
 // rotated pairs in two 16-byte pieces (pairs (d, d + 32): elements 8l..8l+7 and
 // 8l+32..8l+39; pairs (2d, 2d + 1): elements 16l..16l+15), eight heads per pass
 // of the warp.
-#include "kernels.h"
+#include "args_paged.h"
 #include "ptx.cuh"
 
 namespace sinkattn {

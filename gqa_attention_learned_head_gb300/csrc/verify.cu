@@ -34,7 +34,7 @@
 // Every wait is bounded; a wait that gives up sets the device error word.
 #include <climits>
 
-#include "kernels.h"
+#include "args_verify.h"
 #include "ptx.cuh"
 #include "split_kv.cuh"
 
