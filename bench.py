@@ -2,8 +2,8 @@
 """Benchmark of libsinkattn (sink attention, GQA, paged split-KV decode + causal prefill).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload batched_paged_decode|long_context_decode|speculative_verify|causal_prefill|
-                                chunked_prefill]
+                    [--workload batched_paged_decode|long_context_decode|speculative_verify|tree_verify|
+                                causal_prefill|chunked_prefill|serving_step]
 
 Headline: decode KV GB/s on the batched paged decode workload (batch 32,
 64 q / 8 KV heads, head_dim 64, kv_len uniform in [512, 4096], 16-token pages
@@ -54,6 +54,9 @@ WORKLOAD_TEXT = {
                        "+ paged prefill",
     "tree_verify": "verification of a draft tree: batch 32, an EAGLE-style tree of 8 drafted tokens per request "
                    "(depth 4) over the paged cache, 64 q / 8 KV heads, kv_len U[512,4096] (drafts included)",
+    "serving_step": "serving step of the chunked prefill: fused prologue (QKV bias + YaRN rotary of the new tokens, "
+                    "q out, k/v into the pages) + paged prefill; 8 sequences, U[1024,8192] cached + U[256,2048] new "
+                    "tokens each, 64 q / 8 KV heads, head_dim 64",
     "speculative_verify": "verification of drafts: batch 32, 4 query tokens per request over the paged cache, "
                           "64 q / 8 KV heads, head_dim 64, kv_len U[512,4096] (drafts included), permuted pages",
     "mixed_serving": "mixed serving batch: 8 causal prefills L~U[256,4096] + 256 paged decodes kv_len~U[1024,32768], "
@@ -81,6 +84,7 @@ KERNEL_SOURCES = {
     "prefill_pp_kernel": ["prefill_pp.cu", "ptx.cuh", "tile_order.cuh", "args_prefill.h", "args_common.h"],
     "prefill_tc_kernel": ["prefill_tc.cu", "ptx.cuh", "tile_order.cuh", "args_prefill.h", "args_common.h"],
     "prefill_tc_kernel_paged": ["prefill_tc.cu", "ptx.cuh", "tile_order.cuh", "args_prefill.h", "args_common.h"],
+    "qkv_prologue_kernel": ["prologue.cu", "ptx.cuh", "args_paged.h", "args_common.h"],
 }
 
 
@@ -306,7 +310,7 @@ def bench_tree_verify(S, W, rank, K, warmup, flush, stream):
     err = S.sinkattn_get_error(stream)
     if err:
         raise RuntimeError(f"device error {S.status_string(err)}")
-    return inp, step, times, decode_bytes(inp.kv_lens, Hkv, D)
+    return inp, step, times, decode_bytes(inp.kv_lens, Hkv, D), masks
 
 
 YARN_GPT_OSS = dict(theta=150000.0, factor=32.0, original_max_position=4096, beta_fast=32.0, beta_slow=1.0)
@@ -314,7 +318,8 @@ YARN_GPT_OSS = dict(theta=150000.0, factor=32.0, original_max_position=4096, bet
 
 def bench_prologue_chunked(S, W, rank, K, warmup, flush, stream):
     """The chunked prefill with the fused prologue in front: QKV bias + YaRN rotary of the new tokens
-    (q out, k/v into the pages), then the paged prefill.  Returns (ms list, prologue ms list, flops)."""
+    (q out, k/v into the pages), then the paged prefill.  Returns (inputs, step, ms list, flops,
+    prologue ms list, prologue bytes moved, (qkv, bias))."""
     inp = W.chunked_prefill(device="cuda", seed=rank)
     T, Hq, D = inp.q.shape
     Hkv = inp.k_pages.shape[1]
@@ -342,7 +347,7 @@ def bench_prologue_chunked(S, W, rank, K, warmup, flush, stream):
     if err:
         raise RuntimeError(f"device error {S.status_string(err)}")
     moved = (qkv.numel() + q.numel() + 2 * T * Hkv * D) * 2 + bias.numel() * 2  # bytes read + written
-    return times, ptimes, 4 * D * Hq * inp.visible_pairs(), moved
+    return inp, step, times, 4 * D * Hq * inp.visible_pairs(), ptimes, moved, (qkv, bias)
 
 
 def bench_chunked(S, W, rank, K, warmup, flush, stream):
@@ -384,28 +389,40 @@ def bench_prefill(S, W, name, rank, K, warmup, flush, stream):
     return inp, step, times, flops
 
 
-def cpu_baseline_decode(inp, budget_s=12.0):
+def oracle_request(inp, b, masks=None):
+    """Runs the fp64 oracle on every query row of request b of a decode / verification workload
+    (inputs on the host); returns the cache bytes that request reads."""
+    import oracle
+
+    B, Hq = inp.q.shape[0], inp.q.shape[-2]
+    Hkv = inp.k_pages.shape[1]
+    args = (inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens)
+    if inp.q.dim() == 4:  # verification inputs carry q_len query tokens per request
+        QL = inp.q.shape[1]
+        rows = torch.tensor([[b, i, h] for i in range(QL) for h in range(Hq)], dtype=torch.int32).numpy()
+        if masks is None:
+            oracle.verify(*args, inp.sinks, inp.scale, rows=rows)
+        else:
+            oracle.verify_tree(*args, masks, inp.sinks, inp.scale, rows=rows)
+    else:
+        rows = torch.tensor([[b, h] for h in range(Hq)], dtype=torch.int32).numpy()
+        oracle.decode(*args, inp.sinks, inp.scale, rows=rows)
+    return int(inp.kv_lens[b]) * Hkv * 64 * 4
+
+
+def cpu_baseline_decode(inp, masks=None, budget_s=12.0):
     """The fp64 oracle on the host cores, on whole requests of the same workload, ~budget_s of CPU work."""
     import oracle
 
-    q, kp, vp = inp.q.cpu(), inp.k_pages.cpu(), inp.v_pages.cpu()
-    pt, kl, sk = inp.page_table.cpu(), inp.kv_lens.cpu(), inp.sinks.cpu()
-    B, Hq = q.shape[0], q.shape[-2]
-    QL = q.shape[1] if q.dim() == 4 else 1  # verification inputs carry q_len query tokens per request
-    Hkv = kp.shape[1]
+    inp = inp.to("cpu")
+    masks = masks.cpu() if masks is not None else None
+    B, Hq = inp.q.shape[0], inp.q.shape[-2]
+    QL = inp.q.shape[1] if inp.q.dim() == 4 else 1
     done_bytes, reqs = 0, 0
     t0 = time.perf_counter()
-    b = 0
     while time.perf_counter() - t0 < budget_s:
-        if q.dim() == 4:
-            rows = torch.tensor([[b % B, i, h] for i in range(QL) for h in range(Hq)], dtype=torch.int32)
-            oracle.verify(q, kp, vp, pt, kl, sk, inp.scale, rows=rows.numpy())
-        else:
-            rows = torch.stack([torch.full((Hq,), b % B, dtype=torch.int32), torch.arange(Hq, dtype=torch.int32)], 1)
-            oracle.decode(q, kp, vp, pt, kl, sk, inp.scale, rows=rows.numpy())
-        done_bytes += int(kl[b % B]) * Hkv * 64 * 4
+        done_bytes += oracle_request(inp, reqs % B, masks)
         reqs += 1
-        b += 1
     dt = time.perf_counter() - t0
     return {"value": done_bytes / dt / 1e9, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"{reqs} whole requests (all {QL} x {Hq} query rows) of the same workload, fp64, {dt:.1f} s"}
@@ -437,6 +454,47 @@ def cpu_baseline_chunked(inp, budget_s=8.0):
             "sample": f"{n} random new-token rows (all {Hq} heads) of the workload after the append, fp64, {dt:.1f} s"}
 
 
+def cpu_baseline_serving(inp, qkv, bias, budget_s=10.0):
+    """The fp64 oracle for the serving step: the prologue of every new token (bias + YaRN rotary,
+    k/v into the pages), then the paged prefill of random rows, the prefill part scaled to the whole
+    step by its share of the step's pairs."""
+    import numpy as np
+
+    import oracle
+
+    inp = inp.to("cpu")
+    qkv, bias = qkv.cpu(), bias.cpu()
+    T, Hq, _ = inp.q.shape
+    Hkv = inp.k_pages.shape[1]
+    to_bf16 = lambda a: torch.from_numpy(a).float().to(torch.bfloat16)
+    t0 = time.perf_counter()
+    q, k, v = oracle.qkv_prologue(qkv, bias, inp.cu_seqlens, inp.start_pos, Hq, Hkv, **YARN_GPT_OSS)
+    kb, vb = oracle.kv_append(to_bf16(k), to_bf16(v), inp.cu_seqlens, inp.start_pos, inp.page_table, inp.k_pages,
+                              inp.v_pages)
+    q = to_bf16(q)
+    t_pro = time.perf_counter() - t0
+    rng = np.random.default_rng(0)
+    cul, spl = inp.cu_seqlens.tolist(), inp.start_pos.tolist()
+    pairs, n = 0, 0
+    t1 = time.perf_counter()
+    while time.perf_counter() - t1 < budget_s:
+        t = int(rng.integers(0, T))
+        rows = np.stack([np.full(Hq, t), np.arange(Hq)], 1).astype(np.int32)
+        oracle.prefill_paged(q, kb, vb, inp.page_table, inp.cu_seqlens, inp.start_pos, inp.sinks, inp.scale,
+                             rows=rows)
+        s = max(i for i in range(len(cul) - 1) if cul[i] <= t)
+        pairs += (spl[s] + t - cul[s] + 1) * Hq
+        n += 1
+    t_rows = time.perf_counter() - t1
+    total_pairs = Hq * inp.visible_pairs()
+    step_s = t_pro + t_rows * total_pairs / pairs
+    return {"value": 4 * 64 * total_pairs / step_s / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"the prologue + append of all {T} new tokens ({t_pro:.1f} s), then {n} random new-token rows "
+                      f"(all {Hq} heads) of the paged prefill ({t_rows:.1f} s), scaled to the step's "
+                      f"{total_pairs} (row, key) pairs; fp64"}
+
+
 def cpu_baseline_prefill(inp, budget_s=8.0):
     import numpy as np
 
@@ -463,38 +521,85 @@ def cpu_baseline_prefill(inp, budget_s=8.0):
 # ----------------------------------------------------------------------------- arms
 
 def run_reference(args):
-    """Reference arm: the fp64 oracle, as it stands, on the host cores (rank 0 only)."""
+    """Reference arm: the fp64 oracle, as it stands, on the host cores (rank 0 only), on the same
+    workload, metric and unit as the GPU arm.  Decode-type workloads: one step = whole requests
+    (every query row); prefill-type workloads: one step = a fixed number of random new-token rows
+    (all heads), counted by the (row, key) pairs they cover."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
+    import numpy as np
+
     from gqa_attention_learned_head_gb300 import workloads as W
     import oracle
 
-    inp = W.batched_paged_decode(device="cpu", seed=0)
-    B, Hq, _ = inp.q.shape
-    Hkv = inp.k_pages.shape[1]
-    per_step = B  # one step = the whole batch of the workload (tens of ms of CPU on 16 cores)
+    name = args.workload
+    masks, pre = None, None
+    if name in ("batched_paged_decode", "long_context_decode", "tiny_decode", "speculative_verify", "tree_verify"):
+        if name == "tree_verify":
+            inp, masks = W.tree_verify(device="cpu", seed=0)
+        else:
+            inp = getattr(W, name)(device="cpu", seed=0)
+        B, Hq = inp.q.shape[0], inp.q.shape[-2]
+        # about a quarter of a second of oracle work per step on 16 cores; a 131072-token request is a step of its own
+        per_step = {"long_context_decode": 1, "speculative_verify": 8, "tree_verify": 4}.get(name, B)
+        unit, scale_units = "GB/s", 1e9
+        step_text = f"{per_step} whole request(s) x all query rows through the fp64 CPU oracle"
 
-    def step(i):
-        bs = [(i * per_step + j) % B for j in range(per_step)]
-        rows = torch.tensor([[b, h] for b in bs for h in range(Hq)], dtype=torch.int32).numpy()
-        oracle.decode(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.kv_lens, inp.sinks, inp.scale, rows=rows)
-        return sum(int(inp.kv_lens[b]) for b in bs) * Hkv * 64 * 4
+        def step(i):
+            return sum(oracle_request(inp, (i * per_step + j) % B, masks) for j in range(per_step))
+    else:
+        to_bf16 = lambda a: torch.from_numpy(a).float().to(torch.bfloat16)
+        if name in ("causal_prefill",):
+            inp = W.causal_prefill(device="cpu", seed=0)
+            starts = [0] * len(inp.seqlens)
+            run_rows = lambda rows: oracle.prefill(inp.q, inp.k, inp.v, inp.cu_seqlens, inp.sinks, inp.scale, True,
+                                                   rows=rows)
+        else:
+            inp = W.chunked_prefill(device="cpu", seed=0)
+            starts = inp.start_pos.tolist()
+            if name == "serving_step":  # the prologue's output is the prefill's q / k / v (setup, not timed)
+                T, Hq = inp.q.shape[:2]
+                Hkv = inp.k_pages.shape[1]
+                g = torch.Generator().manual_seed(1000)
+                qkv = torch.randn(T, (Hq + 2 * Hkv) * 64, generator=g).to(torch.bfloat16)
+                bias = torch.randn((Hq + 2 * Hkv) * 64, generator=g).to(torch.bfloat16)
+                q, k, v = oracle.qkv_prologue(qkv, bias, inp.cu_seqlens, inp.start_pos, Hq, Hkv, **YARN_GPT_OSS)
+                inp.q, inp.k_new, inp.v_new = to_bf16(q), to_bf16(k), to_bf16(v)
+            kb, vb = oracle.kv_append(inp.k_new, inp.v_new, inp.cu_seqlens, inp.start_pos, inp.page_table,
+                                      inp.k_pages, inp.v_pages)
+            run_rows = lambda rows: oracle.prefill_paged(inp.q, kb, vb, inp.page_table, inp.cu_seqlens,
+                                                         inp.start_pos, inp.sinks, inp.scale, rows=rows)
+        T, Hq = inp.q.shape[:2]
+        cul = inp.cu_seqlens.tolist()
+        rng = np.random.default_rng(0)
+        per_step = 2
+        unit, scale_units = "TFLOP/s", 1e12
+        step_text = (f"{per_step} random new-token rows x {Hq} heads through the fp64 CPU oracle"
+                     + (" (the append / prologue done once, untimed)" if name != "causal_prefill" else ""))
+
+        def step(i):
+            flops = 0
+            for _ in range(per_step):
+                t = int(rng.integers(0, T))
+                run_rows(np.stack([np.full(Hq, t), np.arange(Hq)], 1).astype(np.int32))
+                n = max(j for j in range(len(cul) - 1) if cul[j] <= t)
+                flops += 4 * 64 * Hq * (starts[n] + t - cul[n] + 1)
+            return flops
 
     for i in range(args.warmup):
         step(i)
     t0 = time.perf_counter()
-    nbytes = sum(step(args.warmup + i) for i in range(args.steps))
+    units = sum(step(args.warmup + i) for i in range(args.steps))
     dt = time.perf_counter() - t0
-    value = nbytes / dt / 1e9
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+    value = units / dt / scale_units
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD_TEXT["batched_paged_decode"],
-                       "step": f"{per_step} whole requests x {Hq} heads through the fp64 CPU oracle"},
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
-                             "sample": f"the whole batch ({per_step} requests x {Hq} heads) per step, {args.steps} steps"},
-            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "config": {"workload": WORKLOAD_TEXT[name], "step": step_text},
+            "cpu_baseline": {"value": value, "unit": unit, "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": f"{step_text}, per step; {args.steps} steps"},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
@@ -526,10 +631,13 @@ def run_ours(args):
     barrier(world)
     torch.cuda.synchronize()
     t_load0 = time.time()
-    if name in ("batched_paged_decode", "long_context_decode", "tiny_decode", "speculative_verify"):
+    masks = None
+    if name in ("batched_paged_decode", "long_context_decode", "tiny_decode", "speculative_verify", "tree_verify"):
         workers = 0
         if name == "speculative_verify":
             inp, step, times, nbytes = bench_verify(S, W, rank, K, Wu, flush, stream)
+        elif name == "tree_verify":
+            inp, step, times, nbytes, masks = bench_tree_verify(S, W, rank, K, Wu, flush, stream)
         else:
             inp, step, times, nbytes = bench_decode(S, W, name, rank, K, Wu, flush, stream, workers)
         ms = statistics.mean(times)
@@ -540,16 +648,21 @@ def run_ours(args):
         value = total_bytes / (ms_max * 1e-3) / 1e9
         unit = "GB/s"
         achieved = nbytes / (ms * 1e-3) / 1e9
-        kname, call = (("verify_split_kernel", "sinkattn_verify") if name == "speculative_verify"
-                       else ("decode_split_kernel", "sinkattn_decode"))
+        kname, call = {"speculative_verify": ("verify_split_kernel", "sinkattn_verify"),
+                       "tree_verify": ("verify_split_kernel", "sinkattn_verify_tree")}.get(
+                           name, ("decode_split_kernel", "sinkattn_decode"))
         roof = {"bound": "hbm", "kernel": f"{kname} (the only kernel of a {call} call)",
                 "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                 "peak_source": f"{peak_src} hbm_gbs",
                 "traffic": profiled_traffic(kname, name, KERNEL_SOURCES[kname])}
         launches = K  # one split kernel per step
         cfg_extra = {"kv_tokens": int(inp.kv_lens.sum()), "kv_bytes_per_step": nbytes}
-    elif name == "chunked_prefill":
-        inp, step, times, flops = bench_chunked(S, W, rank, K, Wu, flush, stream)
+    elif name in ("chunked_prefill", "serving_step"):
+        if name == "chunked_prefill":
+            inp, step, times, flops = bench_chunked(S, W, rank, K, Wu, flush, stream)
+        else:
+            inp, step, times, flops, ptimes, moved, (qkv, bias) = bench_prologue_chunked(S, W, rank, K, Wu, flush,
+                                                                                        stream)
         total_flops = sum_over_ranks(float(flops), world)
         ms = statistics.mean(times)
         torch.cuda.synchronize()
@@ -558,12 +671,22 @@ def run_ours(args):
         value = total_flops / (ms_max * 1e-3) / 1e12
         unit = "TFLOP/s"
         achieved = flops / (ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "kernel": "prefill_tc_kernel<paged> + kv_append_kernel (the two kernels of a "
-                                             "step); achieved over the whole step",
+        first = "kv_append_kernel" if name == "chunked_prefill" else "qkv_prologue_kernel"
+        roof = {"bound": "tensor", "kernel": f"prefill_tc_kernel<paged> + {first} (the two kernels of a step); "
+                                             "achieved over the whole step",
                 "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s", "frac": achieved / tc_peak,
                 "peak_source": f"{peak_src} bf16_tflops",
-                "traffic": profiled_traffic("prefill_tc_kernel_paged", name, KERNEL_SOURCES["prefill_tc_kernel_paged"])}
-        launches = 2 * K  # append + paged prefill per step
+                "traffic": profiled_traffic("prefill_tc_kernel_paged", "chunked_prefill",
+                                            KERNEL_SOURCES["prefill_tc_kernel_paged"])}
+        if name == "serving_step":
+            p_ms = statistics.mean(ptimes)
+            p_gbs = moved / (p_ms * 1e-3) / 1e9
+            roof["prologue"] = {"bound": "hbm", "kernel": "qkv_prologue_kernel, timed alone", "ms": p_ms,
+                                "achieved": p_gbs, "peak": hbm_peak, "unit": "GB/s", "frac": p_gbs / hbm_peak,
+                                "bytes_per_launch": moved,
+                                "traffic": profiled_traffic("qkv_prologue_kernel", name,
+                                                            KERNEL_SOURCES["qkv_prologue_kernel"])}
+        launches = 2 * K  # append (or prologue) + paged prefill per step
         cfg_extra = {"new_tokens": int(inp.q.shape[0]), "cached_tokens": int(inp.start_pos.sum()),
                      "flops_per_step": flops}
     else:
@@ -624,6 +747,36 @@ def run_ours(args):
                "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in (h_out, h_lse)),
                "note": "the page pools stay resident (they are the cache); new tokens' q/k/v and the metadata "
                        "come from pinned host memory every step and the output + lse are read back"}
+    elif name == "serving_step":
+        srcs = (qkv, inp.cu_seqlens, inp.start_pos, inp.page_table)
+        h_in = [t.cpu().pin_memory() for t in srcs]
+        d_in = [torch.empty_like(t) for t in srcs]
+        h_out = torch.empty(inp.q.shape, dtype=torch.bfloat16).pin_memory()
+        h_lse = torch.empty(inp.q.shape[:2], dtype=torch.float32).pin_memory()
+        d_q, d_out = torch.empty_like(inp.q), torch.empty_like(inp.q)
+        d_lse = torch.empty(inp.q.shape[:2], dtype=torch.float32, device="cuda")
+        Hq = inp.q.shape[1]
+
+        def e2e_step():
+            for h, d in zip(h_in, d_in):
+                d.copy_(h, non_blocking=True)
+            x, cu, sp, pt = d_in
+            S.sinkattn_qkv_prologue(x, bias, cu, sp, pt, inp.k_pages, inp.v_pages, Hq, q_out=d_q, stream=stream,
+                                    **YARN_GPT_OSS)
+            S.sinkattn_prefill_paged(d_q, inp.k_pages, inp.v_pages, pt, cu, sp, inp.sinks, inp.scale,
+                                     max_seqlen=inp.max_seqlen, out=d_out, lse=d_lse, stream=stream)
+            h_out.copy_(d_out, non_blocking=True)
+            h_lse.copy_(d_lse, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            et = timed_steps(e2e_step, K, Wu, flush, stream)
+        e_ms = max_over_ranks(statistics.mean(et), world)
+        e2e = {"value": total_flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e_ms,
+               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in h_in),
+               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in (h_out, h_lse)),
+               "note": "the page pools and the QKV bias stay resident; the new tokens' fused QKV projection "
+                       "output and the metadata come from pinned host memory every step and the output + lse "
+                       "are read back"}
     elif name == "causal_prefill":
         h_in = [t.cpu().pin_memory() for t in (inp.q, inp.k, inp.v, inp.cu_seqlens)]
         d_in = [torch.empty_like(t) for t in (inp.q, inp.k, inp.v, inp.cu_seqlens)]
@@ -653,9 +806,18 @@ def run_ours(args):
         h_out = torch.empty(inp.q.shape, dtype=torch.bfloat16).pin_memory()
         h_lse = torch.empty(inp.q.shape[:-1], dtype=torch.float32).pin_memory()
         d_q, d_pt, d_kl = torch.empty_like(inp.q), torch.empty_like(inp.page_table), torch.empty_like(inp.kv_lens)
-        verify = name == "speculative_verify"
+        verify = name in ("speculative_verify", "tree_verify")
         ws_size = S.sinkattn_verify_workspace_size if verify else S.sinkattn_decode_workspace_size
         api = S.sinkattn_verify if verify else S.sinkattn_decode
+        h_extra = []
+        if masks is not None:  # draft trees: the masks are per-step input too
+            h_m = torch.as_tensor(masks, dtype=torch.int64).pin_memory()
+            d_m = torch.empty_like(h_m, device="cuda")
+            h_extra = [h_m]
+
+            def api(q, kp, vp, pt, kl, sinks, scale, **kw):
+                d_m.copy_(h_m, non_blocking=True)
+                return S.sinkattn_verify_tree(q, kp, vp, pt, kl, d_m, sinks, scale, **kw)
         ws = torch.empty(ws_size(inp.q, inp.k_pages, inp.page_table), dtype=torch.uint8, device="cuda")
         d_out = torch.empty_like(inp.q)
         d_lse = torch.empty(inp.q.shape[:-1], dtype=torch.float32, device="cuda")
@@ -672,7 +834,7 @@ def run_ours(args):
         with torch.cuda.stream(stream):
             et = timed_steps(e2e_step, K, Wu, flush, stream)
         e_ms = max_over_ranks(statistics.mean(et), world)
-        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_pt, h_kl))
+        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_pt, h_kl, *h_extra))
         d2h = sum(t.numel() * t.element_size() for t in (h_out, h_lse))
         e2e = {"value": total_bytes / (e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e_ms,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -699,10 +861,12 @@ def run_ours(args):
                               "traffic": profiled_traffic("verify_split_kernel", "speculative_verify",
                                                           KERNEL_SOURCES["verify_split_kernel"])})
             del vi
-            ti, _, tt, tb = bench_tree_verify(S, W, rank, Ks, Wu, flush, stream)
+            ti, _, tt, tb, _ = bench_tree_verify(S, W, rank, Ks, Wu, flush, stream)
             tms = statistics.mean(tt)
             secondary.append({"workload": WORKLOAD_TEXT["tree_verify"], "value": tb / (tms * 1e-3) / 1e9,
-                              "unit": "GB/s", "ms_per_step": tms, "frac_of_hbm_peak": tb / (tms * 1e-3) / 1e9 / hbm_peak})
+                              "unit": "GB/s", "ms_per_step": tms, "frac_of_hbm_peak": tb / (tms * 1e-3) / 1e9 / hbm_peak,
+                              "traffic": profiled_traffic("verify_split_kernel", "tree_verify",
+                                                          KERNEL_SOURCES["verify_split_kernel"])})
             del ti
             pi, _, pt_, pf = bench_prefill(S, W, "causal_prefill", rank, Ks, Wu, flush, stream)
             pms = statistics.mean(pt_)
@@ -716,7 +880,7 @@ def run_ours(args):
                               "unit": "TFLOP/s", "ms_per_step": cms,
                               "frac_of_bf16_peak": cf / (cms * 1e-3) / 1e12 / tc_peak})
             del ci
-            st_, pt2, sf, moved = bench_prologue_chunked(S, W, rank, Ks, Wu, flush, stream)
+            _, _, st_, sf, pt2, moved, _ = bench_prologue_chunked(S, W, rank, Ks, Wu, flush, stream)
             sms, pms2 = statistics.mean(st_), statistics.mean(pt2)
             secondary.append({"workload": "serving step of the chunked prefill: fused prologue (QKV bias + YaRN "
                                           "rotary, k/v into the pages) + paged prefill, same sequences",
@@ -730,8 +894,9 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = (cpu_baseline_decode(inp) if unit == "GB/s" else
-               cpu_baseline_chunked(inp) if name == "chunked_prefill" else cpu_baseline_prefill(inp))
+        cpu = (cpu_baseline_decode(inp, masks) if unit == "GB/s" else
+               cpu_baseline_chunked(inp) if name == "chunked_prefill" else
+               cpu_baseline_serving(inp, qkv, bias) if name == "serving_step" else cpu_baseline_prefill(inp))
 
     clocks = None
     if sampler:
@@ -793,7 +958,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="batched_paged_decode",
                     choices=["batched_paged_decode", "long_context_decode", "tiny_decode", "speculative_verify",
-                             "causal_prefill", "chunked_prefill"])
+                             "tree_verify", "causal_prefill", "chunked_prefill", "serving_step"])
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernels-only", action="store_true",

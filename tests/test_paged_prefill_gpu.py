@@ -91,3 +91,29 @@ def test_chunked_prefill_full_size_sampled(S):
                                   rows=rows)
     assert_parity(out[rows[:, 0], rows[:, 1]], lse[rows[:, 0], rows[:, 1]], ro, rl, "chunked prefill")
     assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
+
+
+def test_append_reports_bad_pages_and_positions(S):
+    inp = W.make_paged_prefill(8, 2, [16, 16], [4, 4], seed=54)
+    g = inp.to("cuda")
+    before_k = g.k_pages.clone()
+    pt = g.page_table.clone()
+    pt[1, 1] = -7  # sequence 1's new tokens (positions 16..19) land in page index 1
+    S.sinkattn_kv_append(g.k_new, g.v_new, g.cu_seqlens, g.start_pos, pt, g.k_pages, g.v_pages)
+    assert S.sinkattn_get_error() == S.ERR_BAD_PAGE
+    # sequence 0's tokens were written, sequence 1's skipped: only sequence 0's slots changed
+    changed = (g.k_pages != before_k).any(dim=-1).nonzero().tolist()
+    assert changed and all(p == int(inp.page_table[0, 1]) for p, _, _ in changed)
+    far = torch.tensor([10 ** 6, 0], dtype=torch.int32, device="cuda")  # past max_pages * 16
+    S.sinkattn_kv_append(g.k_new, g.v_new, g.cu_seqlens, far, g.page_table, g.k_pages, g.v_pages)
+    assert S.sinkattn_get_error() == S.ERR_BAD_LENGTH
+
+
+def test_paged_prefill_reports_bad_length(S):
+    inp = W.make_paged_prefill(8, 2, [16, 16], [4, 4], seed=55)
+    g = inp.to("cuda")
+    far = torch.tensor([10 ** 6, 16], dtype=torch.int32, device="cuda")
+    out, lse = S.sinkattn_prefill_paged(g.q, g.k_pages, g.v_pages, g.page_table, g.cu_seqlens, far, g.sinks, g.scale,
+                                        max_seqlen=inp.max_seqlen)
+    assert S.sinkattn_get_error() == S.ERR_BAD_LENGTH
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()

@@ -90,3 +90,18 @@ def test_plain_rope_without_bias(S):
     rq, _, _ = oracle.qkv_prologue(qkv, torch.zeros(qkv.shape[1], dtype=torch.bfloat16), pp.cu_seqlens,
                                    pp.start_pos, Hq, Hkv, **cfg)
     bf16_close(q.float().cpu().numpy(), rq, "q")
+
+
+def test_prologue_reports_bad_page_and_still_writes_q(S):
+    Hq, Hkv = 8, 2
+    pp, qkv, bias = inputs(Hq, Hkv, [16], [5], seed=93)
+    g = pp.to("cuda")
+    pt = g.page_table.clone()
+    pt[0, 1] = pp.k_pages.shape[0] + 2
+    before = g.k_pages.clone()
+    q = S.sinkattn_qkv_prologue(qkv.cuda(), bias.cuda(), g.cu_seqlens, g.start_pos, pt, g.k_pages, g.v_pages, Hq,
+                                **YARN)
+    assert S.sinkattn_get_error() == S.ERR_BAD_PAGE
+    assert torch.equal(g.k_pages, before)  # nothing written through the bad page id
+    rq, _, _ = oracle.qkv_prologue(qkv, bias, pp.cu_seqlens, pp.start_pos, Hq, Hkv, **YARN)
+    bf16_close(q.float().cpu().numpy(), rq, "q")
