@@ -47,7 +47,7 @@ WORKLOAD_TEXT = {
     "batched_paged_decode": "batched paged decode: batch 32, 64 q / 8 KV heads, head_dim 64, kv_len U[512,4096], "
                             "16-token pages randomly permuted in the pool",
     "long_context_decode": "long-context split-KV decode: batch 4, 64 q / 8 KV heads, head_dim 64, kv_len 131072, "
-                           "32 chunks per request merged by LSE",
+                           "split into chunks merged by LSE (the sink counted once)",
     "causal_prefill": "causal prefill: 2 x 8192 tokens (varlen), 64 q / 8 KV heads, head_dim 64",
     "chunked_prefill": "chunked prefill over the paged cache: 8 sequences, U[1024,8192] cached + U[256,2048] new "
                        "tokens each, 64 q / 8 KV heads, head_dim 64; one step = append the new K/V into the pages "
@@ -243,6 +243,218 @@ def timed_steps(step, K, warmup, flush, stream):
     return [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
 
+def graph_ms(step, n, reps, stream, flush=None):
+    """Per-call ms of n calls captured back to back in one CUDA graph and replayed `reps` times (the
+    host's launch overhead stripped).  With `flush`, every call is preceded by the L2 flush inside the
+    graph, and the time of a graph of n flushes alone is subtracted."""
+    def capture(body):
+        g = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(n):
+                body()
+        torch.cuda.synchronize()
+        return g
+
+    def per_call(g):
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            g.replay()
+            torch.cuda.synchronize()
+            t0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            t1.record(stream)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1) / (reps * n)
+
+    if flush is None:
+        return per_call(capture(step))
+
+    def both():
+        flush()
+        step()
+
+    return per_call(capture(both)) - per_call(capture(flush))
+
+
+class Staging:
+    """Tensors packed back to back (each at a 256-byte offset) in one pinned host buffer and one
+    device buffer, so that a step's inputs (or results) cross to the other side in one copy."""
+
+    def __init__(self, specs):
+        offs, off = [], 0
+        for shape, dtype in specs:
+            off = (off + 255) & ~255
+            offs.append(off)
+            off += math.prod(shape) * torch.empty(0, dtype=dtype).element_size()
+        self.nbytes = off
+        self.host = torch.empty(off, dtype=torch.uint8).pin_memory()
+        self.dev = torch.empty(off, dtype=torch.uint8, device="cuda")
+
+        def views(buf):
+            return [buf[o:o + math.prod(sh) * torch.empty(0, dtype=dt).element_size()].view(dt).view(sh)
+                    for o, (sh, dt) in zip(offs, specs)]
+
+        self.h, self.d = views(self.host), views(self.dev)
+
+    def to_device(self):
+        self.dev.copy_(self.host, non_blocking=True)
+
+    def to_host(self):
+        self.host.copy_(self.dev, non_blocking=True)
+
+
+def pipelined_ms(api, ins, outs, K, warmup, stream):
+    """Mean ms per step of a double-buffered loop through the public API: the inputs of step i go up
+    on one copy stream, step i runs on `stream`, its results come back on another copy stream; slot
+    i % 2 is reused only after step i - 2 has released it.  The K steps are captured in one CUDA
+    graph (the three streams fork from and join `stream`) and timed as one replay, from the first
+    upload to the last download, so the host's enqueue cost is not in the figure."""
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def loop(n):
+        up.wait_stream(stream)
+        down.wait_stream(stream)
+        ev_in = [torch.cuda.Event() for _ in range(n)]
+        ev_run = [torch.cuda.Event() for _ in range(n)]
+        ev_out = [torch.cuda.Event() for _ in range(n)]
+        for i in range(n):
+            slot = i % 2
+            with torch.cuda.stream(up):
+                if i >= 2:
+                    up.wait_event(ev_run[i - 2])  # step i - 2 has read this slot's inputs
+                ins[slot].to_device()
+                ev_in[i].record(up)
+            with torch.cuda.stream(stream):
+                stream.wait_event(ev_in[i])
+                if i >= 2:
+                    stream.wait_event(ev_out[i - 2])  # this slot's previous results are on the host
+                api(ins[slot].d, outs[slot].d)
+                ev_run[i].record(stream)
+            with torch.cuda.stream(down):
+                down.wait_event(ev_run[i])
+                outs[slot].to_host()
+                ev_out[i].record(down)
+        stream.wait_stream(up)
+        stream.wait_stream(down)
+
+    with torch.cuda.stream(stream):
+        loop(warmup)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        loop(K)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        g.replay()  # warm
+        torch.cuda.synchronize()
+        t0.record(stream)
+        g.replay()
+        t1.record(stream)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / K
+
+
+def graph_ms(step, n, reps, stream, flush=None):
+    """Per-call ms of n calls captured back to back in one CUDA graph and replayed `reps` times (the
+    host's launch overhead stripped).  With `flush`, every call is preceded by the L2 flush inside the
+    graph, and the time of a graph of n flushes alone is subtracted."""
+    def capture(body):
+        g = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(n):
+                body()
+        torch.cuda.synchronize()
+        return g
+
+    def per_call(g):
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            g.replay()
+            torch.cuda.synchronize()
+            t0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            t1.record(stream)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1) / (reps * n)
+
+    if flush is None:
+        return per_call(capture(step))
+
+    def both():
+        flush()
+        step()
+
+    return per_call(capture(both)) - per_call(capture(flush))
+
+
+class Staging:
+    """Tensors packed back to back (each at a 256-byte offset) in one pinned host buffer and one
+    device buffer, so that a step's inputs (or results) cross to the other side in one copy."""
+
+    def __init__(self, specs):
+        offs, off = [], 0
+        for shape, dtype in specs:
+            off = (off + 255) & ~255
+            offs.append(off)
+            off += math.prod(shape) * torch.empty(0, dtype=dtype).element_size()
+        self.nbytes = off
+        self.host = torch.empty(off, dtype=torch.uint8).pin_memory()
+        self.dev = torch.empty(off, dtype=torch.uint8, device="cuda")
+
+        def views(buf):
+            return [buf[o:o + math.prod(sh) * torch.empty(0, dtype=dt).element_size()].view(dt).view(sh)
+                    for o, (sh, dt) in zip(offs, specs)]
+
+        self.h, self.d = views(self.host), views(self.dev)
+
+    def to_device(self):
+        self.dev.copy_(self.host, non_blocking=True)
+
+    def to_host(self):
+        self.host.copy_(self.dev, non_blocking=True)
+
+
+def pipelined_ms(api, ins, outs, K, warmup, stream):
+    """Mean ms per step of a double-buffered loop through the public API: the inputs of step i go up
+    on one copy stream, step i runs on `stream`, its results come back on another copy stream;
+    slot i % 2 is reused only after step i - 2 has released it.  The K timed steps form one region
+    (from the first upload to the last download)."""
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    n = warmup + K
+    ev_in = [torch.cuda.Event() for _ in range(n)]
+    ev_run = [torch.cuda.Event() for _ in range(n)]
+    ev_out = [torch.cuda.Event() for _ in range(n)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(n):
+        if i == warmup:
+            torch.cuda.synchronize()
+            t0.record(up)
+        slot = i % 2
+        with torch.cuda.stream(up):
+            if i >= 2:
+                up.wait_event(ev_run[i - 2])  # step i - 2 has read this slot's inputs
+            ins[slot].to_device()
+            ev_in[i].record(up)
+        with torch.cuda.stream(stream):
+            stream.wait_event(ev_in[i])
+            if i >= 2:
+                stream.wait_event(ev_out[i - 2])  # this slot's previous results are on the host
+            api(ins[slot].d, outs[slot].d)
+            ev_run[i].record(stream)
+        with torch.cuda.stream(down):
+            down.wait_event(ev_run[i])
+            outs[slot].to_host()
+            ev_out[i].record(down)
+    t1.record(down)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / K
+
+
 # ----------------------------------------------------------------------------- workloads
 
 def decode_bytes(kv_lens, Hkv, D=64):
@@ -408,6 +620,19 @@ def oracle_request(inp, b, masks=None):
         rows = torch.tensor([[b, h] for h in range(Hq)], dtype=torch.int32).numpy()
         oracle.decode(*args, inp.sinks, inp.scale, rows=rows)
     return int(inp.kv_lens[b]) * Hkv * 64 * 4
+
+
+def one_thread(fn, fargs, budget_s=4.0):
+    """The same oracle baseline on one host thread (a shorter sample), for the per-core figure."""
+    import oracle
+
+    n = oracle.num_threads()
+    oracle.set_num_threads(1)
+    try:
+        r = fn(*fargs, budget_s=budget_s)
+    finally:
+        oracle.set_num_threads(n)
+    return {"value": r["value"], "unit": r["unit"], "cores": 1, "sample": r["sample"]}
 
 
 def cpu_baseline_decode(inp, masks=None, budget_s=12.0):
@@ -657,6 +882,9 @@ def run_ours(args):
                 "traffic": profiled_traffic(kname, name, KERNEL_SOURCES[kname])}
         launches = K  # one split kernel per step
         cfg_extra = {"kv_tokens": int(inp.kv_lens.sum()), "kv_bytes_per_step": nbytes}
+        if name == "long_context_decode":
+            cfg_extra["split"] = ("automatic: one share per resident CTA (the configuration's 32 chunks per "
+                                  "(request, KV head) are timed in the secondary lines)")
     elif name in ("chunked_prefill", "serving_step"):
         if name == "chunked_prefill":
             inp, step, times, flops = bench_chunked(S, W, rank, K, Wu, flush, stream)
@@ -716,144 +944,130 @@ def run_ours(args):
         torch.cuda.synchronize()
     t_load1 = time.time()
 
-    # ---- end to end through the public API: per-step inputs from pinned host memory, result read back
+    # ---- end to end through the public API: per-step inputs from pinned host memory, result read back.
+    # A step's inputs travel in one host-to-device copy and its results in one device-to-host copy
+    # (Staging), as a serving loop that stages each step's tensors in one buffer would do.
     e2e = None
-    if args.kernels_only:
-        pass
-    elif name == "chunked_prefill":
-        srcs = (inp.q, inp.k_new, inp.v_new, inp.cu_seqlens, inp.start_pos, inp.page_table)
-        h_in = [t.cpu().pin_memory() for t in srcs]
-        d_in = [torch.empty_like(t) for t in srcs]
-        h_out = torch.empty(inp.q.shape, dtype=torch.bfloat16).pin_memory()
-        h_lse = torch.empty(inp.q.shape[:2], dtype=torch.float32).pin_memory()
-        d_out = torch.empty_like(inp.q)
-        d_lse = torch.empty(inp.q.shape[:2], dtype=torch.float32, device="cuda")
+    if not args.kernels_only:
+        bf16, i32, f32 = torch.bfloat16, torch.int32, torch.float32
+        if name == "chunked_prefill":
+            srcs = (inp.q, inp.k_new, inp.v_new, inp.cu_seqlens, inp.start_pos, inp.page_table)
+            res = [(inp.q.shape, bf16), (inp.q.shape[:2], f32)]
+            metric_units, unit_scale, e_unit = total_flops, 1e12, "TFLOP/s"
+            note = ("the page pools stay resident (they are the cache); new tokens' q/k/v and the metadata come from "
+                    "pinned host memory every step and the output + lse are read back")
+
+            def api(d, o):
+                q, kn, vn, cu, sp, pt = d
+                S.sinkattn_kv_append(kn, vn, cu, sp, pt, inp.k_pages, inp.v_pages, stream=stream)
+                S.sinkattn_prefill_paged(q, inp.k_pages, inp.v_pages, pt, cu, sp, inp.sinks, inp.scale,
+                                         max_seqlen=inp.max_seqlen, out=o[0], lse=o[1], stream=stream)
+        elif name == "serving_step":
+            srcs = (qkv, inp.cu_seqlens, inp.start_pos, inp.page_table)
+            res = [(inp.q.shape, bf16), (inp.q.shape[:2], f32)]
+            metric_units, unit_scale, e_unit = total_flops, 1e12, "TFLOP/s"
+            note = ("the page pools and the QKV bias stay resident; the new tokens' fused QKV projection output and "
+                    "the metadata come from pinned host memory every step and the output + lse are read back")
+            d_q = torch.empty_like(inp.q)
+            Hq = inp.q.shape[1]
+
+            def api(d, o):
+                x, cu, sp, pt = d
+                S.sinkattn_qkv_prologue(x, bias, cu, sp, pt, inp.k_pages, inp.v_pages, Hq, q_out=d_q, stream=stream,
+                                        **YARN_GPT_OSS)
+                S.sinkattn_prefill_paged(d_q, inp.k_pages, inp.v_pages, pt, cu, sp, inp.sinks, inp.scale,
+                                         max_seqlen=inp.max_seqlen, out=o[0], lse=o[1], stream=stream)
+        elif name == "causal_prefill":
+            srcs = (inp.q, inp.k, inp.v, inp.cu_seqlens)
+            res = [(inp.q.shape, bf16), (inp.q.shape[:2], f32)]
+            metric_units, unit_scale, e_unit = total_flops, 1e12, "TFLOP/s"
+            note = "q, k, v and cu_seqlens come from pinned host memory every step and the output + lse are read back"
+
+            def api(d, o):
+                S.sinkattn_prefill(d[0], d[1], d[2], d[3], inp.sinks, inp.scale, True, max_seqlen=inp.max_seqlen,
+                                   out=o[0], lse=o[1], stream=stream)
+        else:
+            srcs = (inp.q, inp.page_table, inp.kv_lens) + ((masks,) if masks is not None else ())
+            res = [(inp.q.shape, bf16), (inp.q.shape[:-1], f32)]
+            metric_units, unit_scale, e_unit = total_bytes, 1e9, "GB/s"
+            note = ("KV pool stays resident in HBM (it is the cache); q, page table and lengths"
+                    + (" and the tree masks" if masks is not None else "")
+                    + " come from pinned host memory every step and the output + lse are read back")
+            verify = name in ("speculative_verify", "tree_verify")
+            ws_size = S.sinkattn_verify_workspace_size if verify else S.sinkattn_decode_workspace_size
+            ws = torch.empty(ws_size(inp.q, inp.k_pages, inp.page_table), dtype=torch.uint8, device="cuda")
+
+            def api(d, o):
+                kw = dict(out=o[0], lse=o[1], workspace=ws, stream=stream)
+                if masks is not None:
+                    S.sinkattn_verify_tree(d[0], inp.k_pages, inp.v_pages, d[1], d[2], d[3], inp.sinks, inp.scale, **kw)
+                elif verify:
+                    S.sinkattn_verify(d[0], inp.k_pages, inp.v_pages, d[1], d[2], inp.sinks, inp.scale, **kw)
+                else:
+                    S.sinkattn_decode(d[0], inp.k_pages, inp.v_pages, d[1], d[2], inp.sinks, inp.scale, **kw)
+
+        ins = [Staging([(t.shape, t.dtype) for t in srcs]) for _ in range(2)]
+        for slot in ins:
+            for h, t in zip(slot.h, srcs):
+                h.copy_(t)
+        outs = [Staging(res) for _ in range(2)]
 
         def e2e_step():
-            for h, d in zip(h_in, d_in):
-                d.copy_(h, non_blocking=True)
-            q, kn, vn, cu, sp, pt = d_in
-            S.sinkattn_kv_append(kn, vn, cu, sp, pt, inp.k_pages, inp.v_pages, stream=stream)
-            S.sinkattn_prefill_paged(q, inp.k_pages, inp.v_pages, pt, cu, sp, inp.sinks, inp.scale,
-                                     max_seqlen=inp.max_seqlen, out=d_out, lse=d_lse, stream=stream)
-            h_out.copy_(d_out, non_blocking=True)
-            h_lse.copy_(d_lse, non_blocking=True)
+            ins[0].to_device()
+            api(ins[0].d, outs[0].d)
+            outs[0].to_host()
 
         with torch.cuda.stream(stream):
             et = timed_steps(e2e_step, K, Wu, flush, stream)
         e_ms = max_over_ranks(statistics.mean(et), world)
-        e2e = {"value": total_flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e_ms,
-               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in h_in),
-               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in (h_out, h_lse)),
-               "note": "the page pools stay resident (they are the cache); new tokens' q/k/v and the metadata "
-                       "come from pinned host memory every step and the output + lse are read back"}
-    elif name == "serving_step":
-        srcs = (qkv, inp.cu_seqlens, inp.start_pos, inp.page_table)
-        h_in = [t.cpu().pin_memory() for t in srcs]
-        d_in = [torch.empty_like(t) for t in srcs]
-        h_out = torch.empty(inp.q.shape, dtype=torch.bfloat16).pin_memory()
-        h_lse = torch.empty(inp.q.shape[:2], dtype=torch.float32).pin_memory()
-        d_q, d_out = torch.empty_like(inp.q), torch.empty_like(inp.q)
-        d_lse = torch.empty(inp.q.shape[:2], dtype=torch.float32, device="cuda")
-        Hq = inp.q.shape[1]
-
-        def e2e_step():
-            for h, d in zip(h_in, d_in):
-                d.copy_(h, non_blocking=True)
-            x, cu, sp, pt = d_in
-            S.sinkattn_qkv_prologue(x, bias, cu, sp, pt, inp.k_pages, inp.v_pages, Hq, q_out=d_q, stream=stream,
-                                    **YARN_GPT_OSS)
-            S.sinkattn_prefill_paged(d_q, inp.k_pages, inp.v_pages, pt, cu, sp, inp.sinks, inp.scale,
-                                     max_seqlen=inp.max_seqlen, out=d_out, lse=d_lse, stream=stream)
-            h_out.copy_(d_out, non_blocking=True)
-            h_lse.copy_(d_lse, non_blocking=True)
-
-        with torch.cuda.stream(stream):
-            et = timed_steps(e2e_step, K, Wu, flush, stream)
-        e_ms = max_over_ranks(statistics.mean(et), world)
-        e2e = {"value": total_flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e_ms,
-               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in h_in),
-               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in (h_out, h_lse)),
-               "note": "the page pools and the QKV bias stay resident; the new tokens' fused QKV projection "
-                       "output and the metadata come from pinned host memory every step and the output + lse "
-                       "are read back"}
-    elif name == "causal_prefill":
-        h_in = [t.cpu().pin_memory() for t in (inp.q, inp.k, inp.v, inp.cu_seqlens)]
-        d_in = [torch.empty_like(t) for t in (inp.q, inp.k, inp.v, inp.cu_seqlens)]
-        h_out = torch.empty(inp.q.shape, dtype=torch.bfloat16).pin_memory()
-        h_lse = torch.empty(inp.q.shape[:2], dtype=torch.float32).pin_memory()
-        d_out = torch.empty_like(inp.q)
-        d_lse = torch.empty(inp.q.shape[:2], dtype=torch.float32, device="cuda")
-
-        def e2e_step():
-            for h, d in zip(h_in, d_in):
-                d.copy_(h, non_blocking=True)
-            S.sinkattn_prefill(d_in[0], d_in[1], d_in[2], d_in[3], inp.sinks, inp.scale, True,
-                               max_seqlen=inp.max_seqlen, out=d_out, lse=d_lse, stream=stream)
-            h_out.copy_(d_out, non_blocking=True)
-            h_lse.copy_(d_lse, non_blocking=True)
-
-        with torch.cuda.stream(stream):
-            et = timed_steps(e2e_step, K, Wu, flush, stream)
-        e_ms = max_over_ranks(statistics.mean(et), world)
-        e2e = {"value": total_flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e_ms,
-               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in h_in),
-               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in (h_out, h_lse))}
-    else:
-        h_q = inp.q.cpu().pin_memory()
-        h_pt = inp.page_table.cpu().pin_memory()
-        h_kl = inp.kv_lens.cpu().pin_memory()
-        h_out = torch.empty(inp.q.shape, dtype=torch.bfloat16).pin_memory()
-        h_lse = torch.empty(inp.q.shape[:-1], dtype=torch.float32).pin_memory()
-        d_q, d_pt, d_kl = torch.empty_like(inp.q), torch.empty_like(inp.page_table), torch.empty_like(inp.kv_lens)
-        verify = name in ("speculative_verify", "tree_verify")
-        ws_size = S.sinkattn_verify_workspace_size if verify else S.sinkattn_decode_workspace_size
-        api = S.sinkattn_verify if verify else S.sinkattn_decode
-        h_extra = []
-        if masks is not None:  # draft trees: the masks are per-step input too
-            h_m = torch.as_tensor(masks, dtype=torch.int64).pin_memory()
-            d_m = torch.empty_like(h_m, device="cuda")
-            h_extra = [h_m]
-
-            def api(q, kp, vp, pt, kl, sinks, scale, **kw):
-                d_m.copy_(h_m, non_blocking=True)
-                return S.sinkattn_verify_tree(q, kp, vp, pt, kl, d_m, sinks, scale, **kw)
-        ws = torch.empty(ws_size(inp.q, inp.k_pages, inp.page_table), dtype=torch.uint8, device="cuda")
-        d_out = torch.empty_like(inp.q)
-        d_lse = torch.empty(inp.q.shape[:-1], dtype=torch.float32, device="cuda")
-
-        def e2e_step():
-            d_q.copy_(h_q, non_blocking=True)
-            d_pt.copy_(h_pt, non_blocking=True)
-            d_kl.copy_(h_kl, non_blocking=True)
-            api(d_q, inp.k_pages, inp.v_pages, d_pt, d_kl, inp.sinks, inp.scale, out=d_out, lse=d_lse, workspace=ws,
-                stream=stream)
-            h_out.copy_(d_out, non_blocking=True)
-            h_lse.copy_(d_lse, non_blocking=True)
-
-        with torch.cuda.stream(stream):
-            et = timed_steps(e2e_step, K, Wu, flush, stream)
-        e_ms = max_over_ranks(statistics.mean(et), world)
-        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_pt, h_kl, *h_extra))
-        d2h = sum(t.numel() * t.element_size() for t in (h_out, h_lse))
-        e2e = {"value": total_bytes / (e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e_ms,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "note": "KV pool stays resident in HBM (it is the cache); q, page table and lengths come from "
-                       "pinned host memory every step and the output + lse are read back"}
+        try:
+            p_ms, p_err = pipelined_ms(api, ins, outs, K, Wu, stream), None
+        except Exception as exc:  # report, never hide (every rank still joins the reduction below)
+            p_ms, p_err = float("nan"), f"{type(exc).__name__}: {exc}"
+        p_ms = max_over_ranks(p_ms, world)
+        e2e = {"value": metric_units / (e_ms * 1e-3) / unit_scale, "unit": e_unit, "ms_per_step": e_ms,
+               "h2d_bytes_per_step": ins[0].nbytes, "d2h_bytes_per_step": outs[0].nbytes,
+               "copies_per_step": {"h2d": 1, "d2h": 1}, "note": note,
+               "pipelined": {"value": metric_units / (p_ms * 1e-3) / unit_scale, "unit": e_unit, "ms_per_step": p_ms,
+                             "mode": "double-buffered serving loop captured in one CUDA graph, no L2 flush: step "
+                                     "i+1's inputs copy in and step i-1's results copy out on their own streams "
+                                     "while step i computes; K steps timed as one replay",
+                             **({"error": p_err} if p_err else {})}}
 
     # ---- secondary workloads (rank 0 reports its own numbers)
     secondary = []
     if not args.no_secondary:
         Ks = max(3, min(K, 20))
         try:
-            li, _, lt, lb = bench_decode(S, W, "long_context_decode", rank, Ks, Wu, flush, stream,
-                                         num_workers=4 * 8 * W.LONG_CONTEXT_CHUNKS)
-            lms = statistics.mean(lt)
-            secondary.append({"workload": WORKLOAD_TEXT["long_context_decode"], "value": lb / (lms * 1e-3) / 1e9,
-                              "unit": "GB/s", "ms_per_step": lms, "frac_of_hbm_peak": lb / (lms * 1e-3) / 1e9 / hbm_peak,
-                              "traffic": profiled_traffic("decode_split_kernel", "long_context_decode",
-                                                          KERNEL_SOURCES["decode_split_kernel"])})
-            del li
+            for split, workers in (("the configuration's 32 chunks per (request, KV head): 1024 shares, 1.7 waves "
+                                    "of resident CTAs", 4 * 8 * W.LONG_CONTEXT_CHUNKS),
+                                   ("automatic: one share per resident CTA, ~19 pieces per (request, KV head)", 0)):
+                li, _, lt, lb = bench_decode(S, W, "long_context_decode", rank, Ks, Wu, flush, stream,
+                                             num_workers=workers)
+                lms = statistics.mean(lt)
+                secondary.append({"workload": WORKLOAD_TEXT["long_context_decode"], "split": split,
+                                  "value": lb / (lms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": lms,
+                                  "frac_of_hbm_peak": lb / (lms * 1e-3) / 1e9 / hbm_peak,
+                                  "traffic": profiled_traffic("decode_split_kernel", "long_context_decode",
+                                                              KERNEL_SOURCES["decode_split_kernel"])})
+                del li
+            # the two decode configurations also replayed from a CUDA graph (launch overhead stripped)
+            gi, gstep, gt, gb = bench_decode(S, W, "tiny_decode", rank, Ks, Wu, flush, stream)
+            g_ms = graph_ms(gstep, 100, 5, stream)
+            tms = statistics.mean(gt)
+            secondary.append({"workload": WORKLOAD_TEXT["tiny_decode"], "value": gb / (tms * 1e-3) / 1e9,
+                              "unit": "GB/s", "ms_per_step": tms, "us_per_call": tms * 1e3,
+                              "graph": {"us_per_call": g_ms * 1e3, "value": gb / (g_ms * 1e-3) / 1e9, "unit": "GB/s",
+                                        "method": "100 calls back to back in one CUDA graph, replayed 5 times "
+                                                  "(32 KB of K/V: no flush)"}})
+            del gi
+            bi, bstep, _, bb = bench_decode(S, W, "batched_paged_decode", rank, 3, Wu, flush, stream)
+            b_ms = graph_ms(bstep, 20, 5, stream, flush=flush)
+            secondary.append({"workload": WORKLOAD_TEXT["batched_paged_decode"], "value": bb / (b_ms * 1e-3) / 1e9,
+                              "unit": "GB/s", "ms_per_step": b_ms, "frac_of_hbm_peak": bb / (b_ms * 1e-3) / 1e9 / hbm_peak,
+                              "graph": {"method": "20 x (L2 flush, call) in one CUDA graph, replayed 5 times, minus a "
+                                                  "graph of the 20 flushes alone"}})
+            del bi
             vi, _, vt, vb = bench_verify(S, W, rank, Ks, Wu, flush, stream)
             vms = statistics.mean(vt)
             secondary.append({"workload": WORKLOAD_TEXT["speculative_verify"], "value": vb / (vms * 1e-3) / 1e9,
@@ -894,9 +1108,12 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = (cpu_baseline_decode(inp, masks) if unit == "GB/s" else
-               cpu_baseline_chunked(inp) if name == "chunked_prefill" else
-               cpu_baseline_serving(inp, qkv, bias) if name == "serving_step" else cpu_baseline_prefill(inp))
+        fn, fargs = ((cpu_baseline_decode, (inp, masks)) if unit == "GB/s" else
+                     (cpu_baseline_chunked, (inp,)) if name == "chunked_prefill" else
+                     (cpu_baseline_serving, (inp, qkv, bias)) if name == "serving_step" else
+                     (cpu_baseline_prefill, (inp,)))
+        cpu = fn(*fargs)
+        cpu["one_thread"] = one_thread(fn, fargs)
 
     clocks = None
     if sampler:

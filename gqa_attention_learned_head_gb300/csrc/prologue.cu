@@ -13,10 +13,11 @@
 // sequence, position and page; lane d turns position x frequency of pair d
 // into a rotation (angle taken in double and reduced to [-pi, pi] before a
 // single-precision sincos, so that positions of 10^5 and beyond keep full
-// accuracy) and the lanes share them by shuffles; then four lanes take a head (its 32 pairs), each lane eight
-// rotated pairs in two 16-byte pieces (pairs (d, d + 32): elements 8l..8l+7 and
-// 8l+32..8l+39; pairs (2d, 2d + 1): elements 16l..16l+15), eight heads per pass
-// of the warp.
+// accuracy) and the lanes share them by shuffles; then four lanes take a head
+// (its 32 pairs), each lane eight rotated pairs in two 16-byte pieces (pairs
+// (d, d + 32): elements 8l..8l+7 and 8l+32..8l+39; pairs (2d, 2d + 1):
+// elements 16l..16l+15), eight heads at a time across the warp, and each lane
+// loads several of its heads before it uses any.
 #include "args_paged.h"
 #include "ptx.cuh"
 
@@ -84,11 +85,8 @@ __global__ void __launch_bounds__(kWarps * 32) qkv_prologue_kernel(const Prologu
     const int heads = a.Hq + 2 * a.Hkv;
     // element offsets of this lane's two 16-byte pieces
     const int o0 = a.interleaved ? 16 * l : 8 * l, o1 = a.interleaved ? 16 * l + 8 : 8 * l + kHeadDim / 2;
-    for (int hd = lane >> 2; hd < heads; hd += 8) {
-        const uint4* src = reinterpret_cast<const uint4*>(a.qkv + ((long long)t * heads + hd) * kHeadDim);
-        float u[8], w[8];
-        unpack8(__ldg(src + o0 / 8), u);
-        unpack8(__ldg(src + o1 / 8), w);
+    // one head's 16 elements of this lane: bias, rotation (q and k), store
+    auto finish = [&](int hd, float (&u)[8], float (&w)[8]) {
         if (a.bias) {
             const uint4* bs = reinterpret_cast<const uint4*>(a.bias + hd * kHeadDim);
             float bu[8], bw[8];
@@ -115,7 +113,7 @@ __global__ void __launch_bounds__(kWarps * 32) qkv_prologue_kernel(const Prologu
         if (hd < a.Hq) {
             dst = reinterpret_cast<uint4*>(a.q_out + ((long long)t * a.Hq + hd) * kHeadDim);
         } else {
-            if (page < 0) continue;
+            if (page < 0) return;
             const bool is_k = hd < a.Hq + a.Hkv;
             const int g = hd - a.Hq - (is_k ? 0 : a.Hkv);
             dst = reinterpret_cast<uint4*>((is_k ? a.k_pages : a.v_pages) +
@@ -123,6 +121,27 @@ __global__ void __launch_bounds__(kWarps * 32) qkv_prologue_kernel(const Prologu
         }
         dst[o0 / 8] = pack8(u);
         dst[o1 / 8] = pack8(w);
+    };
+    const uint4* row = reinterpret_cast<const uint4*>(a.qkv + (long long)t * heads * kHeadDim);
+    int hd = lane >> 2;
+    // this lane's heads are lane / 4 + 8j, taken two per pass with all four 16-byte loads issued
+    // before either head is used (one head in flight leaves the warp waiting on DRAM latency)
+    for (; hd + 8 < heads; hd += 16) {
+        const uint4 x0 = __ldg(row + hd * 8 + o0 / 8), x1 = __ldg(row + hd * 8 + o1 / 8);
+        const uint4 y0 = __ldg(row + (hd + 8) * 8 + o0 / 8), y1 = __ldg(row + (hd + 8) * 8 + o1 / 8);
+        float u[8], w[8];
+        unpack8(x0, u);
+        unpack8(x1, w);
+        finish(hd, u, w);
+        unpack8(y0, u);
+        unpack8(y1, w);
+        finish(hd + 8, u, w);
+    }
+    if (hd < heads) {
+        float u[8], w[8];
+        unpack8(__ldg(row + hd * 8 + o0 / 8), u);
+        unpack8(__ldg(row + hd * 8 + o1 / 8), w);
+        finish(hd, u, w);
     }
 }
 

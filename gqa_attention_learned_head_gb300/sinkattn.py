@@ -92,7 +92,7 @@ def _load():
     lib.sinkattn_status_string.restype = ctypes.c_char_p
     lib.sinkattn_version.restype = i32
     for fn in ("sinkattn_decode", "sinkattn_prefill", "sinkattn_merge", "sinkattn_get_error", "sinkattn_verify",
-               "sinkattn_kv_append", "sinkattn_prefill_paged", "sinkattn_verify_tree", "sinkattn_qkv_prologue", "sinkattn_qkv_prologue"):
+               "sinkattn_kv_append", "sinkattn_prefill_paged", "sinkattn_verify_tree", "sinkattn_qkv_prologue"):
         getattr(lib, fn).restype = ctypes.c_int
     return lib
 

@@ -225,9 +225,9 @@ def make_prefill(Hq, Hkv, seqlens, seed=0, causal=True, device="cpu", D=HEAD_DIM
 
 # ---- the named benchmark workloads -------------------------------------------------
 
-def tiny_decode(device="cpu"):
+def tiny_decode(device="cpu", seed=0):
     """Batch 1, 4 query heads on 1 KV head, kv_len 128, contiguous pages, seed 0."""
-    return make_decode(1, 4, 1, [128], seed=0, contiguous=True, device=device)
+    return make_decode(1, 4, 1, [128], seed=seed, contiguous=True, device=device)
 
 
 def batched_paged_decode(device="cpu", seed=0):

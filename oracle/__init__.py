@@ -59,6 +59,8 @@ def _load():
         for fn in ("oracle_decode", "oracle_prefill", "oracle_decode_partials", "oracle_merge", "oracle_verify", "oracle_prefill_paged", "oracle_verify_tree",
                    "oracle_num_threads"):
             getattr(_lib, fn).restype = ctypes.c_int
+        _lib.oracle_set_num_threads.argtypes = [i]
+        _lib.oracle_set_num_threads.restype = None
     return _lib
 
 
@@ -93,6 +95,11 @@ def _check(rc: int, what: str):
 
 def num_threads() -> int:
     return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads the oracle's later calls use (OpenMP); returns with the count changed for the process."""
+    _load().oracle_set_num_threads(int(n))
 
 
 def decode(q, k_pages, v_pages, page_table, kv_lens, sinks, scale, rows=None):

@@ -489,3 +489,13 @@ int oracle_num_threads(void) {
     return 1;
 #endif
 }
+
+/* Sets the number of threads later calls use (n >= 1; ignored without OpenMP). */
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+    extern void omp_set_num_threads(int);
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
