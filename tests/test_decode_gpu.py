@@ -141,3 +141,16 @@ def test_empty_batch(S):
     out, lse = S.sinkattn_decode(q, inp.k_pages, inp.v_pages, inp.page_table[:0], inp.kv_lens[:0], inp.sinks,
                                  inp.scale)
     assert out.shape == (0, 8, 64) and S.sinkattn_get_error() == 0
+
+
+def test_one_million_token_request(S):
+    """Maximum-size case: a 2^20-token request (65536 pages, 2 GiB of K/V) beside a 5-token one; every
+    head of both requests against the oracle (inputs drawn on the device, copied to the host)."""
+    g = W.make_decode(2, 64, 8, [1 << 20, 5], seed=77, device="cuda")
+    out, lse = S.sinkattn_decode(g.q, g.k_pages, g.v_pages, g.page_table, g.kv_lens, g.sinks, g.scale)
+    assert S.sinkattn_get_error() == 0
+    out, lse = out.float().cpu().numpy(), lse.cpu().numpy()
+    c = g.to("cpu")
+    del g
+    ro, rl = ref(c)
+    assert_parity(out, lse, ro, rl, "2^20-token request")

@@ -91,3 +91,15 @@ def test_too_long_sequence_is_reported(S):
     inp = W.make_prefill(4, 1, [100, 40], seed=4)
     out, lse, err = run(S, inp, max_seqlen=64)
     assert err == S.ERR_BAD_LENGTH
+
+
+def test_long_single_sequence_sampled(S):
+    """A 65536-token causal sequence (512 query tiles) next to a 3-token one; sampled rows include the
+    last rows, which see every key."""
+    inp = W.make_prefill(16, 2, [65536, 3], seed=21)
+    out, lse, err = run(S, inp)
+    assert err == 0
+    rows = sampled_rows(inp, 64, 2)
+    rows = np.concatenate([rows, np.array([[65535, h] for h in range(16)], dtype=np.int32)])
+    ro, rl = ref(inp, rows)
+    assert_parity(out[rows[:, 0], rows[:, 1]], lse[rows[:, 0], rows[:, 1]], ro, rl, "65536-token sequence")
