@@ -81,9 +81,14 @@ def peaks():
 KERNEL_SOURCES = {
     "decode_split_kernel": ["decode.cu", "ptx.cuh", "split_kv.cuh", "args_decode.h", "args_common.h"],
     "verify_split_kernel": ["verify.cu", "ptx.cuh", "split_kv.cuh", "args_verify.h", "args_common.h"],
-    "prefill_pp_kernel": ["prefill_pp.cu", "ptx.cuh", "tile_order.cuh", "args_prefill.h", "args_common.h"],
-    "prefill_tc_kernel": ["prefill_tc.cu", "ptx.cuh", "tile_order.cuh", "args_prefill.h", "args_common.h"],
-    "prefill_tc_kernel_paged": ["prefill_tc.cu", "ptx.cuh", "tile_order.cuh", "args_prefill.h", "args_common.h"],
+    "verify_tc_kernel": ["verify_tc.cu", "verify.cu", "ptx.cuh", "split_kv.cuh", "tc_tile.cuh", "args_verify.h",
+                         "args_common.h"],
+    "prefill_pp_kernel": ["prefill_pp.cu", "ptx.cuh", "tc_tile.cuh", "tile_order.cuh", "args_prefill.h",
+                          "args_common.h"],
+    "prefill_tc_kernel": ["prefill_tc.cu", "ptx.cuh", "tc_tile.cuh", "tile_order.cuh", "args_prefill.h",
+                          "args_common.h"],
+    "prefill_tc_kernel_paged": ["prefill_tc.cu", "ptx.cuh", "tc_tile.cuh", "tile_order.cuh", "args_prefill.h",
+                                "args_common.h"],
     "qkv_prologue_kernel": ["prologue.cu", "ptx.cuh", "args_paged.h", "args_common.h"],
 }
 
@@ -873,8 +878,8 @@ def run_ours(args):
         value = total_bytes / (ms_max * 1e-3) / 1e9
         unit = "GB/s"
         achieved = nbytes / (ms * 1e-3) / 1e9
-        kname, call = {"speculative_verify": ("verify_split_kernel", "sinkattn_verify"),
-                       "tree_verify": ("verify_split_kernel", "sinkattn_verify_tree")}.get(
+        kname, call = {"speculative_verify": ("verify_tc_kernel", "sinkattn_verify"),
+                       "tree_verify": ("verify_tc_kernel", "sinkattn_verify_tree")}.get(
                            name, ("decode_split_kernel", "sinkattn_decode"))
         roof = {"bound": "hbm", "kernel": f"{kname} (the only kernel of a {call} call)",
                 "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
@@ -1072,15 +1077,15 @@ def run_ours(args):
             vms = statistics.mean(vt)
             secondary.append({"workload": WORKLOAD_TEXT["speculative_verify"], "value": vb / (vms * 1e-3) / 1e9,
                               "unit": "GB/s", "ms_per_step": vms, "frac_of_hbm_peak": vb / (vms * 1e-3) / 1e9 / hbm_peak,
-                              "traffic": profiled_traffic("verify_split_kernel", "speculative_verify",
-                                                          KERNEL_SOURCES["verify_split_kernel"])})
+                              "traffic": profiled_traffic("verify_tc_kernel", "speculative_verify",
+                                                          KERNEL_SOURCES["verify_tc_kernel"])})
             del vi
             ti, _, tt, tb, _ = bench_tree_verify(S, W, rank, Ks, Wu, flush, stream)
             tms = statistics.mean(tt)
             secondary.append({"workload": WORKLOAD_TEXT["tree_verify"], "value": tb / (tms * 1e-3) / 1e9,
                               "unit": "GB/s", "ms_per_step": tms, "frac_of_hbm_peak": tb / (tms * 1e-3) / 1e9 / hbm_peak,
-                              "traffic": profiled_traffic("verify_split_kernel", "tree_verify",
-                                                          KERNEL_SOURCES["verify_split_kernel"])})
+                              "traffic": profiled_traffic("verify_tc_kernel", "tree_verify",
+                                                          KERNEL_SOURCES["verify_tc_kernel"])})
             del ti
             pi, _, pt_, pf = bench_prefill(S, W, "causal_prefill", rank, Ks, Wu, flush, stream)
             pms = statistics.mean(pt_)

@@ -88,6 +88,28 @@ PrefillKernel prefill_kernel_choice() {
     return choice;
 }
 
+// Which verification kernel runs: SINKATTN_VERIFY_KERNEL=tc the tcgen05 kernel, =mma the mma.sync
+// kernel, unset the library's choice (by query rows per KV head).  Read at every call.
+int verify_kernel_choice() {
+    const char* s = std::getenv("SINKATTN_VERIFY_KERNEL");
+    if (s && std::strcmp(s, "tc") == 0) return 1;
+    if (s && std::strcmp(s, "mma") == 0) return 0;
+    return -1;
+}
+
+// 3-D bf16 tensor map over q [tokens, H, 64] whose box is 64 x box_heads heads x box_tokens tokens
+// (the rows of one query-head group of several consecutive tokens), 128-byte swizzle.
+bool encode_token_groups(CUtensorMap* map, const void* base, long long tokens, int H, unsigned box_heads,
+                         unsigned box_tokens) {
+    cuuint64_t dims[3] = {64, (cuuint64_t)H, (cuuint64_t)tokens};
+    cuuint64_t strides[2] = {128, (cuuint64_t)H * 128};
+    cuuint32_t box[3] = {64, box_heads, box_tokens};
+    cuuint32_t estride[3] = {1, 1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estride,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2-D bf16 tensor map over rows of 64 elements (128 B), box = box_rows x 64, 128-byte swizzle.
 bool encode_rows(CUtensorMap* map, const void* base, unsigned long long rows, unsigned long long row_stride_bytes,
                  unsigned box_rows) {
@@ -241,8 +263,8 @@ sinkattn_status_t sinkattn_decode(const void* q, const void* k_pages, const void
 size_t sinkattn_verify_workspace_size(const sinkattn_verify_dims_t* dims) {
     if (check_verify_dims(dims) != SINKATTN_OK) return 0;
     VerifyPlan plan;
-    if (verify_plan(dims->batch, dims->q_len, dims->num_q_heads, dims->num_kv_heads, dims->num_workers, &plan) !=
-        cudaSuccess)
+    if (verify_plan(dims->batch, dims->q_len, dims->num_q_heads, dims->num_kv_heads, dims->num_workers, -1,
+                    &plan) != cudaSuccess)
         return 0;
     return plan.ws_bytes;
 }
@@ -293,9 +315,12 @@ sinkattn_status_t verify_common(const void* q, const void* k_pages, const void* 
     if (!(scale == scale)) return SINKATTN_ERR_INVALID_ARG;
     DeviceState* ds = nullptr;
     if ((st = device_state(&ds)) != SINKATTN_OK) return st;
+    // The tcgen05 kernel fetches absent pages as zero-filled copies, which need a real tensor map:
+    // with an empty pool the mma.sync kernel runs (it issues no copy for an absent page).
+    const int choice = dims->num_pages == 0 ? 0 : verify_kernel_choice();
     VerifyPlan plan;
-    if (verify_plan(dims->batch, dims->q_len, dims->num_q_heads, dims->num_kv_heads, dims->num_workers, &plan) !=
-        cudaSuccess)
+    if (verify_plan(dims->batch, dims->q_len, dims->num_q_heads, dims->num_kv_heads, dims->num_workers, choice,
+                    &plan) != cudaSuccess)
         return SINKATTN_ERR_CUDA;
     if (!workspace || workspace_bytes < plan.ws_bytes || !aligned(workspace, 256)) return SINKATTN_ERR_WORKSPACE;
 
@@ -335,9 +360,20 @@ sinkattn_status_t verify_common(const void* q, const void* k_pages, const void* 
     a.workers = plan.grid;
     a.min_pages_per_worker = 0;  // set by the launcher
     a.fixed_workers = dims->num_workers > 0 ? 1 : 0;
+    a.tc_target = plan.tc_target;
+    a.tc_grid = plan.tc_grid;
     a.scale_log2 = scale * 1.4426950408889634f;
-    return verify_launch(a, plan, tk, tv, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SINKATTN_OK
-                                                                                            : SINKATTN_ERR_CUDA;
+    cudaError_t e;
+    if (plan.tc) {
+        CUtensorMap tq;
+        if (!encode_token_groups(&tq, q, (long long)dims->batch * dims->q_len, dims->num_q_heads, (unsigned)G,
+                                 (unsigned)dims->q_len))
+            return SINKATTN_ERR_INVALID_ARG;
+        e = verify_tc_launch(a, tq, tk, tv, static_cast<cudaStream_t>(stream));
+    } else {
+        e = verify_launch(a, plan, tk, tv, static_cast<cudaStream_t>(stream));
+    }
+    return e == cudaSuccess ? SINKATTN_OK : SINKATTN_ERR_CUDA;
 }
 }  // namespace
 }  // namespace sinkattn

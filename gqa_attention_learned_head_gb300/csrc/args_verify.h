@@ -21,15 +21,26 @@ struct VerifyArgs {
     unsigned long long epoch;      // this call's epoch, in [1, 2^40)
     unsigned* err;
     int B, QL, Hq, Hkv, G, R, num_pages, max_pages;  // R = QL * G rows per segment
-    int workers, min_pages_per_worker, fixed_workers;
+    int workers, min_pages_per_worker, fixed_workers;  // the mma.sync kernel's split
+    // the tcgen05 kernel's split: request b gets chunks in proportion to its 128-key tiles, about
+    // tc_target over all tiles; CTA x of tc_grid (>= every chunk) finds its chunk on the device
+    long long tc_target, tc_grid;
     float scale_log2;
 };
 struct VerifyPlan {
-    int grid, warps, stages;
-    size_t smem, slots, counters_offset, ws_bytes;
+    bool tc;  // the tcgen05 kernel runs (else the mma.sync kernel)
+    int grid, warps, stages;  // mma.sync kernel
+    long long tc_target, tc_grid;  // tcgen05 kernel
+    size_t smem, slots, counters_offset, ws_bytes;  // workspace: enough for either kernel
 };
-cudaError_t verify_plan(int B, int QL, int Hq, int Hkv, int num_workers, VerifyPlan* plan);
+// use_tc: -1 = the library's choice, 0 = the mma.sync kernel, 1 = the tcgen05 kernel
+cudaError_t verify_plan(int B, int QL, int Hq, int Hkv, int num_workers, int use_tc, VerifyPlan* plan);
 cudaError_t verify_launch(const VerifyArgs& args, const VerifyPlan& plan, const CUtensorMap& tmap_k,
                           const CUtensorMap& tmap_v, cudaStream_t stream);
+// tcgen05 kernel (verify_tc.cu); tmap_q covers q as [B * q_len tokens, Hq, 64] with a box of
+// 64 x G heads x q_len tokens.
+cudaError_t verify_tc_occupancy(int* per_sm);
+cudaError_t verify_tc_launch(const VerifyArgs& args, const CUtensorMap& tmap_q, const CUtensorMap& tmap_k,
+                             const CUtensorMap& tmap_v, cudaStream_t stream);
 
 }  // namespace sinkattn

@@ -47,6 +47,10 @@ constexpr int kMinPages = 32;  // automatic mode: never cut shares finer than th
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kNegInf = -__builtin_huge_valf();
+// The library's choice between the two kernels: the tcgen05 kernel from this many query rows per
+// (request, KV head) on, and its chunking target in CTAs per resident slot.
+constexpr int kTcMinRows = 16;
+constexpr int kTcWaves = 1;
 
 // Shared memory: ring | full / empty barriers | bad-page flags | misc | pend | queue | prefix[B+1].
 struct Layout {
@@ -572,8 +576,9 @@ cudaError_t resident(int W, size_t smem, long long* ctas) {
 
 }  // namespace
 
-cudaError_t verify_plan(int B, int QL, int Hq, int Hkv, int num_workers, VerifyPlan* plan) {
+cudaError_t verify_plan(int B, int QL, int Hq, int Hkv, int num_workers, int use_tc, VerifyPlan* plan) {
     const int G = Hq / Hkv, R = QL * G;
+    // mma.sync kernel: one share per resident CTA (or num_workers shares)
     const int W = warps_for(R);
     const int S = 3 * W + 1;
     const size_t smem = Layout(S, B).total;
@@ -585,11 +590,25 @@ cudaError_t verify_plan(int B, int QL, int Hq, int Hkv, int num_workers, VerifyP
     plan->warps = W;
     plan->stages = S;
     plan->smem = smem;
-    plan->slots = (size_t)shares + (size_t)B * Hkv;
+    // tcgen05 kernel: chunks of whole 128-key tiles, planned on the device in proportion to each
+    // request's tiles, about kTcWaves CTAs per resident slot in all (num_workers > 0: that many);
+    // the grid covers every chunk (at most the target plus one per segment)
+    int per_sm = 0, sms = 0, dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = verify_tc_occupancy(&per_sm)) != cudaSuccess) return e;
+    const long long segs = (long long)B * Hkv;
+    plan->tc_target = num_workers > 0 ? num_workers : (long long)kTcWaves * sms * (per_sm > 0 ? per_sm : 1);
+    plan->tc_grid = plan->tc_target + segs;
+    plan->tc = use_tc >= 0 ? use_tc != 0 : R >= kTcMinRows;
+    // workspace for either kernel: partials (o, lse) per slot and row, then a counter per segment
+    plan->slots = (size_t)shares + (size_t)segs;
+    const size_t tc_slots = (size_t)plan->tc_grid;
+    if (tc_slots > plan->slots) plan->slots = tc_slots;
     size_t bytes = plan->slots * R * kHeadDim * 4;  // partial o
     bytes += plan->slots * R * 4;                   // partial lse (base 2)
     plan->counters_offset = (bytes + 255) & ~size_t(255);
-    plan->ws_bytes = plan->counters_offset + (size_t)B * Hkv * sizeof(unsigned long long);
+    plan->ws_bytes = plan->counters_offset + (size_t)segs * sizeof(unsigned long long);
     return cudaSuccess;
 }
 

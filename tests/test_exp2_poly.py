@@ -18,7 +18,7 @@ def _script():
 
 
 def kernel_constants():
-    src = (CSRC / "prefill_tc.cu").read_text()
+    src = (CSRC / "tc_tile.cuh").read_text()
     return np.array([float(re.search(rf"kExp2C{i} = ([0-9.e+-]+)f;", src).group(1)) for i in range(4)],
                     dtype=np.float32)
 

@@ -18,6 +18,14 @@ def S():
     return sinkattn
 
 
+@pytest.fixture(autouse=True, params=["mma", "tc"])
+def kernel(request, monkeypatch):
+    """Every case runs on both verification kernels: the mma.sync one and the tcgen05 one (the
+    library reads SINKATTN_VERIFY_KERNEL at every call)."""
+    monkeypatch.setenv("SINKATTN_VERIFY_KERNEL", request.param)
+    return request.param
+
+
 def run(S, inp, **kw):
     g = inp.to("cuda")
     out, lse = S.sinkattn_verify(g.q, g.k_pages, g.v_pages, g.page_table, g.kv_lens, g.sinks, g.scale, **kw)
