@@ -89,7 +89,7 @@ PrefillKernel prefill_kernel_choice() {
 }
 
 // Which verification kernel runs: SINKATTN_VERIFY_KERNEL=tc the tcgen05 kernel, =mma the mma.sync
-// kernel, unset the library's choice (by query rows per KV head).  Read at every call.
+// kernel, unset the library's choice (the tcgen05 kernel).  Read at every call.
 int verify_kernel_choice() {
     const char* s = std::getenv("SINKATTN_VERIFY_KERNEL");
     if (s && std::strcmp(s, "tc") == 0) return 1;
@@ -360,7 +360,6 @@ sinkattn_status_t verify_common(const void* q, const void* k_pages, const void* 
     a.workers = plan.grid;
     a.min_pages_per_worker = 0;  // set by the launcher
     a.fixed_workers = dims->num_workers > 0 ? 1 : 0;
-    a.tc_target = plan.tc_target;
     a.tc_grid = plan.tc_grid;
     a.scale_log2 = scale * 1.4426950408889634f;
     cudaError_t e;

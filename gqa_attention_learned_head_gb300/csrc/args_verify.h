@@ -22,15 +22,13 @@ struct VerifyArgs {
     unsigned* err;
     int B, QL, Hq, Hkv, G, R, num_pages, max_pages;  // R = QL * G rows per segment
     int workers, min_pages_per_worker, fixed_workers;  // the mma.sync kernel's split
-    // the tcgen05 kernel's split: request b gets chunks in proportion to its 128-key tiles, about
-    // tc_target over all tiles; CTA x of tc_grid (>= every chunk) finds its chunk on the device
-    long long tc_target, tc_grid;
+    long long tc_grid;  // the tcgen05 kernel's shares (one CTA each); fixed_workers: exactly that many
     float scale_log2;
 };
 struct VerifyPlan {
     bool tc;  // the tcgen05 kernel runs (else the mma.sync kernel)
     int grid, warps, stages;  // mma.sync kernel
-    long long tc_target, tc_grid;  // tcgen05 kernel
+    long long tc_grid;  // tcgen05 kernel: shares
     size_t smem, slots, counters_offset, ws_bytes;  // workspace: enough for either kernel
 };
 // use_tc: -1 = the library's choice, 0 = the mma.sync kernel, 1 = the tcgen05 kernel

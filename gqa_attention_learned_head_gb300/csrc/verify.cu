@@ -48,9 +48,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kNegInf = -__builtin_huge_valf();
 // The library's choice between the two kernels: the tcgen05 kernel from this many query rows per
-// (request, KV head) on, and its chunking target in CTAs per resident slot.
-constexpr int kTcMinRows = 16;
-constexpr int kTcWaves = 1;
+// (request, KV head) on (measured faster at 8, 16, 32 and 64 rows).
+constexpr int kTcMinRows = 1;
 
 // Shared memory: ring | full / empty barriers | bad-page flags | misc | pend | queue | prefix[B+1].
 struct Layout {
@@ -590,20 +589,18 @@ cudaError_t verify_plan(int B, int QL, int Hq, int Hkv, int num_workers, int use
     plan->warps = W;
     plan->stages = S;
     plan->smem = smem;
-    // tcgen05 kernel: chunks of whole 128-key tiles, planned on the device in proportion to each
-    // request's tiles, about kTcWaves CTAs per resident slot in all (num_workers > 0: that many);
-    // the grid covers every chunk (at most the target plus one per segment)
+    // tcgen05 kernel: one share of the (request, KV head, 128-key tile) units per resident slot
+    // (num_workers > 0: that many shares)
     int per_sm = 0, sms = 0, dev = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     if ((e = verify_tc_occupancy(&per_sm)) != cudaSuccess) return e;
     const long long segs = (long long)B * Hkv;
-    plan->tc_target = num_workers > 0 ? num_workers : (long long)kTcWaves * sms * (per_sm > 0 ? per_sm : 1);
-    plan->tc_grid = plan->tc_target + segs;
+    plan->tc_grid = num_workers > 0 ? num_workers : (long long)sms * (per_sm > 0 ? per_sm : 1);
     plan->tc = use_tc >= 0 ? use_tc != 0 : R >= kTcMinRows;
     // workspace for either kernel: partials (o, lse) per slot and row, then a counter per segment
     plan->slots = (size_t)shares + (size_t)segs;
-    const size_t tc_slots = (size_t)plan->tc_grid;
+    const size_t tc_slots = (size_t)plan->tc_grid + (size_t)segs;  // partial slot = share + segment
     if (tc_slots > plan->slots) plan->slots = tc_slots;
     size_t bytes = plan->slots * R * kHeadDim * 4;  // partial o
     bytes += plan->slots * R * 4;                   // partial lse (base 2)

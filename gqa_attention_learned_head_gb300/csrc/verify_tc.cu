@@ -13,19 +13,25 @@
 // GB300 design.  The R = q_len x G query rows of one (request b, KV head g) --
 // row r = i * G + h is drafted token i of query head g * G + h -- form ONE
 // tcgen05 tile (R <= 64, padded to the MMA's 128 rows), so the group's K/V pass
-// costs the cache bytes once and every product runs on the tensor core:
-//   warps 0, 3  TMA producers: warp 0 loads the rows of Q with one 3-D copy
-//               (64 dims x G heads x q_len tokens, landing as rows i * G + h)
-//               and the K tiles, warp 3 the V tiles; a 128-key tile is 8 page
-//               copies of 2 KB (lanes 0-7), 128-byte swizzle.
+// costs the cache bytes once and every product runs on the tensor core.
+// Work: the flattened list of (request, KV head, 128-key tile) units, one
+// contiguous share per CTA (one CTA per resident slot), cut at segment ends
+// into pieces (the split of split_kv.cuh with tiles as units).  The pipeline
+// runs on across the pieces of a share:
+//   warps 0, 3  TMA producers: warp 0 loads each piece's Q rows with one 3-D
+//               copy (64 dims x G heads x q_len tokens, landing as rows
+//               i * G + h) into a 2-slot Q ring and the K tiles, warp 3 the V
+//               tiles; a tile is 8 page copies of 2 KB (lanes 0-7), 128-byte
+//               swizzle.
 //   warp 1      allocates 256 TMEM columns; one lane issues S_j = Q K_j^T.
-//   warp 2      one lane issues O += P_j V_j (P read from TMEM).
-//   warps 4-7   softmax, thread r = row r (only the warps that hold rows work):
-//               each row masked at its own causal limit or by its tree mask.
-// A (request, KV head) segment is cut into chunks of whole 128-key tiles, one CTA
-// each; the chunk holding token 0 is seeded with the sink.  A segment of several
-// chunks writes fp32 partials per row and the CTA that completes it (an epoch-
-// tagged arrival counter) merges them by log-sum-exp.  Every wait is bounded.
+//   warp 2      one lane issues O += P_j V_j (P read from TMEM; the first tile
+//               of a piece starts O afresh).
+//   warps 4-7   softmax, thread r = row r (only the warps that hold rows work),
+//               each row masked at its own causal limit or by its tree mask; at
+//               a piece's end they read O and write the rows (or fp32 partials).
+// A piece holding token 0 is seeded with the sink; the pieces of a segment
+// split between CTAs are merged by the CTA whose arrival completes it.  Every
+// wait is bounded.
 #include "args_verify.h"
 #include "ptx.cuh"
 #include "split_kv.cuh"
@@ -39,17 +45,71 @@ using namespace tc;
 constexpr int kThreads = 256;
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColS = 0, kColO = 128, kColP = 192;
-constexpr int kKStages = 3, kVStages = 2;
+constexpr int kKStages = 2, kVStages = 2;
 constexpr int kPagesPerTile = kBN / kPageSize;  // 8
+constexpr int kMinTiles = 4;  // automatic mode: never cut shares finer than this
+
+
+__device__ __forceinline__ int kv_len_of(const VerifyArgs& a, int i) {
+    return clamp_len(__ldg(&a.kv_lens[i]), a.max_pages * kPageSize);
+}
+__device__ __forceinline__ int tiles_of(int kv_len) { return (kv_len + kBN - 1) / kBN; }
+
+// One piece: tiles [ta, tb) of segment (b, g), whose first unit is seg_start and which has `tiles` tiles.
+struct Piece {
+    int b, g, ta, tb, tiles, kv_len;
+    long long seg_start;
+};
+
+// Walks the pieces of units [x, x1); every role of the CTA runs its own walker over the same share.
+struct Walk {
+    int b, g, tiles, kv_len;
+    long long seg_start, x, x1;
+    int B, Hkv;
+
+    // the next segment with at least one tile (a walk never passes the share's end)
+    __device__ void advance(const VerifyArgs& a) {
+        seg_start += tiles;
+        if (++g == Hkv) {
+            g = 0;
+            do {
+                ++b;
+                kv_len = kv_len_of(a, b);
+                tiles = tiles_of(kv_len);
+            } while (tiles == 0 && b + 1 < B);
+        }
+    }
+    __device__ bool next(const VerifyArgs& a, Piece& p) {
+        if (x >= x1) return false;
+        while (x >= seg_start + tiles) advance(a);
+        p.b = b;
+        p.g = g;
+        p.tiles = tiles;
+        p.kv_len = kv_len;
+        p.seg_start = seg_start;
+        p.ta = (int)(x - seg_start);
+        const long long end = x1 < seg_start + tiles ? x1 : seg_start + tiles;
+        p.tb = (int)(end - seg_start);
+        x = end;
+        return true;
+    }
+};
 
 struct __align__(1024) Smem {
-    uint8_t q[kTileBytes];
+    uint8_t q[2][kTileBytes];
     uint8_t k[kKStages][kTileBytes];
     uint8_t v[kVStages][kTileBytes];
-    uint64_t q_full, k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
-    uint64_t s_full, s_free, p_full, o_done, mma_done, v_fixed;
+    uint64_t q_full[2], q_empty[2], k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
+    uint64_t s_full, s_free, p_full, o_done, mma_done;
     uint32_t tmem_base;
-    int last;  // this CTA completes its segment and merges it
+    int pend[2];         // segments of this share's partial pieces ...
+    int pend_tiles[2];   // ... their tiles ...
+    long long pend_start[2];  // ... and their first units
+    int last;            // this CTA completes the segment being merged
+    long long red[8];    // block reductions
+    long long found[4];  // share start: request, its first unit, its tiles, flag
+    Walk walk[4];        // the softmax warps' walkers (kept out of their registers)
+    Piece piece[4];      // ... and their current pieces
 };
 
 // TMA row of page pg of segment (b, g) in the 2-D map over the page pool; a page past the cache
@@ -67,141 +127,62 @@ __device__ __forceinline__ int page_row(const VerifyArgs& a, int b, int g, int p
 
 __device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-// 128-key tiles of request i's cache (its length clamped to the page table's reach)
-__device__ __forceinline__ int request_tiles(const VerifyArgs& a, int i) {
-    return (clamp_len(__ldg(&a.kv_lens[i]), a.max_pages * kPageSize) + kBN - 1) / kBN;
-}
-
-// Chunks of request i (every KV head of the request has that many): chunks of at most
-// ceil(U / target) tiles, so that the U tiles of all segments make at most target + segments chunks.
-__device__ __forceinline__ int request_chunks(long long tiles, long long target, long long U) {
-    if (U <= 0 || tiles <= 1) return 1;
-    const long long size = (U + target - 1) / target;
-    return (int)((tiles + size - 1) / size);
-}
-
-struct Located {
-    int b, x0, n, tiles;  // request, index of its first chunk, chunks per KV head, tiles per segment
-};
-
-// Finds the request whose chunks hold CTA index x (chunk index = request-major, then KV head, then
-// chunk): U over all requests, then a running block-wide scan of the chunk counts.  Every CTA
-// computes the same plan; false if x is past the last chunk.  All threads take part.
-__device__ bool locate(const VerifyArgs& a, long long x, int* scratch, Located& loc) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    constexpr int kWarpsPerCta = kThreads / 32;
-    long long part = 0;
-    for (int i = tid; i < a.B; i += kThreads) {
-        const int raw = __ldg(&a.kv_lens[i]);
-        if ((raw < 0 || raw > a.max_pages * kPageSize) && blockIdx.x == 0) atomicOr(a.err, kErrBadLength);
-        part += request_tiles(a, i);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-    long long* red = reinterpret_cast<long long*>(scratch);  // [kWarpsPerCta] warp totals
-    if (lane == 0) red[warp] = part;
-    __syncthreads();
-    long long U = 0;
-#pragma unroll
-    for (int w = 0; w < kWarpsPerCta; ++w) U += red[w];
-    U *= a.Hkv;
-    int* found = scratch + 2 * kWarpsPerCta;  // [0] flag, [1] b, [2] x0, [3] n, [4] tiles
-    if (tid == 0) found[0] = 0;
-    __syncthreads();
-    long long base = 0;
-    for (int p0 = 0; p0 < a.B; p0 += kThreads) {
-        const int i = p0 + tid;
-        int tb = 0, nb = 0;
-        long long cnt = 0;
-        if (i < a.B) {
-            tb = request_tiles(a, i);
-            nb = request_chunks(tb, a.tc_target, U);
-            cnt = (long long)nb * a.Hkv;
-        }
-        long long incl = cnt;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const long long y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
-        }
-        __syncthreads();  // the previous pass has read red[]
-        if (lane == 31) red[warp] = incl;
-        __syncthreads();
-        long long woff = 0, total = 0;
-#pragma unroll
-        for (int w = 0; w < kWarpsPerCta; ++w) {
-            woff += w < warp ? red[w] : 0;
-            total += red[w];
-        }
-        const long long lo = base + woff + incl - cnt;
-        if (i < a.B && cnt > 0 && x >= lo && x < lo + cnt) {
-            found[0] = 1;
-            found[1] = i;
-            found[2] = (int)lo;
-            found[3] = nb;
-            found[4] = tb;
-        }
-        base += total;
-        __syncthreads();
-        if (found[0]) break;
-    }
-    loc.b = found[1];
-    loc.x0 = found[2];
-    loc.n = found[3];
-    loc.tiles = found[4];
-    return found[0] != 0;
-}
-
-// ---- a segment of several chunks: the CTA whose arrival completes it merges the partials, by the
-// four softmax warps (after their partials are written) with one thread per row
-__device__ __forceinline__ void merge_segment(const VerifyArgs& a, Smem& sm, int seg, long long slot0, int b, int g,
-                                              int nchunks) {
-    const int R = a.R, QL = a.QL, G = a.G;
-    softmax_bar();  // every partial of this CTA is written (CTA scope) ...
-    if (threadIdx.x == 128) sm.last = arrive_last(&a.counters[seg], a.epoch, nchunks) ? 1 : 0;  // ... and published
-    softmax_bar();
-    const int r = threadIdx.x - 128;
-    if (!sm.last || r >= R) return;
+// Log-sum-exp merge of segment seg from its pieces' partials (base-2 lse), by the 128 softmax threads:
+// DIMS head-dims of one row per thread (64 / DIMS threads per row), pieces taken four at a time
+// with all their loads issued together and combined online.
+template <int DIMS>
+__device__ void merge_rows(const VerifyArgs& a, int seg, long long slot0, int pieces, int t) {
+    constexpr int kTpr = kHeadDim / DIMS, kChunk = 4;
+    const int R = a.R, G = a.G, b = seg / a.Hkv, g = seg - b * a.Hkv;
+    const int r = t / kTpr, d0 = (t % kTpr) * DIMS;
+    if (r >= R) return;
     const float* lp = a.part_lse + slot0 * R + r;
-    const float* op = a.part_o + (slot0 * R + r) * kHeadDim;
-    float M = kNegInf;
-    for (int k = 0; k < nchunks; ++k) M = fmaxf(M, __ldcg(lp + (long long)k * R));
-    const int i = r / G, h = r % G;
-    const long long row = ((long long)b * QL + i) * a.Hq + g * G + h;
-    uint4* dst = reinterpret_cast<uint4*>(a.out + row * kHeadDim);
-    if (M == kNegInf) {  // no live key and no finite sink in any chunk
+    const float* op = a.part_o + (slot0 * R + r) * kHeadDim + d0;
+    float M = kNegInf, sum = 0.f, o[DIMS];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) dst[e] = make_uint4(0u, 0u, 0u, 0u);
-        if (a.lse) a.lse[row] = kNegInf;
-        return;
-    }
-    float sum = 0.f;
-    float acc[64];
+    for (int e = 0; e < DIMS; ++e) o[e] = 0.f;
+    for (int c0 = 0; c0 < pieces; c0 += kChunk) {
+        float l[kChunk];
+        float4 v[kChunk][DIMS / 4];
 #pragma unroll
-    for (int e = 0; e < 64; ++e) acc[e] = 0.f;
-    for (int k = 0; k < nchunks; ++k) {
-        const float l = __ldcg(lp + (long long)k * R);
-        if (l == kNegInf) continue;
-        const float w = exp2f(l - M);
-        sum += w;
-        const float4* src = reinterpret_cast<const float4*>(op + (long long)k * R * kHeadDim);
+        for (int k = 0; k < kChunk; ++k) {
+            const bool in = c0 + k < pieces;
+            l[k] = in ? __ldcg(lp + (long long)(c0 + k) * R) : kNegInf;
+            const float4* src = reinterpret_cast<const float4*>(op + (long long)(c0 + k) * R * kHeadDim);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            const float4 v = __ldcg(src + e);
-            acc[4 * e + 0] += w * v.x;
-            acc[4 * e + 1] += w * v.y;
-            acc[4 * e + 2] += w * v.z;
-            acc[4 * e + 3] += w * v.w;
+            for (int e = 0; e < DIMS / 4; ++e) v[k][e] = in ? __ldcg(src + e) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-    }
-    const float inv = 1.f / sum;
+        float Mc = M;
 #pragma unroll
-    for (int e = 0; e < 8; ++e)
-        dst[e] = make_uint4(pack_bf16(acc[8 * e + 0] * inv, acc[8 * e + 1] * inv),
-                            pack_bf16(acc[8 * e + 2] * inv, acc[8 * e + 3] * inv),
-                            pack_bf16(acc[8 * e + 4] * inv, acc[8 * e + 5] * inv),
-                            pack_bf16(acc[8 * e + 6] * inv, acc[8 * e + 7] * inv));
-    if (a.lse) a.lse[row] = (M + log2f(sum)) * kLn2;
+        for (int k = 0; k < kChunk; ++k) Mc = fmaxf(Mc, l[k]);
+        if (Mc == kNegInf) continue;
+        const float rs = M == kNegInf ? 0.f : exp2f(M - Mc);
+        sum *= rs;
+#pragma unroll
+        for (int e = 0; e < DIMS; ++e) o[e] *= rs;
+#pragma unroll
+        for (int k = 0; k < kChunk; ++k) {
+            const float w = l[k] == kNegInf ? 0.f : exp2f(l[k] - Mc);
+            sum += w;
+#pragma unroll
+            for (int e = 0; e < DIMS / 4; ++e) {
+                o[4 * e + 0] += w * v[k][e].x;
+                o[4 * e + 1] += w * v[k][e].y;
+                o[4 * e + 2] += w * v[k][e].z;
+                o[4 * e + 3] += w * v[k][e].w;
+            }
+        }
+        M = Mc;
+    }
+    const int i = r / G, h = r % G;
+    const long long row = ((long long)b * a.QL + i) * a.Hq + g * G + h;
+    uint4* dst = reinterpret_cast<uint4*>(a.out + row * kHeadDim + d0);
+    const float inv = M == kNegInf ? 0.f : 1.f / sum;  // no live key and no finite sink: zeros
+#pragma unroll
+    for (int e = 0; e < DIMS / 8; ++e)
+        dst[e] = make_uint4(pack_bf16(o[8 * e + 0] * inv, o[8 * e + 1] * inv), pack_bf16(o[8 * e + 2] * inv, o[8 * e + 3] * inv),
+                            pack_bf16(o[8 * e + 4] * inv, o[8 * e + 5] * inv), pack_bf16(o[8 * e + 6] * inv, o[8 * e + 7] * inv));
+    if (d0 == 0 && a.lse) a.lse[row] = M == kNegInf ? kNegInf : (M + log2f(sum)) * kLn2;
 }
 
 __global__ void __launch_bounds__(kThreads, 2)
@@ -209,27 +190,118 @@ __global__ void __launch_bounds__(kThreads, 2)
                      const __grid_constant__ CUtensorMap tmap_v, const VerifyArgs a) {
     extern __shared__ uint8_t smem_raw[];
     Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    Located loc;
-    if (!locate(a, blockIdx.x, reinterpret_cast<int*>(sm.k[0]), loc)) return;  // whole CTA: past the last chunk
-    const int nchunks = loc.n, local = (int)(blockIdx.x - loc.x0);
-    const int b = loc.b, g = local / nchunks, c = local % nchunks;
-    const int seg = b * a.Hkv + g;
-    const long long slot0 = (long long)loc.x0 + (long long)g * nchunks;  // partial slot of the segment's chunk 0
-    const int kv_len = clamp_len(__ldg(&a.kv_lens[b]), a.max_pages * kPageSize);
-    const int tiles = loc.tiles;
-    // chunk c of the segment: tiles [c * tiles / n, (c + 1) * tiles / n)
-    const int t0 = (int)((long long)c * tiles / nchunks), t1 = (int)((long long)(c + 1) * tiles / nchunks);
-    const int ntile = t1 - t0;
-    const bool whole = nchunks == 1;
-    const int R = a.R, QL = a.QL, G = a.G;
-    const int pos0 = kv_len - QL;  // cache position of drafted token 0 (negative for a short cache)
-    const int active = (R + 31) / 32;  // softmax warps that hold rows
-    // the last V tile may end inside a page whose later slots hold anything
-    const bool fix_last_v = ntile > 0 && t1 == tiles && tiles * kBN > kv_len;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int B = a.B, Hkv = a.Hkv, R = a.R, QL = a.QL, G = a.G;
 
-    if (threadIdx.x == 0) {
-        mbar_init(&sm.q_full, 1);
+    // ---- 1. units (Hkv x tiles) per request: their total U and, by a running block-wide scan, the
+    // request holding this share's first unit (one pass when the batch fits the CTA's threads)
+    if (tid == 0) sm.found[3] = 0;
+    long long U = 0, base = 0, lo = 0, cnt = 0;
+    for (int p0 = 0; p0 < B; p0 += kThreads) {
+        const int i = p0 + tid;
+        int ti = 0;
+        if (i < B) {
+            const int raw = __ldg(&a.kv_lens[i]);
+            if ((raw < 0 || raw > a.max_pages * kPageSize) && blockIdx.x == 0) atomicOr(a.err, kErrBadLength);
+            ti = tiles_of(clamp_len(raw, a.max_pages * kPageSize));
+        }
+        const long long c = (long long)ti * Hkv;
+        long long incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        __syncthreads();  // red[] is free
+        if (lane == 31) sm.red[warp] = incl;
+        __syncthreads();
+        long long woff = 0, total = 0;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) {
+            woff += w < warp ? sm.red[w] : 0;
+            total += sm.red[w];
+        }
+        if (B <= kThreads) {  // one pass: this thread's request and its units stay in registers
+            lo = woff + incl - c;
+            cnt = c;
+        }
+        U = base + total;
+        base = U;
+    }
+    {  // rows of requests with an empty cache carry only the sink
+        const long long rows = (long long)B * QL * a.Hq;
+        for (long long r = (long long)blockIdx.x * kThreads + tid; r < rows; r += (long long)gridDim.x * kThreads) {
+            const int b = (int)(r / ((long long)QL * a.Hq));
+            if (kv_len_of(a, b) != 0) continue;
+            uint4* dst = reinterpret_cast<uint4*>(a.out + r * kHeadDim);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) dst[e] = make_uint4(0u, 0u, 0u, 0u);
+            if (a.lse) a.lse[r] = __ldg(&a.sinks[r % a.Hq]);
+        }
+    }
+    if (U == 0) return;
+    const long long C = effective_shares(a.tc_grid, a.fixed_workers, kMinTiles, U);
+    const long long cta = blockIdx.x;
+    if (cta >= C) return;
+    const long long x0 = cta * U / C, x1 = (cta + 1) * U / C;
+    if (B <= kThreads) {
+        if (cnt > 0 && x0 >= lo && x0 < lo + cnt) {
+            sm.found[0] = tid;
+            sm.found[1] = lo;
+            sm.found[2] = cnt / Hkv;
+        }
+        __syncthreads();
+    } else {
+        // ---- 2. a second scan, now that U (and so x0) is known
+        base = 0;
+        for (int p0 = 0; p0 < B; p0 += kThreads) {
+            const int i = p0 + tid;
+            const int ti = i < B ? tiles_of(kv_len_of(a, i)) : 0;
+            const long long c = (long long)ti * Hkv;
+            long long incl = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            __syncthreads();  // red[] (and found[3]) are settled
+            if (lane == 31) sm.red[warp] = incl;
+            __syncthreads();
+            long long woff = 0, total = 0;
+#pragma unroll
+            for (int w = 0; w < kThreads / 32; ++w) {
+                woff += w < warp ? sm.red[w] : 0;
+                total += sm.red[w];
+            }
+            const long long l0 = base + woff + incl - c;
+            if (c > 0 && x0 >= l0 && x0 < l0 + c) {
+                sm.found[0] = i;
+                sm.found[1] = l0;
+                sm.found[2] = ti;
+                sm.found[3] = 1;
+            }
+            base += total;
+            __syncthreads();
+            if (sm.found[3]) break;
+        }
+    }
+    Walk walk;
+    walk.B = B;
+    walk.Hkv = Hkv;
+    walk.b = (int)sm.found[0];
+    walk.tiles = (int)sm.found[2];
+    walk.kv_len = kv_len_of(a, walk.b);
+    walk.g = (int)((x0 - sm.found[1]) / walk.tiles);
+    walk.seg_start = sm.found[1] + (long long)walk.g * walk.tiles;
+    walk.x = x0;
+    walk.x1 = x1;
+    const int active = (R + 31) / 32;  // softmax warps that hold rows
+
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm.q_full[i], 1);
+            mbar_init(&sm.q_empty[i], 1);
+        }
         for (int i = 0; i < kKStages; ++i) {
             mbar_init(&sm.k_full[i], 1);
             mbar_init(&sm.k_empty[i], 1);
@@ -243,8 +315,6 @@ __global__ void __launch_bounds__(kThreads, 2)
         mbar_init(&sm.p_full, 32 * active);
         mbar_init(&sm.o_done, 1);
         mbar_init(&sm.mma_done, 2);
-        mbar_init(&sm.v_fixed, 1);
-        sm.last = 0;
         fence_mbar_init();
         fence_proxy_async_smem();
     }
@@ -253,8 +323,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         tmem_relinquish();
     }
     // Q rows R..127 (no query) are zeros, so their scores stay finite; the TMA writes rows 0..R-1
-    for (int e = R * 8 + (int)threadIdx.x; e < kBM * 8; e += kThreads)
-        reinterpret_cast<uint4*>(sm.q)[e] = make_uint4(0u, 0u, 0u, 0u);
+    for (int e = R * 8 + tid; e < kBM * 8; e += kThreads) {
+        reinterpret_cast<uint4*>(sm.q[0])[e] = make_uint4(0u, 0u, 0u, 0u);
+        reinterpret_cast<uint4*>(sm.q[1])[e] = make_uint4(0u, 0u, 0u, 0u);
+    }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -263,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     if (warp < 4) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
-        if (ntile > 0 && (warp == 0 || warp == 3)) {
+        if (warp == 0 || warp == 3) {
             // ------------------------------------------------------------ TMA producers
             const bool is_k = warp == 0;
             const int stages = is_k ? kKStages : kVStages;
@@ -272,222 +344,264 @@ __global__ void __launch_bounds__(kThreads, 2)
             const CUtensorMap* map = is_k ? &tmap_k : &tmap_v;
             if (lane == 0) {
                 tma_prefetch_desc(map);
-                if (is_k) {
-                    tma_prefetch_desc(&tmap_q);
-                    mbar_arrive_expect_tx(&sm.q_full, (uint32_t)R * 128u);
-                    tma_load_3d(sm.q, &tmap_q, 0, g * G, b * QL, &sm.q_full);
-                }
+                if (is_k) tma_prefetch_desc(&tmap_q);
             }
-            int issued = 0;
+            int J = 0, p = 0, issued = 0;  // tiles, pieces (their Q issued) and tile copies issued so far
             bool ok = true;
-            for (int j = 0; j < ntile; ++j) {
-                const int st = j % stages;
-                if (j >= stages) {
-                    int got = 0;
-                    if (lane == 0) got = mbar_wait(&empty[st], ((j / stages) - 1) & 1);
+            Piece pc;
+            while (ok && walk.next(a, pc)) {
+                if (is_k) {  // this piece's Q rows into Q slot p & 1, once the piece two back has used it
+                    int got = 1;
+                    if (lane == 0) {
+                        if (p >= 2) got = mbar_wait(&sm.q_empty[p & 1], ((p >> 1) - 1) & 1);
+                        if (got) {
+                            mbar_arrive_expect_tx(&sm.q_full[p & 1], (uint32_t)R * 128u);
+                            tma_load_3d(sm.q[p & 1], &tmap_q, 0, pc.g * G, pc.b * QL, &sm.q_full[p & 1]);
+                        }
+                    }
                     if (!(ok = __shfl_sync(0xffffffffu, got, 0) != 0)) break;
                 }
-                const int row = page_row(a, b, g, (t0 + j) * kPagesPerTile + (lane & 7), kv_len);
-                if (lane == 0) mbar_arrive_expect_tx(&full[st], kTileBytes);
-                __syncwarp();
-                uint8_t* tile = is_k ? sm.k[st] : sm.v[st];
-                if (lane < kPagesPerTile) tma_load_2d(tile + lane * (kPageSize * 128), map, 0, row, &full[st]);
-                issued = j + 1;
-            }
-            if (!ok && lane == 0) atomicOr(a.err, kErrTimeout);
-            if (!is_k && ok && fix_last_v) {
-                // zero the rows of the last V tile at or past the cache end, then hand it over
-                const int j = ntile - 1, st = j % kVStages;
-                const bool landed = __all_sync(0xffffffffu, mbar_wait(&sm.v_full[st], (j / kVStages) & 1));
-                if (landed) {
-                    const int r0 = kv_len - (t1 - 1) * kBN;
-                    for (int i = r0 * 8 + lane; i < kBN * 8; i += 32)
-                        reinterpret_cast<uint4*>(sm.v[st])[i] = make_uint4(0u, 0u, 0u, 0u);
-                    fence_proxy_async_smem();
+                ++p;
+                for (int t = pc.ta; ok && t < pc.tb; ++t, ++J) {
+                    const int st = J % stages;
+                    if (J >= stages) {
+                        int got = 0;
+                        if (lane == 0) got = mbar_wait(&empty[st], ((J / stages) - 1) & 1);
+                        if (!(ok = __shfl_sync(0xffffffffu, got, 0) != 0)) break;
+                    }
+                    const int row = page_row(a, pc.b, pc.g, t * kPagesPerTile + (lane & 7), pc.kv_len);
+                    if (lane == 0) mbar_arrive_expect_tx(&full[st], kTileBytes);
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&sm.v_fixed);
-                } else if (lane == 0) {
-                    atomicOr(a.err, kErrTimeout);
+                    uint8_t* tile = is_k ? sm.k[st] : sm.v[st];
+                    if (lane < kPagesPerTile) tma_load_2d(tile + lane * (kPageSize * 128), map, 0, row, &full[st]);
+                    issued = J + 1;
                 }
             }
+            if (!ok && lane == 0) atomicOr(a.err, kErrTimeout);
             // every copy this warp started has landed before the CTA can exit (bounded)
             if (lane == 0) {
-                if (is_k) (void)mbar_wait(&sm.q_full, 0);
                 for (int j = issued - stages < 0 ? 0 : issued - stages; j < issued; ++j)
                     (void)mbar_wait(&full[j % stages], (j / stages) & 1);
+                if (is_k)
+                    for (int q = p - 2 < 0 ? 0 : p - 2; q < p; ++q) (void)mbar_wait(&sm.q_full[q & 1], (q >> 1) & 1);
             }
-        } else if (ntile > 0 && warp == 1 && lane == 0) {
+        } else if (warp == 1 && lane == 0) {
             // ------------------------------------------------------------ S issuer: S_j = Q K_j^T
             const uint32_t tS = tbase + kColS;
-            const uint32_t qaddr = smem_u32(sm.q);
-            bool ok = mbar_wait(&sm.q_full, 0);
-            for (int j = 0; ok && j < ntile; ++j) {
-                const int st = j % kKStages;
-                ok = mbar_wait(&sm.k_full[st], (j / kKStages) & 1) && (j == 0 || mbar_wait(&sm.s_free, (j - 1) & 1));
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t kaddr = smem_u32(sm.k[st]);
+            int J = 0, p = 0;
+            bool ok = true;
+            Piece pc;
+            while (ok && walk.next(a, pc)) {
+                if (!(ok = mbar_wait(&sm.q_full[p & 1], (p >> 1) & 1))) break;
+                const uint32_t qaddr = smem_u32(sm.q[p & 1]);
+                for (int t = pc.ta; t < pc.tb; ++t, ++J) {
+                    const int st = J % kKStages;
+                    ok = mbar_wait(&sm.k_full[st], (J / kKStages) & 1) && (J == 0 || mbar_wait(&sm.s_free, (J - 1) & 1));
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t kaddr = smem_u32(sm.k[st]);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    tc_mma_ss(tS, sw128_desc(qaddr + kk * 32), sw128_desc(kaddr + kk * 32), kIdescQK, kk > 0);
-                tc_commit(&sm.s_full);
-                tc_commit(&sm.k_empty[st]);
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc_mma_ss(tS, sw128_desc(qaddr + kk * 32), sw128_desc(kaddr + kk * 32), kIdescQK, kk > 0);
+                    tc_commit(&sm.s_full);
+                    tc_commit(&sm.k_empty[st]);
+                }
+                tc_commit(&sm.q_empty[p & 1]);  // this piece's Q slot is free once its products end
+                ++p;
             }
             if (!ok) atomicOr(a.err, kErrTimeout);
             tc_commit(&sm.mma_done);  // every MMA of both issuers has finished before TMEM is released
             (void)mbar_wait(&sm.mma_done, 0);
-        } else if (ntile > 0 && warp == 2 && lane == 0) {
+        } else if (warp == 2) {
             // ------------------------------------------------------------ PV issuer: O += P_j V_j
+            // Lane 0 issues; the whole warp zeroes the rows past the cache end of a segment's last V tile
+            // (they may hold anything, and a 0 weight times NaN is NaN) before its product.
             const uint32_t tO = tbase + kColO, tP = tbase + kColP;
+            int J = 0;
             bool ok = true;
-            for (int j = 0; ok && j < ntile; ++j) {
-                ok = ((fix_last_v && j == ntile - 1) ? mbar_wait(&sm.v_fixed, 0)
-                                                     : mbar_wait(&sm.v_full[j % kVStages], (j / kVStages) & 1)) &&
-                     mbar_wait(&sm.p_full, j & 1);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t vaddr = smem_u32(sm.v[j % kVStages]);
+            Piece pc;
+            while (ok && walk.next(a, pc)) {
+                for (int t = pc.ta; t < pc.tb; ++t, ++J) {
+                    const int st = J % kVStages;
+                    ok = warp_wait(&sm.v_full[st], (J / kVStages) & 1);
+                    if (!ok) break;
+                    if (t == pc.tiles - 1 && pc.tiles * kBN > pc.kv_len) {
+                        for (int e = (pc.kv_len - t * kBN) * 8 + lane; e < kBN * 8; e += 32)
+                            reinterpret_cast<uint4*>(sm.v[st])[e] = make_uint4(0u, 0u, 0u, 0u);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                    }
+                    if (!(ok = warp_wait(&sm.p_full, J & 1))) break;
+                    if (lane == 0) {
+                        tc_fence_after();
+                        const uint32_t vaddr = smem_u32(sm.v[st]);
+                        // P_j is written only after the softmax has read the previous piece's O, so the
+                        // first tile of a piece may start O afresh
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    tc_mma_ts(tO, tP + ks * 8, sw128_desc(vaddr + ks * 2048), kIdescPV, (j > 0 || ks > 0) ? 1u : 0u);
-                tc_commit(&sm.v_empty[j % kVStages]);
-                tc_commit(&sm.o_done);
+                        for (int ks = 0; ks < 8; ++ks)
+                            tc_mma_ts(tO, tP + ks * 8, sw128_desc(vaddr + ks * 2048), kIdescPV,
+                                      (t > pc.ta || ks > 0) ? 1u : 0u);
+                        tc_commit(&sm.v_empty[st]);
+                        tc_commit(&sm.o_done);
+                    }
+                    __syncwarp();
+                }
             }
-            if (!ok) atomicOr(a.err, kErrTimeout);
-            tc_commit(&sm.mma_done);
-            (void)mbar_wait(&sm.mma_done, 0);
+            if (lane == 0) {
+                if (!ok) atomicOr(a.err, kErrTimeout);
+                tc_commit(&sm.mma_done);
+                (void)mbar_wait(&sm.mma_done, 0);
+            }
         }
     } else {
         // 128 x 56 + 128 x 200 = 256 x 128, the launch's registers
         asm volatile("setmaxnreg.inc.sync.aligned.u32 200;");
-        const int r = threadIdx.x - 128;
+        const int r = tid - 128;
         const bool live = r < R;
         const int i = live ? r / G : 0, h = live ? r % G : 0;
+        int pend_n = 0;  // partial pieces of this share (at most its first and its last)
         if (warp - 4 < active) {
             // ---------------------------------------------------------------- softmax
             const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
             const uint32_t tS = tbase + lane_off + kColS, tO = tbase + lane_off + kColO, tP = tbase + lane_off + kColP;
             const bool tree = a.tree_mask != nullptr;
-            // the drafted keys this tree row sees (q_len <= 16 bits)
-            const uint32_t dbits =
-                (tree && live) ? (uint32_t)(__ldg(&a.tree_mask[(long long)b * QL + i]) & ((1ull << QL) - 1)) : 0u;
-            // a linear row sees keys [0, lim)
-            const int lim = live ? pos0 + i + 1 : 0;
             const float scale_log2 = a.scale_log2;
-            float m = (c == 0 && live) ? __ldg(&a.sinks[g * G + h]) * kLog2e : kNegInf;  // seeded with the sink
-            float d = (c == 0 && live) ? 1.f : 0.f;                                      // e^(sink - m) = 1
+            int J = 0;
             bool ok = true;
-            for (int j = 0; j < ntile; ++j) {
-                if (!(ok = warp_wait(&sm.s_full, j & 1))) break;
-                tc_fence_after();
-                float s[128];
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc)
-                    tmem_ld32(tS + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[cc * 32]));
-                tc_wait_ld();
-                tc_fence_before();
-                mbar_arrive(&sm.s_free);
-
-                const int kb = (t0 + j) * kBN;
-                float mul = scale_log2;
-                if (!(scale_log2 > 0.f)) {  // zero or negative scale: scale first, mask after
-#pragma unroll
-                    for (int cc = 0; cc < 128; ++cc) s[cc] *= scale_log2;
-                    mul = 1.f;
-                }
-                if (kb + kBN > pos0) {
-                    // the tile holds drafted keys or the cache end: this row's visible keys of the tile
-                    // as four 32-bit words -- every key before the draft, then (tree) the drafted keys
-                    // its mask names or (linear) the drafted keys up to its own
-                    const int lo = pos0 - kb;  // keys of the tile before the draft
-                    uint32_t vis[4];
-#pragma unroll
-                    for (int w = 0; w < 4; ++w) {
-                        const int n = (tree ? lo : lim - kb) - 32 * w;
-                        uint32_t bitsw = n <= 0 ? 0u : n >= 32 ? 0xFFFFFFFFu : ((1u << n) - 1u);
-                        const int off = lo - 32 * w;
-                        if (tree && off > -32 && off < 32) bitsw |= off >= 0 ? (dbits << off) : (dbits >> -off);
-                        vis[w] = bitsw;
-                    }
-#pragma unroll
-                    for (int cc = 0; cc < 128; ++cc) s[cc] = ((vis[cc >> 5] >> (cc & 31)) & 1u) ? s[cc] : kNegInf;
-                }
-                float acc[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) acc[e] = fmax3(s[e], s[8 + e], s[16 + e]);
-#pragma unroll
-                for (int cc = 24; cc < 120; cc += 16)
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[e] = fmax3(acc[e], s[cc + e], s[cc + 8 + e]);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) acc[e] = fmaxf(acc[e], s[120 + e]);
-                const float mx_raw =
-                    fmaxf(fmax3(acc[0], acc[1], acc[2]), fmax3(acc[3], acc[4], fmax3(acc[5], acc[6], acc[7])));
-                const float mx = mx_raw == kNegInf ? kNegInf : mx_raw * mul;
-                const float m_new = fmaxf(m, mx);
-                float factor = 1.f;
-                bool rescale_o = false;
-                if (j == 0 || m_new > m + kRescaleThreshold) {
-                    factor = (m_new == kNegInf) ? 1.f : fast_exp2(m - m_new);
-                    rescale_o = (j > 0);
-                    m = m_new;
-                    d *= factor;
-                }
-                const float neg_m = (m == kNegInf) ? 0.f : -m;
-                const float2 mul2 = make_float2(mul, mul), negm2 = make_float2(neg_m, neg_m);
-                float2 sums[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                                  make_float2(0.f, 0.f)};
-                uint32_t pk[64];
-#pragma unroll
-                for (int cc = 0; cc < 64; ++cc) {
-                    const float2 xx = ffma2(make_float2(s[2 * cc], s[2 * cc + 1]), mul2, negm2);
-                    const float2 pp = make_float2(fast_exp2(xx.x), fast_exp2(xx.y));
-                    sums[cc & 3] = fadd2(sums[cc & 3], pp);
-                    pk[cc] = pack_bf16(pp.x, pp.y);
-                }
-                const float2 s01 = fadd2(fadd2(sums[0], sums[1]), fadd2(sums[2], sums[3]));
-                d += s01.x + s01.y;
-                if (j > 0) {  // P_{j-1} consumed and O_{j-1} final before P and O are touched
-                    if (!(ok = warp_wait(&sm.o_done, (j - 1) & 1))) break;
+            const int sw = warp - 4;
+            if (lane == 0) sm.walk[sw] = walk;
+            __syncwarp();
+            while (ok) {
+                int has = 0;
+                __syncwarp();  // every lane is done with the previous piece
+                if (lane == 0) has = sm.walk[sw].next(a, sm.piece[sw]) ? 1 : 0;
+                if (!__shfl_sync(0xffffffffu, has, 0)) break;
+                __syncwarp();
+                const Piece& pc = sm.piece[sw];
+                const int pos0 = pc.kv_len - QL;  // cache position of drafted token 0 (negative: short cache)
+                // the drafted keys this tree row sees (q_len <= 16 bits); a linear row sees keys [0, lim)
+                const uint32_t dbits =
+                    (tree && live) ? (uint32_t)(__ldg(&a.tree_mask[(long long)pc.b * QL + i]) & ((1ull << QL) - 1))
+                                   : 0u;
+                const int lim = live ? pos0 + i + 1 : 0;
+                const int ta = pc.ta, tb = pc.tb;
+                const bool seeded = ta == 0;
+                float m = (seeded && live) ? __ldg(&a.sinks[pc.g * G + h]) * kLog2e : kNegInf;
+                float d = (seeded && live) ? 1.f : 0.f;  // the sink's own e^(sink - m) = 1
+                for (int t = ta; t < tb; ++t, ++J) {
+                    if (!(ok = warp_wait(&sm.s_full, J & 1))) break;
                     tc_fence_after();
-                    if (__any_sync(0xffffffffu, rescale_o)) {
+                    float s[128];
 #pragma unroll
-                        for (int cc = 0; cc < 2; ++cc) {
-                            uint32_t o[32];
-                            tmem_ld32(tO + cc * 32, o);
-                            tc_wait_ld();
+                    for (int cc = 0; cc < 4; ++cc)
+                        tmem_ld32(tS + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[cc * 32]));
+                    tc_wait_ld();
+                    tc_fence_before();
+                    mbar_arrive(&sm.s_free);
+
+                    const int kb = t * kBN;
+                    float mul = scale_log2;
+                    if (!(scale_log2 > 0.f)) {  // zero or negative scale: scale first, mask after
 #pragma unroll
-                            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * factor);
-                            tmem_st32(tO + cc * 32, o);
+                        for (int cc = 0; cc < 128; ++cc) s[cc] *= scale_log2;
+                        mul = 1.f;
+                    }
+                    if (kb + kBN > pos0) {
+                        // the tile holds drafted keys or the cache end: this row's visible keys of the
+                        // tile as four 32-bit words -- every key before the draft, then (tree) the
+                        // drafted keys its mask names or (linear) the drafted keys up to its own
+                        const int lo = pos0 - kb;  // keys of the tile before the draft
+                        uint32_t vis[4];
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+                            const int n = (tree ? lo : lim - kb) - 32 * w;
+                            uint32_t bitsw = n <= 0 ? 0u : n >= 32 ? 0xFFFFFFFFu : ((1u << n) - 1u);
+                            const int off = lo - 32 * w;
+                            if (tree && off > -32 && off < 32) bitsw |= off >= 0 ? (dbits << off) : (dbits >> -off);
+                            vis[w] = bitsw;
+                        }
+#pragma unroll
+                        for (int cc = 0; cc < 128; ++cc) s[cc] = ((vis[cc >> 5] >> (cc & 31)) & 1u) ? s[cc] : kNegInf;
+                    }
+                    float acc[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[e] = fmax3(s[e], s[8 + e], s[16 + e]);
+#pragma unroll
+                    for (int cc = 24; cc < 120; cc += 16)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[e] = fmax3(acc[e], s[cc + e], s[cc + 8 + e]);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[e] = fmaxf(acc[e], s[120 + e]);
+                    const float mx_raw =
+                        fmaxf(fmax3(acc[0], acc[1], acc[2]), fmax3(acc[3], acc[4], fmax3(acc[5], acc[6], acc[7])));
+                    const float mx = mx_raw == kNegInf ? kNegInf : mx_raw * mul;
+                    const float m_new = fmaxf(m, mx);
+                    const bool first = t == ta;  // O starts afresh with this piece
+                    float factor = 1.f;
+                    bool rescale_o = false;
+                    if (first || m_new > m + kRescaleThreshold) {
+                        factor = (m_new == kNegInf) ? 1.f : fast_exp2(m - m_new);
+                        rescale_o = !first;
+                        m = m_new;
+                        d *= factor;
+                    }
+                    const float neg_m = (m == kNegInf) ? 0.f : -m;
+                    const float2 mul2 = make_float2(mul, mul), negm2 = make_float2(neg_m, neg_m);
+                    float2 sums[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                      make_float2(0.f, 0.f)};
+                    uint32_t pk[64];
+#pragma unroll
+                    for (int cc = 0; cc < 64; ++cc) {
+                        const float2 xx = ffma2(make_float2(s[2 * cc], s[2 * cc + 1]), mul2, negm2);
+                        const float2 pp = make_float2(fast_exp2(xx.x), fast_exp2(xx.y));
+                        sums[cc & 3] = fadd2(sums[cc & 3], pp);
+                        pk[cc] = pack_bf16(pp.x, pp.y);
+                    }
+                    const float2 s01 = fadd2(fadd2(sums[0], sums[1]), fadd2(sums[2], sums[3]));
+                    d += s01.x + s01.y;
+                    if (!first) {  // P_{j-1} consumed and O_{j-1} final before P and O are touched
+                        if (!(ok = warp_wait(&sm.o_done, (J - 1) & 1))) break;
+                        tc_fence_after();
+                        if (__any_sync(0xffffffffu, rescale_o)) {
+#pragma unroll
+                            for (int cc = 0; cc < 2; ++cc) {
+                                uint32_t o[32];
+                                tmem_ld32(tO + cc * 32, o);
+                                tc_wait_ld();
+#pragma unroll
+                                for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * factor);
+                                tmem_st32(tO + cc * 32, o);
+                            }
                         }
                     }
+                    tmem_st32(tP, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+                    tmem_st32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+                    tc_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(&sm.p_full);
                 }
-                tmem_st32(tP, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-                tmem_st32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
-                tc_wait_st();
-                tc_fence_before();
-                mbar_arrive(&sm.p_full);
-            }
-            if (ok && ntile > 0) ok = warp_wait(&sm.o_done, (ntile - 1) & 1);
-            if (!ok) {
-                if (lane == 0) atomicOr(a.err, kErrTimeout);
-            } else {
-                // O / d of this row (zero when the chunk has no key: only an empty cache's single chunk)
+                if (!ok) break;
+                // ---- end of the piece (the PV of its last tile has finished): O / d of this row
+                if (!(ok = warp_wait(&sm.o_done, (J - 1) & 1))) break;
+                tc_fence_after();
                 uint32_t o[64];
-                if (ntile > 0) {
-                    tc_fence_after();
-                    tmem_ld32(tO, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
-                    tmem_ld32(tO + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
-                    tc_wait_ld();
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 64; ++e) o[e] = 0u;
+                tmem_ld32(tO, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
+                tmem_ld32(tO + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
+                tc_wait_ld();
+                tc_fence_before();
+                const bool whole = seeded && tb == pc.tiles;
+                const int seg = pc.b * Hkv + pc.g;
+                if (!whole && tid == 128) {
+                    sm.pend[pend_n] = seg;
+                    sm.pend_tiles[pend_n] = pc.tiles;
+                    sm.pend_start[pend_n] = pc.seg_start;
                 }
+                pend_n += whole ? 0 : 1;
                 if (live) {
                     const float inv = d > 0.f ? 1.f / d : 0.f;
                     const float l2 = d > 0.f ? m + log2f(d) : kNegInf;
                     if (whole) {
-                        const long long row = ((long long)b * QL + i) * a.Hq + g * G + h;
+                        const long long row = ((long long)pc.b * QL + i) * a.Hq + pc.g * G + h;
                         uint4* dst = reinterpret_cast<uint4*>(a.out + row * kHeadDim);
 #pragma unroll
                         for (int e = 0; e < 8; ++e) {
@@ -500,7 +614,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                         }
                         if (a.lse) a.lse[row] = l2 * kLn2;
                     } else {
-                        const long long slot = slot0 + c;
+                        const long long slot = cta + seg;  // partial slot of this piece
                         float4* dst = reinterpret_cast<float4*>(a.part_o + (slot * R + r) * kHeadDim);
 #pragma unroll
                         for (int e = 0; e < 16; ++e)
@@ -510,11 +624,36 @@ __global__ void __launch_bounds__(kThreads, 2)
                     }
                 }
             }
+            if (!ok && lane == 0) atomicOr(a.err, kErrTimeout);
+        } else {
+            // a softmax warp without rows counts the share's partial pieces too
+            Piece pc;
+            while (walk.next(a, pc)) pend_n += (pc.ta == 0 && pc.tb == pc.tiles) ? 0 : 1;
         }
-        if (!whole) merge_segment(a, sm, seg, slot0, b, g, nchunks);
+        // ---- the share's partial pieces (at most its first and its last): arrive on their segments'
+        // counters together; the CTA completing a segment merges it
+        pend_n = __shfl_sync(0xffffffffu, pend_n, 0);
+        softmax_bar();  // the partials of this CTA are written (CTA scope) and pend[] is set
+        if (tid - 128 < pend_n) {
+            const int k = tid - 128;
+            const int seg = sm.pend[k];
+            long long c_first = 0;
+            int pieces = 0;
+            segment_pieces(sm.pend_start[k], sm.pend_tiles[k], C, U, c_first, pieces);
+            const bool last = arrive_last(&a.counters[seg], a.epoch, pieces);  // release + acquire
+            sm.red[2 * k] = last ? c_first + seg : -1;  // merge job: the segment's first partial slot ...
+            sm.red[2 * k + 1] = pieces;                  // ... and its pieces
+        }
+        softmax_bar();
+        for (int k = 0; k < pend_n; ++k) {
+            const long long slot0 = sm.red[2 * k];
+            if (slot0 < 0) continue;
+            if (R <= 32) merge_rows<16>(a, sm.pend[k], slot0, (int)sm.red[2 * k + 1], r);
+            else merge_rows<32>(a, sm.pend[k], slot0, (int)sm.red[2 * k + 1], r);
+        }
     }
     tc_fence_before();
-    __syncthreads();  // TMEM is no longer read
+    __syncthreads();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tbase, kTmemCols);
@@ -525,28 +664,47 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 size_t verify_tc_smem() { return 1024 + sizeof(Smem); }
 
+// CTAs of this kernel that fit on one SM, from its registers, its shared memory (with the per-block
+// reservation) and its tensor memory (512 columns per SM, kTmemCols per CTA).  Computed here because
+// the runtime's occupancy query reports one CTA per SM for this kernel whatever its size, while the
+// hardware keeps two resident.
 cudaError_t verify_tc_occupancy(int* per_sm) {
-    static thread_local bool set[64] = {};
+    static thread_local int cached[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev >= 64 || !set[dev]) {
-        e = cudaFuncSetAttribute(verify_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)verify_tc_smem());
-        if (e != cudaSuccess) return e;
-        if (dev < 64) set[dev] = true;
+    if (dev < 64 && cached[dev] > 0) {
+        *per_sm = cached[dev];
+        return cudaSuccess;
     }
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, verify_tc_kernel, kThreads, verify_tc_smem());
+    e = cudaFuncSetAttribute(verify_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)verify_tc_smem());
+    if (e != cudaSuccess) return e;
+    cudaFuncAttributes fa;
+    if ((e = cudaFuncGetAttributes(&fa, verify_tc_kernel)) != cudaSuccess) return e;
+    int smem_sm = 0, reserved = 0, regs_sm = 0;
+    if ((e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev)) != cudaSuccess)
+        return e;
+    const size_t block_smem = verify_tc_smem() + fa.sharedSizeBytes + (size_t)reserved;
+    const int regs_warp = ((fa.numRegs * 32 + 255) / 256) * 256;  // allocated per warp in units of 256
+    int n = 512 / (int)kTmemCols;
+    n = n < (int)(smem_sm / block_smem) ? n : (int)(smem_sm / block_smem);
+    n = n < regs_sm / (regs_warp * (kThreads / 32)) ? n : regs_sm / (regs_warp * (kThreads / 32));
+    if (n < 1) return cudaErrorInvalidConfiguration;
+    if (dev < 64) cached[dev] = n;
+    *per_sm = n;
+    return cudaSuccess;
 }
 
 cudaError_t verify_tc_launch(const VerifyArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                              cudaStream_t stream) {
     if (a.B == 0) return cudaSuccess;
-    const long long grid = a.tc_grid;
-    if (grid > 0x7fffffffll) return cudaErrorInvalidConfiguration;
+    if (a.tc_grid > 0x7fffffffll || a.tc_grid < 1) return cudaErrorInvalidConfiguration;
     int per_sm = 0;  // also sets the kernel's shared-memory limit
     cudaError_t e = verify_tc_occupancy(&per_sm);
     if (e != cudaSuccess) return e;
-    verify_tc_kernel<<<(unsigned)grid, kThreads, verify_tc_smem(), stream>>>(tq, tk, tv, a);
+    verify_tc_kernel<<<(unsigned)a.tc_grid, kThreads, verify_tc_smem(), stream>>>(tq, tk, tv, a);
     return cudaGetLastError();
 }
 
