@@ -80,7 +80,6 @@ def peaks():
 # Sources each profiled kernel is compiled from (its own file, the headers it includes).
 KERNEL_SOURCES = {
     "decode_split_kernel": ["decode.cu", "ptx.cuh", "split_kv.cuh", "args_decode.h", "args_common.h"],
-    "verify_split_kernel": ["verify.cu", "ptx.cuh", "split_kv.cuh", "args_verify.h", "args_common.h"],
     "verify_tc_kernel": ["verify_tc.cu", "verify.cu", "ptx.cuh", "split_kv.cuh", "tc_tile.cuh", "args_verify.h",
                          "args_common.h"],
     "prefill_pp_kernel": ["prefill_pp.cu", "ptx.cuh", "tc_tile.cuh", "tile_order.cuh", "args_prefill.h",
