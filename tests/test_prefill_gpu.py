@@ -87,6 +87,22 @@ def test_mixed_serving_prefill_sampled(S):
     assert_parity(out[rows[:, 0], rows[:, 1]], lse[rows[:, 0], rows[:, 1]], ro, rl, "mixed prefill")
 
 
+def test_causal_prefill_every_row(S):
+    """The full-size causal prefill (2 x 8192 tokens, 64 q / 8 KV heads), every one of its 1 048 576
+    rows against the oracle (a minute or two of the oracle on the host cores)."""
+    inp = W.causal_prefill()
+    out, lse, err = run(S, inp)
+    assert err == 0
+    assert_parity(out, lse, *ref(inp), "causal prefill 2x8192, every row")
+
+
+def test_mixed_serving_prefill_every_row(S):
+    inp = W.mixed_serving_prefill()
+    out, lse, err = run(S, inp)
+    assert err == 0
+    assert_parity(out, lse, *ref(inp), "mixed prefill, every row")
+
+
 def test_too_long_sequence_is_reported(S):
     inp = W.make_prefill(4, 1, [100, 40], seed=4)
     out, lse, err = run(S, inp, max_seqlen=64)
