@@ -488,7 +488,18 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const bool seeded = ta == 0;
                 float m = (seeded && live) ? __ldg(&a.sinks[pc.g * G + h]) * kLog2e : kNegInf;
                 float d = (seeded && live) ? 1.f : 0.f;  // the sink's own e^(sink - m) = 1
+                // page ids of a tile (lanes 0-7), loaded one tile ahead: a page outside the pool was
+                // fetched as zeros, and its tokens count as absent
+                const int kvl = pc.kv_len;
+                const int* row_pt = a.page_table + (long long)pc.b * a.max_pages;
+                auto page_id = [&](int t) {
+                    const int pg = t * kPagesPerTile + (lane & 7);
+                    return (lane < kPagesPerTile && pg < a.max_pages && pg * kPageSize < kvl) ? __ldg(&row_pt[pg]) : 0;
+                };
+                int pid = page_id(ta);
                 for (int t = ta; t < tb; ++t, ++J) {
+                    const uint32_t bad8 = __ballot_sync(0xffffffffu, pid < 0 || pid >= a.num_pages);
+                    if (t + 1 < tb) pid = page_id(t + 1);
                     if (!(ok = warp_wait(&sm.s_full, J & 1))) break;
                     tc_fence_after();
                     float s[128];
@@ -506,19 +517,23 @@ __global__ void __launch_bounds__(kThreads, 2)
                         for (int cc = 0; cc < 128; ++cc) s[cc] *= scale_log2;
                         mul = 1.f;
                     }
-                    if (kb + kBN > pos0) {
-                        // the tile holds drafted keys or the cache end: this row's visible keys of the
-                        // tile as four 32-bit words -- every key before the draft, then (tree) the
-                        // drafted keys its mask names or (linear) the drafted keys up to its own
+                    const bool draft_tile = kb + kBN > pos0;
+                    if (draft_tile || bad8 != 0u) {
+                        // the tile holds drafted keys, the cache end or an absent page: this row's
+                        // visible keys of the tile as four 32-bit words -- every key before the draft,
+                        // then (tree) the drafted keys its mask names or (linear) the drafted keys up
+                        // to its own, less the keys of absent pages
                         const int lo = pos0 - kb;  // keys of the tile before the draft
                         uint32_t vis[4];
 #pragma unroll
                         for (int w = 0; w < 4; ++w) {
-                            const int n = (tree ? lo : lim - kb) - 32 * w;
+                            const int n = draft_tile ? (tree ? lo : lim - kb) - 32 * w : 32;
                             uint32_t bitsw = n <= 0 ? 0u : n >= 32 ? 0xFFFFFFFFu : ((1u << n) - 1u);
                             const int off = lo - 32 * w;
                             if (tree && off > -32 && off < 32) bitsw |= off >= 0 ? (dbits << off) : (dbits >> -off);
-                            vis[w] = bitsw;
+                            const uint32_t absent = ((bad8 >> (2 * w)) & 1u ? 0x0000FFFFu : 0u) |
+                                                    ((bad8 >> (2 * w + 1)) & 1u ? 0xFFFF0000u : 0u);
+                            vis[w] = bitsw & ~absent;
                         }
 #pragma unroll
                         for (int cc = 0; cc < 128; ++cc) s[cc] = ((vis[cc >> 5] >> (cc & 31)) & 1u) ? s[cc] : kNegInf;

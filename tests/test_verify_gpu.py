@@ -197,3 +197,21 @@ def test_tree_verify_full_size_sampled(S):
     ro, rl = ref_tree(inp, masks, rows)
     assert_parity(out[rows[:, 0], rows[:, 1], rows[:, 2]], lse[rows[:, 0], rows[:, 1], rows[:, 2]], ro, rl, "tree")
     assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
+
+
+def test_bad_page_tokens_count_as_absent(S):
+    """A page id outside the pool: its tokens count as absent on both kernels -- the request's rows equal
+    the oracle's on the same cache with that page's 16 tokens left out (the page lies before the draft,
+    and visibility depends only on positions relative to the draft)."""
+    inp = W.make_decode(2, 8, 2, [40, 40], seed=37, q_len=2)
+    ok = W.make_decode(2, 8, 2, [40, 40], seed=37, q_len=2)
+    P = inp.k_pages.shape[0]
+    pt = inp.page_table.clone()
+    inp.page_table[1, 0] = P + 5
+    out, lse, err = run(S, inp)
+    assert err == S.ERR_BAD_PAGE
+    ok.page_table[1, 0], ok.page_table[1, 1] = pt[1, 1], pt[1, 2]  # the cache without its first page
+    ok.kv_lens[1] = 24
+    rows = np.array([[1, i, h] for i in range(2) for h in range(8)], dtype=np.int32)
+    ro, rl = ref(ok, rows)
+    assert_parity(out[1].reshape(-1, 64), lse[1].reshape(-1), ro, rl, "request with an absent page")
