@@ -587,6 +587,14 @@ sinkattn_status_t sinkattn_merge(const float* partial_o, const float* partial_ls
     return merge_launch(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SINKATTN_OK : SINKATTN_ERR_CUDA;
 }
 
+sinkattn_status_t sinkattn_selftest_wait_timeout(void* stream) {
+    DeviceState* ds = nullptr;
+    sinkattn_status_t st = device_state(&ds);
+    if (st != SINKATTN_OK) return st;
+    return wait_timeout_selftest_launch(ds->err, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SINKATTN_OK
+                                                                                                  : SINKATTN_ERR_CUDA;
+}
+
 sinkattn_status_t sinkattn_get_error(void* stream) {
     DeviceState* ds = nullptr;
     sinkattn_status_t st = device_state(&ds);

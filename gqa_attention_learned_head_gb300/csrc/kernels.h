@@ -7,3 +7,8 @@
 #include "args_paged.h"
 #include "args_prefill.h"
 #include "args_verify.h"
+
+namespace sinkattn {
+// selftest.cu: one thread waits, with the library's bounded wait, on an mbarrier nothing completes.
+cudaError_t wait_timeout_selftest_launch(unsigned* err, cudaStream_t stream);
+}  // namespace sinkattn

@@ -18,8 +18,10 @@ enum : unsigned {
 };
 
 // A wait polls try_wait at most this many times (each poll may also suspend
-// the thread for a short hardware-chosen time) before it is declared lost.
-constexpr uint32_t kMaxPolls = 1u << 22;
+// the thread for a short hardware-chosen time) before it is declared lost:
+// about a second on GB300 (2^22 polls took 16 s), while the longest wait of a
+// healthy pipeline -- one tile's copy or product -- takes microseconds.
+constexpr uint32_t kMaxPolls = 1u << 18;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -63,7 +63,7 @@ class MergeDims(ctypes.Structure):
 
 EXPORTS = ("sinkattn_decode", "sinkattn_prefill", "sinkattn_merge", "sinkattn_decode_workspace_size", "sinkattn_verify",
            "sinkattn_verify_workspace_size", "sinkattn_kv_append", "sinkattn_prefill_paged", "sinkattn_verify_tree", "sinkattn_qkv_prologue",
-           "sinkattn_get_error", "sinkattn_status_string", "sinkattn_version")
+           "sinkattn_get_error", "sinkattn_status_string", "sinkattn_version", "sinkattn_selftest_wait_timeout")
 
 
 def _load():
@@ -88,6 +88,8 @@ def _load():
                                           ctypes.POINTER(PagedDims), P]
     lib.sinkattn_prefill_paged.argtypes = [P, P, P, P, P, P, P, f32, P, P, ctypes.POINTER(PagedDims), P]
     lib.sinkattn_get_error.argtypes = [P]
+    lib.sinkattn_selftest_wait_timeout.argtypes = [P]
+    lib.sinkattn_selftest_wait_timeout.restype = ctypes.c_int
     lib.sinkattn_status_string.argtypes = [ctypes.c_int]
     lib.sinkattn_status_string.restype = ctypes.c_char_p
     lib.sinkattn_version.restype = i32
@@ -398,6 +400,12 @@ def sinkattn_decode_noalloc(q, k_pages, v_pages, page_table, kv_lens, sinks, sca
                                       _stream(stream))
     _check(st, "sinkattn_decode_noalloc")
     return out, lse
+
+
+def sinkattn_selftest_wait_timeout(stream=None) -> None:
+    """Enqueues the bounded-wait failure path (one thread waiting on an mbarrier nothing completes);
+    the device error word then holds ERR_TIMEOUT (see include/sinkattn.h)."""
+    _check(_lib.sinkattn_selftest_wait_timeout(_stream(stream)), "sinkattn_selftest_wait_timeout")
 
 
 def sinkattn_get_error(stream=None) -> int:

@@ -382,6 +382,16 @@ sinkattn_status_t sinkattn_decode_noalloc(const void *q, const void *k_pages, co
  */
 sinkattn_status_t sinkattn_get_error(void *stream);
 
+/*
+ * Diagnostic for the failure path of the kernels' bounded waits (not for the hot path): enqueues on
+ * `stream` one thread that waits, with the same bounded wait as every pipeline stage of the
+ * attention kernels, on an mbarrier that nothing completes.  The wait gives up after its poll limit
+ * (seconds) and raises SINKATTN_ERR_TIMEOUT in the device error word -- read it with
+ * sinkattn_get_error -- and the kernel returns: no trap, and the context stays usable.  Returns
+ * the status of the launch itself.
+ */
+sinkattn_status_t sinkattn_selftest_wait_timeout(void *stream);
+
 /* Static English text for a status code. */
 const char *sinkattn_status_string(sinkattn_status_t status);
 
