@@ -86,7 +86,7 @@ KERNEL_SOURCES = {
                           "args_common.h"],
     "prefill_tc_kernel": ["prefill_tc.cu", "ptx.cuh", "tc_tile.cuh", "tile_order.cuh", "args_prefill.h",
                           "args_common.h"],
-    "prefill_tc_kernel_paged": ["prefill_tc.cu", "ptx.cuh", "tc_tile.cuh", "tile_order.cuh", "args_prefill.h",
+    "prefill_pp_kernel_paged": ["prefill_pp.cu", "ptx.cuh", "tc_tile.cuh", "tile_order.cuh", "args_prefill.h",
                                 "args_common.h"],
     "qkv_prologue_kernel": ["prologue.cu", "ptx.cuh", "args_paged.h", "args_common.h"],
 }
@@ -904,12 +904,12 @@ def run_ours(args):
         unit = "TFLOP/s"
         achieved = flops / (ms * 1e-3) / 1e12
         first = "kv_append_kernel" if name == "chunked_prefill" else "qkv_prologue_kernel"
-        roof = {"bound": "tensor", "kernel": f"prefill_tc_kernel<paged> + {first} (the two kernels of a step); "
+        roof = {"bound": "tensor", "kernel": f"prefill_pp_kernel<paged> + {first} (the two kernels of a step); "
                                              "achieved over the whole step",
                 "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s", "frac": achieved / tc_peak,
                 "peak_source": f"{peak_src} bf16_tflops",
-                "traffic": profiled_traffic("prefill_tc_kernel_paged", "chunked_prefill",
-                                            KERNEL_SOURCES["prefill_tc_kernel_paged"])}
+                "traffic": profiled_traffic("prefill_pp_kernel_paged", "chunked_prefill",
+                                            KERNEL_SOURCES["prefill_pp_kernel_paged"])}
         if name == "serving_step":
             p_ms = statistics.mean(ptimes)
             p_gbs = moved / (p_ms * 1e-3) / 1e9

@@ -76,7 +76,8 @@ unsigned long long next_epoch() {
 
 // Which prefill kernel runs.  By default the two-head tcgen05 kernel when the query-head group
 // size is even, else the one-head tcgen05 kernel.  SINKATTN_PREFILL_KERNEL=tc forces the one-head
-// kernel and =mma the warp-level mma.sync kernel (kept as the measured baseline only).
+// kernel and =mma the warp-level mma.sync kernel (kept as the measured baseline only; the paged
+// prefill has no mma.sync form and runs the one-head kernel then).
 enum class PrefillKernel { kAuto, kOneHead, kLegacy };
 PrefillKernel prefill_kernel_choice() {
     static const PrefillKernel choice = [] {
@@ -454,7 +455,10 @@ sinkattn_status_t sinkattn_prefill_paged(const void* q, const void* k_pages, con
     a.start_pos = start_pos;
     a.num_pages = d.num_pages;
     a.max_pages = d.max_pages;
-    const cudaError_t e = prefill_paged_launch(a, tq, tk, tv, static_cast<cudaStream_t>(stream));
+    // the two-head kernel for an even query-head group (unless the one-head kernel is forced)
+    const bool two_head = a.G % 2 == 0 && prefill_kernel_choice() == PrefillKernel::kAuto;
+    const cudaError_t e = two_head ? prefill_pp_paged_launch(a, tq, tk, tv, static_cast<cudaStream_t>(stream))
+                                   : prefill_paged_launch(a, tq, tk, tv, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? SINKATTN_OK : SINKATTN_ERR_CUDA;
 }
 

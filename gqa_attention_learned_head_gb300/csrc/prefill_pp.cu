@@ -52,6 +52,7 @@ struct __align__(1024) Smem {
     uint64_t s_full[2], s_free[2], p_full[2], o_done[2];
     uint64_t turn[2];  // turn[w] completes a phase when the other warpgroup has finished an exp phase
     uint64_t mma_done;
+    uint64_t v_fixed;  // paged: the last V tile with its rows past the cache end zeroed
     uint32_t tmem_base;
 };
 
@@ -62,6 +63,9 @@ __device__ __forceinline__ float ex2_in_turn(float x) {
 }
 
 
+// kPaged: K and V come from the page pool through page_table, the new tokens of a sequence sit at
+// cache positions start_pos .. start_pos + L - 1 and see the whole cached prefix.
+template <bool kPaged>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_pp_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v, const PrefillArgs a) {
@@ -83,8 +87,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int L = min(a.cu_seqlens[seq + 1] - s0, a.max_seqlen);
     const int row0 = qt * kBM;
     const int kvh = h0 / a.G;  // h0 and h0 + 1 share it: the group size is even
-    const int kend = a.causal ? min(L, row0 + kBM) : L;
+    int start = 0;  // cache position of the sequence's first new token
+    if constexpr (kPaged) {
+        start = __ldg(&a.start_pos[seq]);
+        if (start < 0 || (long long)start + L > (long long)a.max_pages * kPageSize) {
+            if (h0 == 0 && threadIdx.x == 0) atomicOr(a.err, kErrBadLength);
+            start = max(0, min(start, a.max_pages * kPageSize - L));
+        }
+    }
+    const int kv_total = start + L;  // cached tokens once the new ones are in
+    const int kend = a.causal ? min(kv_total, start + row0 + kBM) : kv_total;
     const int ntile = (kend + kBN - 1) / kBN;
+    // paged: the last V tile may end inside a page whose later slots hold anything
+    const bool fix_last_v = kPaged && ntile * kBN > kv_total;
 
     if (threadIdx.x == 0) {
         mbar_init(&sm.q_full, 1);
@@ -104,6 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sm.turn[w], 4);  // one arrival per warp of the other warpgroup
         }
         mbar_init(&sm.mma_done, 2);
+        mbar_init(&sm.v_fixed, 1);
         fence_mbar_init();
         fence_proxy_async_smem();
     }
@@ -118,7 +134,61 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp < 4) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
-        if (warp == 0 && lane == 0) {
+        if (kPaged && (warp == 0 || warp == 3)) {
+            // ------------------------------------------------------------ TMA producers over the page pool:
+            // warp 0 Q_0, Q_1 and K_j, warp 3 V_j; lanes 0-7 each copy one 16-token page of a 128-key tile.
+            const bool is_k = warp == 0;
+            const int stages = is_k ? kKStages : kVStages;
+            uint64_t* full = is_k ? sm.k_full : sm.v_full;
+            uint64_t* empty = is_k ? sm.k_empty : sm.v_empty;
+            const CUtensorMap* map = is_k ? &tmap_k : &tmap_v;
+            if (lane == 0) {
+                tma_prefetch_desc(map);
+                if (is_k) {
+                    tma_prefetch_desc(&tmap_q);
+                    mbar_arrive_expect_tx(&sm.q_full, 2 * kTileBytes);
+                    tma_load_3d(sm.q[0], &tmap_q, 0, h0, s0 + row0, &sm.q_full);
+                    tma_load_3d(sm.q[1], &tmap_q, 0, h0 + 1, s0 + row0, &sm.q_full);
+                }
+            }
+            int issued = 0;
+            bool ok = true;
+            for (int j = 0; j < ntile; ++j) {
+                const int st = j % stages;
+                if (j >= stages) {
+                    int got = 0;
+                    if (lane == 0) got = mbar_wait(&empty[st], ((j / stages) - 1) & 1);
+                    if (!(ok = __shfl_sync(0xffffffffu, got, 0) != 0)) break;
+                }
+                const int row = page_tile_row(a, seq, kvh, j * (kBN / kPageSize) + (lane & 7), kv_total);
+                if (lane == 0) mbar_arrive_expect_tx(&full[st], kTileBytes);
+                __syncwarp();
+                uint8_t* tile = is_k ? sm.k[st] : sm.v[st];
+                if (lane < kBN / kPageSize) tma_load_2d(tile + lane * (kPageSize * 128), map, 0, row, &full[st]);
+                issued = j + 1;
+            }
+            if (!ok && lane == 0) atomicOr(a.err, kErrTimeout);
+            if (!is_k && ok && fix_last_v) {
+                // zero the rows of the last V tile at or past the cache end, then hand it over
+                const int j = ntile - 1, st = j % kVStages;
+                const bool landed = __all_sync(0xffffffffu, mbar_wait(&sm.v_full[st], (j / kVStages) & 1));
+                if (landed) {
+                    for (int i = (kv_total - j * kBN) * 8 + lane; i < kBN * 8; i += 32)
+                        reinterpret_cast<uint4*>(sm.v[st])[i] = make_uint4(0u, 0u, 0u, 0u);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sm.v_fixed);
+                } else if (lane == 0) {
+                    atomicOr(a.err, kErrTimeout);
+                }
+            }
+            // every copy this warp started has landed before the CTA can exit (bounded)
+            if (lane == 0) {
+                if (is_k) (void)mbar_wait(&sm.q_full, 0);
+                for (int j = issued - stages < 0 ? 0 : issued - stages; j < issued; ++j)
+                    (void)mbar_wait(&full[j % stages], (j / stages) & 1);
+            }
+        } else if (!kPaged && warp == 0 && lane == 0) {
             // ------------------------------------------------------------ TMA producer: Q_0, Q_1, then K_j
             tma_prefetch_desc(&tmap_q);
             tma_prefetch_desc(&tmap_k);
@@ -140,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             (void)mbar_wait(&sm.q_full, 0);
             for (int j = issued - kKStages < 0 ? 0 : issued - kKStages; j < issued; ++j)
                 (void)mbar_wait(&sm.k_full[j % kKStages], (j / kKStages) & 1);
-        } else if (warp == 3 && lane == 0) {
+        } else if (!kPaged && warp == 3 && lane == 0) {
             // ------------------------------------------------------------ TMA producer: V_j
             tma_prefetch_desc(&tmap_v);
             int issued = 0;
@@ -185,7 +255,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int j = 0; ok && j < ntile; ++j) {
                 const int st = j % kVStages;
-                if (!(ok = mbar_wait(&sm.v_full[st], (j / kVStages) & 1))) break;
+                if (!(ok = (fix_last_v && j == ntile - 1) ? mbar_wait(&sm.v_fixed, 0)
+                                                           : mbar_wait(&sm.v_full[st], (j / kVStages) & 1)))
+                    break;
                 const uint32_t vaddr = smem_u32(sm.v[st]);
 #pragma unroll
                 for (int w = 0; w < 2; ++w) {
@@ -231,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&sm.s_free[w]);
 
             const int kb = j * kBN;
-            const bool masked = (kb + kBN > L) || (a.causal && kb + kBN - 1 > row0);
+            const bool masked = (kb + kBN > kv_total) || (a.causal && kb + kBN - 1 > start + row0);
             // The row max is taken on the raw scores (scale > 0) with eight independent 3-input max
             // chains; p = exp2(s * scale_log2 - m) is then one FFMA and one MUFU per score.
             float mul = scale_log2;
@@ -241,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mul = 1.f;
             }
             if (masked) {
-                const int lim = (a.causal ? min(L, qrow + 1) : L) - kb;  // keys kb + [0, lim) are visible
+                const int lim = (a.causal ? min(kv_total, start + qrow + 1) : kv_total) - kb;  // keys kb + [0, lim)
 #pragma unroll
                 for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? s[c] : kNegInf;
             }
@@ -351,8 +423,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-cudaError_t prefill_pp_launch(const PrefillArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
-                              const CUtensorMap& tv, cudaStream_t stream) {
+namespace {
+
+template <bool kPaged>
+cudaError_t launch_pp(const PrefillArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                      cudaStream_t stream) {
     if (a.G % 2 != 0) return cudaErrorInvalidValue;  // heads are taken in pairs of one KV group
     const int kmax = (a.max_seqlen + kBM - 1) / kBM;
     const long long tiles_ub = (long long)(a.T + kBM - 1) / kBM + a.N;
@@ -367,18 +442,30 @@ cudaError_t prefill_pp_launch(const PrefillArgs& a, const CUtensorMap& tq, const
     if (dev >= 64 || !regs_ok[dev]) {
         // The register split (setmaxnreg) must fit in what the block is launched with.
         cudaFuncAttributes fa;
-        if ((e = cudaFuncGetAttributes(&fa, prefill_pp_kernel)) != cudaSuccess) return e;
+        if ((e = cudaFuncGetAttributes(&fa, prefill_pp_kernel<kPaged>)) != cudaSuccess) return e;
         if ((long long)fa.numRegs * kThreads < 128ll * kProducerRegs + 256ll * kSoftmaxRegs)
             return cudaErrorInvalidConfiguration;
         if (dev < 64) regs_ok[dev] = 1;
     }
     if (dev >= 64 || set_to[dev] < smem) {
-        e = cudaFuncSetAttribute(prefill_pp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        e = cudaFuncSetAttribute(prefill_pp_kernel<kPaged>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         if (dev < 64) set_to[dev] = smem;
     }
-    prefill_pp_kernel<<<(unsigned)grid, kThreads, smem, stream>>>(tq, tk, tv, a);
+    prefill_pp_kernel<kPaged><<<(unsigned)grid, kThreads, smem, stream>>>(tq, tk, tv, a);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t prefill_pp_launch(const PrefillArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                              const CUtensorMap& tv, cudaStream_t stream) {
+    return launch_pp<false>(a, tq, tk, tv, stream);
+}
+
+cudaError_t prefill_pp_paged_launch(const PrefillArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                                    const CUtensorMap& tv, cudaStream_t stream) {
+    return launch_pp<true>(a, tq, tk, tv, stream);
 }
 
 }  // namespace sinkattn

@@ -54,20 +54,6 @@ struct __align__(1024) Smem {
     uint32_t tmem_base;
 };
 
-// Paged cache: TMA row of page pg (the pg-th page of sequence seq, KV head kvh) in the 2-D map over
-// the page pool; a page past the cache end (or past the page-table row) and a page id outside the
-// pool get a row past the pool's end, which the copy fills with zeros.
-__device__ __forceinline__ int paged_tile_row(const PrefillArgs& a, int seq, int kvh, int pg, int kv_total) {
-    const int oob = a.num_pages * a.Hkv * kPageSize;
-    if (pg >= a.max_pages || pg * kPageSize >= kv_total) return oob;
-    const int pid = __ldg(&a.page_table[(long long)seq * a.max_pages + pg]);
-    if (pid < 0 || pid >= a.num_pages) {
-        atomicOr(a.err, kErrBadPage);
-        return oob;
-    }
-    return (pid * a.Hkv + kvh) * kPageSize;
-}
-
 // kPaged: K and V come from the page pool through page_table, the new tokens of a sequence sit at
 // cache positions start_pos .. start_pos + L - 1 and see the whole cached prefix.
 template <bool kPaged>
@@ -162,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     if (lane == 0) got = mbar_wait(&empty[st], ((j / stages) - 1) & 1);
                     if (!(ok = __shfl_sync(0xffffffffu, got, 0) != 0)) break;
                 }
-                const int row = paged_tile_row(a, seq, kvh, j * (kBN / kPageSize) + (lane & 7), kv_total);
+                const int row = page_tile_row(a, seq, kvh, j * (kBN / kPageSize) + (lane & 7), kv_total);
                 if (lane == 0) mbar_arrive_expect_tx(&full[st], kTileBytes);
                 __syncwarp();
                 uint8_t* tile = is_k ? sm.k[st] : sm.v[st];

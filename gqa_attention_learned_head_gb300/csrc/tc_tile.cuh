@@ -75,6 +75,22 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         : "memory");
 }
 
+// Paged cache: TMA row of page pg of request / sequence `seq` and KV head kvh in the 2-D map over the
+// page pool (rows of 64 elements, a (page, KV head) slice = 16 rows).  A page past the cache end
+// (kv_len tokens) or past the page-table row, and a page id outside the pool, give a row past the
+// pool's end, which the copy fills with zeros; an id outside the pool is also reported.
+template <class Args>
+__device__ __forceinline__ int page_tile_row(const Args& a, int seq, int kvh, int pg, int kv_len) {
+    const int oob = a.num_pages * a.Hkv * kPageSize;
+    if (pg >= a.max_pages || pg * kPageSize >= kv_len) return oob;
+    const int pid = __ldg(&a.page_table[(long long)seq * a.max_pages + pg]);
+    if (pid < 0 || pid >= a.num_pages) {
+        atomicOr(a.err, kErrBadPage);
+        return oob;
+    }
+    return (pid * a.Hkv + kvh) * kPageSize;
+}
+
 // Every lane waits (bounded); true only if every lane saw the phase complete.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
     return __all_sync(0xffffffffu, mbar_wait(bar, parity));

@@ -112,19 +112,6 @@ struct __align__(1024) Smem {
     Piece piece[4];      // ... and their current pieces
 };
 
-// TMA row of page pg of segment (b, g) in the 2-D map over the page pool; a page past the cache
-// end and a page id outside the pool give a row past the pool's end, which the copy fills with zeros.
-__device__ __forceinline__ int page_row(const VerifyArgs& a, int b, int g, int pg, int kv_len) {
-    const int oob = a.num_pages * a.Hkv * kPageSize;
-    if (pg >= a.max_pages || pg * kPageSize >= kv_len) return oob;
-    const int pid = __ldg(&a.page_table[(long long)b * a.max_pages + pg]);
-    if (pid < 0 || pid >= a.num_pages) {
-        atomicOr(a.err, kErrBadPage);
-        return oob;
-    }
-    return (pid * a.Hkv + g) * kPageSize;
-}
-
 __device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 // Log-sum-exp merge of segment seg from its pieces' partials (base-2 lse), by the 128 softmax threads:
@@ -369,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                         if (lane == 0) got = mbar_wait(&empty[st], ((J / stages) - 1) & 1);
                         if (!(ok = __shfl_sync(0xffffffffu, got, 0) != 0)) break;
                     }
-                    const int row = page_row(a, pc.b, pc.g, t * kPagesPerTile + (lane & 7), pc.kv_len);
+                    const int row = page_tile_row(a, pc.b, pc.g, t * kPagesPerTile + (lane & 7), pc.kv_len);
                     if (lane == 0) mbar_arrive_expect_tx(&full[st], kTileBytes);
                     __syncwarp();
                     uint8_t* tile = is_k ? sm.k[st] : sm.v[st];

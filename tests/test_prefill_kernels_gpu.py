@@ -33,6 +33,18 @@ for Hq, Hkv, lens, causal in cases:
     assert S.sinkattn_get_error() == 0
     ro, rl = oracle.prefill(inp.q, inp.k, inp.v, inp.cu_seqlens, inp.sinks, inp.scale, inp.causal)
     assert_parity(out.float().cpu().numpy(), lse.cpu().numpy(), ro, rl, f"Hq={Hq} Hkv={Hkv} lens={lens} causal={causal}")
+# the chunked prefill over pages (the mma.sync choice falls back to the one-head tcgen05 kernel there)
+for Hq, Hkv in ((64, 8), (6, 2)):
+    inp = W.make_paged_prefill(Hq, Hkv, [0, 300, 1000], [40, 129, 300], seed=Hq)
+    g = inp.to("cuda")
+    S.sinkattn_kv_append(g.k_new, g.v_new, g.cu_seqlens, g.start_pos, g.page_table, g.k_pages, g.v_pages)
+    out, lse = S.sinkattn_prefill_paged(g.q, g.k_pages, g.v_pages, g.page_table, g.cu_seqlens, g.start_pos, g.sinks,
+                                        g.scale, max_seqlen=inp.max_seqlen)
+    assert S.sinkattn_get_error() == 0
+    kb, vb = oracle.kv_append(inp.k_new, inp.v_new, inp.cu_seqlens, inp.start_pos, inp.page_table, inp.k_pages,
+                              inp.v_pages)
+    ro, rl = oracle.prefill_paged(inp.q, kb, vb, inp.page_table, inp.cu_seqlens, inp.start_pos, inp.sinks, inp.scale)
+    assert_parity(out.float().cpu().numpy(), lse.cpu().numpy(), ro, rl, f"paged Hq={Hq} Hkv={Hkv}")
 print("ok")
 """
 
