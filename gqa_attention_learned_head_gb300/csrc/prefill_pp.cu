@@ -74,10 +74,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     int* order_ints = reinterpret_cast<int*>(&sm + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    TileOrder<kThreads> order;
-    order.build_warp0(order_ints, a.cu_seqlens, a.N, a.T, a.max_seqlen, kBM, a.err);
+    SeqOrder order;
+    order.build_warp0(order_ints, a.cu_seqlens, kPaged ? a.start_pos : nullptr, a.N, a.T, a.max_seqlen, kBM, a.err);
     __syncthreads();
-    order.finish_warp0_build();
+    order.finish_build();
     const int npairs = a.Hq >> 1;
     const int idx = (int)(blockIdx.x / npairs), h0 = 2 * (int)(blockIdx.x % npairs);
     if (idx >= order.total) return;  // whole CTA: no tile left
@@ -429,11 +429,10 @@ template <bool kPaged>
 cudaError_t launch_pp(const PrefillArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                       cudaStream_t stream) {
     if (a.G % 2 != 0) return cudaErrorInvalidValue;  // heads are taken in pairs of one KV group
-    const int kmax = (a.max_seqlen + kBM - 1) / kBM;
     const long long tiles_ub = (long long)(a.T + kBM - 1) / kBM + a.N;
     const long long grid = tiles_ub * (a.Hq / 2);
     if (grid > 0x7fffffffll) return cudaErrorInvalidConfiguration;
-    const size_t smem = 1024 + sizeof(Smem) + tile_order_smem_ints(a.N, kmax) * sizeof(int);
+    const size_t smem = 1024 + sizeof(Smem) + seq_order_smem_ints(a.N) * sizeof(int);
     static thread_local size_t set_to[64] = {};
     static thread_local int regs_ok[64] = {};  // 0 unknown, 1 checked
     int dev = 0;

@@ -65,10 +65,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     int* order_ints = reinterpret_cast<int*>(&sm + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    TileOrder<kThreads> order;
-    order.build_warp0(order_ints, a.cu_seqlens, a.N, a.T, a.max_seqlen, kBM, a.err);
+    SeqOrder order;
+    order.build_warp0(order_ints, a.cu_seqlens, kPaged ? a.start_pos : nullptr, a.N, a.T, a.max_seqlen, kBM, a.err);
     __syncthreads();
-    order.finish_warp0_build();
+    order.finish_build();
     const int idx = (int)(blockIdx.x / a.Hq), h = (int)(blockIdx.x % a.Hq);
     if (idx >= order.total) return;  // whole CTA: no tile left
     int seq, qt;
@@ -400,11 +400,10 @@ namespace {
 template <bool kPaged>
 cudaError_t launch(const PrefillArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                    cudaStream_t stream) {
-    const int kmax = (a.max_seqlen + kBM - 1) / kBM;
     const long long tiles_ub = (long long)(a.T + kBM - 1) / kBM + a.N;
     const long long grid = tiles_ub * a.Hq;
     if (grid > 0x7fffffffll) return cudaErrorInvalidConfiguration;
-    const size_t smem = 1024 + sizeof(Smem) + tile_order_smem_ints(a.N, kmax) * sizeof(int);
+    const size_t smem = 1024 + sizeof(Smem) + seq_order_smem_ints(a.N) * sizeof(int);
     static thread_local size_t set_to[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

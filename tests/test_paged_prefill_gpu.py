@@ -45,6 +45,21 @@ def test_small_shapes(S, Hq, Hkv, prefix, new):
     assert_parity(out, lse, ro, rl, f"Hq={Hq} Hkv={Hkv} prefix={prefix} new={new}")
 
 
+@pytest.mark.parametrize("N", [40, 140])
+@pytest.mark.parametrize("Hq,Hkv", [(8, 2), (6, 2)])
+def test_many_sequences(S, N, Hq, Hkv):
+    """Batches ranked by cached prefix + new tokens (40 sequences) and past the ranked limit (140,
+    index order); prefixes and new lengths repeat, so equal weights occur."""
+    rng = np.random.default_rng(N + Hq)
+    prefix = rng.choice([0, 5, 16, 200, 700], size=N).tolist()
+    new = rng.choice([1, 30, 128, 129], size=N).tolist()
+    inp = W.make_paged_prefill(Hq, Hkv, prefix, new, seed=N + Hq)
+    g, out, lse, err, kb, vb = append_and_prefill(S, inp)
+    assert err == 0
+    ro, rl = oracle.prefill_paged(inp.q, kb, vb, inp.page_table, inp.cu_seqlens, inp.start_pos, inp.sinks, inp.scale)
+    assert_parity(out, lse, ro, rl, f"N={N} Hq={Hq} Hkv={Hkv}")
+
+
 def test_no_prefix_equals_plain_prefill(S):
     """start_pos = 0: the paged prefill is the causal prefill of the new tokens."""
     inp = W.make_paged_prefill(16, 2, [0, 0, 0], [200, 1, 129], seed=51)

@@ -55,6 +55,19 @@ def test_empty_sequences_in_batch(S):
     assert_parity(out, lse, *ref(inp), "empty sequences")
 
 
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("N", [33, 128, 129, 300])
+@pytest.mark.parametrize("Hq,Hkv", [(8, 2), (6, 2)])
+def test_many_sequences(S, causal, N, Hq, Hkv):
+    """Batches ranked four keys per lane (33..128 sequences) and past the ranked limit (index order);
+    lengths repeat and include 0, so ties and empty sequences occur in the order."""
+    lens = np.random.default_rng(N).choice([0, 1, 17, 64, 129, 200], size=N).tolist()
+    inp = W.make_prefill(Hq, Hkv, lens, seed=N + Hq, causal=causal)
+    out, lse, err = run(S, inp)
+    assert err == 0
+    assert_parity(out, lse, *ref(inp), f"N={N} causal={causal} Hq={Hq} Hkv={Hkv}")
+
+
 def sampled_rows(inp, n, seed):
     rng = np.random.default_rng(seed)
     cu = inp.cu_seqlens.tolist()
