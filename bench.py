@@ -361,104 +361,6 @@ def pipelined_ms(api, ins, outs, K, warmup, stream):
     return t0.elapsed_time(t1) / K
 
 
-def graph_ms(step, n, reps, stream, flush=None):
-    """Per-call ms of n calls captured back to back in one CUDA graph and replayed `reps` times (the
-    host's launch overhead stripped).  With `flush`, every call is preceded by the L2 flush inside the
-    graph, and the time of a graph of n flushes alone is subtracted."""
-    def capture(body):
-        g = torch.cuda.CUDAGraph()
-        torch.cuda.synchronize()
-        with torch.cuda.graph(g, stream=stream):
-            for _ in range(n):
-                body()
-        torch.cuda.synchronize()
-        return g
-
-    def per_call(g):
-        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            g.replay()
-            torch.cuda.synchronize()
-            t0.record(stream)
-            for _ in range(reps):
-                g.replay()
-            t1.record(stream)
-        torch.cuda.synchronize()
-        return t0.elapsed_time(t1) / (reps * n)
-
-    if flush is None:
-        return per_call(capture(step))
-
-    def both():
-        flush()
-        step()
-
-    return per_call(capture(both)) - per_call(capture(flush))
-
-
-class Staging:
-    """Tensors packed back to back (each at a 256-byte offset) in one pinned host buffer and one
-    device buffer, so that a step's inputs (or results) cross to the other side in one copy."""
-
-    def __init__(self, specs):
-        offs, off = [], 0
-        for shape, dtype in specs:
-            off = (off + 255) & ~255
-            offs.append(off)
-            off += math.prod(shape) * torch.empty(0, dtype=dtype).element_size()
-        self.nbytes = off
-        self.host = torch.empty(off, dtype=torch.uint8).pin_memory()
-        self.dev = torch.empty(off, dtype=torch.uint8, device="cuda")
-
-        def views(buf):
-            return [buf[o:o + math.prod(sh) * torch.empty(0, dtype=dt).element_size()].view(dt).view(sh)
-                    for o, (sh, dt) in zip(offs, specs)]
-
-        self.h, self.d = views(self.host), views(self.dev)
-
-    def to_device(self):
-        self.dev.copy_(self.host, non_blocking=True)
-
-    def to_host(self):
-        self.host.copy_(self.dev, non_blocking=True)
-
-
-def pipelined_ms(api, ins, outs, K, warmup, stream):
-    """Mean ms per step of a double-buffered loop through the public API: the inputs of step i go up
-    on one copy stream, step i runs on `stream`, its results come back on another copy stream;
-    slot i % 2 is reused only after step i - 2 has released it.  The K timed steps form one region
-    (from the first upload to the last download)."""
-    up, down = torch.cuda.Stream(), torch.cuda.Stream()
-    n = warmup + K
-    ev_in = [torch.cuda.Event() for _ in range(n)]
-    ev_run = [torch.cuda.Event() for _ in range(n)]
-    ev_out = [torch.cuda.Event() for _ in range(n)]
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    for i in range(n):
-        if i == warmup:
-            torch.cuda.synchronize()
-            t0.record(up)
-        slot = i % 2
-        with torch.cuda.stream(up):
-            if i >= 2:
-                up.wait_event(ev_run[i - 2])  # step i - 2 has read this slot's inputs
-            ins[slot].to_device()
-            ev_in[i].record(up)
-        with torch.cuda.stream(stream):
-            stream.wait_event(ev_in[i])
-            if i >= 2:
-                stream.wait_event(ev_out[i - 2])  # this slot's previous results are on the host
-            api(ins[slot].d, outs[slot].d)
-            ev_run[i].record(stream)
-        with torch.cuda.stream(down):
-            down.wait_event(ev_run[i])
-            outs[slot].to_host()
-            ev_out[i].record(down)
-    t1.record(down)
-    torch.cuda.synchronize()
-    return t0.elapsed_time(t1) / K
-
-
 # ----------------------------------------------------------------------------- workloads
 
 def decode_bytes(kv_lens, Hkv, D=64):
