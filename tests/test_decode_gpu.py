@@ -147,6 +147,16 @@ def test_empty_batch(S):
     assert out.shape == (0, 8, 64) and S.sinkattn_get_error() == 0
 
 
+def test_maximum_batch(S):
+    """32768 requests, the most a decode call takes (the per-CTA page prefix fills 128 KB of shared
+    memory); cache lengths 0..40, so empty requests and partial pages occur throughout."""
+    lens = np.random.default_rng(32768).integers(0, 41, 32768).tolist()
+    inp = W.make_decode(32768, 8, 2, lens, seed=9)
+    out, lse, err = run(S, inp)
+    assert err == 0
+    assert_parity(out, lse, *ref(inp), "32768 requests")
+
+
 def test_one_million_token_request(S):
     """Maximum-size case: a 2^20-token request (65536 pages, 2 GiB of K/V) beside a 5-token one; every
     head of both requests against the oracle (inputs drawn on the device, copied to the host)."""

@@ -60,6 +60,18 @@ def test_many_sequences(S, N, Hq, Hkv):
     assert_parity(out, lse, ro, rl, f"N={N} Hq={Hq} Hkv={Hkv}")
 
 
+def test_maximum_sequence_count(S):
+    """16384 sequences (the most a paged prefill call takes), 0..20 cached and 1..3 new tokens each."""
+    rng = np.random.default_rng(16383)
+    prefix = rng.integers(0, 21, 16384).tolist()
+    new = rng.integers(1, 4, 16384).tolist()
+    inp = W.make_paged_prefill(8, 2, prefix, new, seed=12)
+    g, out, lse, err, kb, vb = append_and_prefill(S, inp)
+    assert err == 0
+    ro, rl = oracle.prefill_paged(inp.q, kb, vb, inp.page_table, inp.cu_seqlens, inp.start_pos, inp.sinks, inp.scale)
+    assert_parity(out, lse, ro, rl, "16384 sequences")
+
+
 def test_no_prefix_equals_plain_prefill(S):
     """start_pos = 0: the paged prefill is the causal prefill of the new tokens."""
     inp = W.make_paged_prefill(16, 2, [0, 0, 0], [200, 1, 129], seed=51)

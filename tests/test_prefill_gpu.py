@@ -68,6 +68,18 @@ def test_many_sequences(S, causal, N, Hq, Hkv):
     assert_parity(out, lse, *ref(inp), f"N={N} causal={causal} Hq={Hq} Hkv={Hkv}")
 
 
+def test_maximum_sequence_count(S):
+    """16384 sequences, the most a prefill call takes: the tile order runs in index order from its
+    largest table.  Lengths 0..3 with 40 sequences of 130 (two tiles, the second ragged)."""
+    rng = np.random.default_rng(16384)
+    lens = rng.choice([0, 1, 2, 3], size=16384)
+    lens[rng.choice(16384, 40, replace=False)] = 130
+    inp = W.make_prefill(8, 2, lens.tolist(), seed=5)
+    out, lse, err = run(S, inp)
+    assert err == 0
+    assert_parity(out, lse, *ref(inp), "16384 sequences")
+
+
 def sampled_rows(inp, n, seed):
     rng = np.random.default_rng(seed)
     cu = inp.cu_seqlens.tolist()

@@ -105,6 +105,16 @@ def test_bad_page_is_skipped_and_reported(S):
     assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
 
 
+def test_maximum_batch(S):
+    """32768 requests of 2 drafted tokens (the most a verification call takes): the share search
+    walks the requests in many passes; cache lengths 2..40."""
+    lens = np.random.default_rng(32767).integers(2, 41, 32768).tolist()
+    inp = W.make_decode(32768, 8, 2, lens, seed=10, q_len=2)
+    out, lse, err = run(S, inp)
+    assert err == 0
+    assert_parity(out, lse, *ref(inp), "32768 requests")
+
+
 def test_speculative_verify_full_size_sampled(S):
     """Full-size workload in the launch configuration the benchmark times; 96 sampled rows."""
     inp = W.speculative_verify()
