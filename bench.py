@@ -1042,26 +1042,40 @@ def run_ours(args):
 
 
 def bench_mixed(S, W, rank, K, Wu, flush, hbm_peak, tc_peak):
-    """Prefill and decode halves of the mixed batch on two streams; time vs t* = bytes/BW + flops/peak."""
+    """Prefill and decode halves of the mixed batch on two streams; time vs t* = bytes/BW + flops/peak.
+    Schedule: the decode goes first with two shares per SM, then the prefill with share_sms (the
+    one-head kernel), so every SM runs two decode CTAs beside one prefill CTA -- the HBM-bound half
+    beside the tensor-bound one.  With the default kernels each half fills whole SMs and the two run
+    one after the other (reported as serial_ms)."""
     pre = W.mixed_serving_prefill(device="cuda", seed=rank)
     dec = W.mixed_serving_decode(device="cuda", seed=rank)
     s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
-    ws = torch.empty(S.sinkattn_decode_workspace_size(dec.q, dec.k_pages, dec.page_table), dtype=torch.uint8,
+    workers = 2 * torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    ws = torch.empty(S.sinkattn_decode_workspace_size(dec.q, dec.k_pages, dec.page_table, workers), dtype=torch.uint8,
                      device="cuda")
+    ws_auto = torch.empty(S.sinkattn_decode_workspace_size(dec.q, dec.k_pages, dec.page_table), dtype=torch.uint8,
+                          device="cuda")
     po, dout = torch.empty_like(pre.q), torch.empty_like(dec.q)
     main = torch.cuda.current_stream()
 
     def step():
         s1.wait_stream(main)
         s2.wait_stream(main)
-        S.sinkattn_prefill(pre.q, pre.k, pre.v, pre.cu_seqlens, pre.sinks, pre.scale, True,
-                           max_seqlen=pre.max_seqlen, out=po, return_lse=False, stream=s1)
         S.sinkattn_decode(dec.q, dec.k_pages, dec.v_pages, dec.page_table, dec.kv_lens, dec.sinks, dec.scale,
-                          out=dout, return_lse=False, workspace=ws, stream=s2)
+                          out=dout, return_lse=False, workspace=ws, num_workers=workers, stream=s2)
+        S.sinkattn_prefill(pre.q, pre.k, pre.v, pre.cu_seqlens, pre.sinks, pre.scale, True,
+                           max_seqlen=pre.max_seqlen, out=po, return_lse=False, share_sms=True, stream=s1)
         main.wait_stream(s1)
         main.wait_stream(s2)
 
+    def serial():  # the default kernels, one after the other
+        S.sinkattn_decode(dec.q, dec.k_pages, dec.v_pages, dec.page_table, dec.kv_lens, dec.sinks, dec.scale,
+                          out=dout, return_lse=False, workspace=ws_auto, stream=main)
+        S.sinkattn_prefill(pre.q, pre.k, pre.v, pre.cu_seqlens, pre.sinks, pre.scale, True,
+                           max_seqlen=pre.max_seqlen, out=po, return_lse=False, stream=main)
+
     times = timed_steps(step, K, Wu, flush, main)
+    serial_times = timed_steps(serial, K, Wu, flush, main)
     if S.sinkattn_get_error(main):
         raise RuntimeError("device error in mixed batch")
     ms = statistics.mean(times)
@@ -1070,7 +1084,9 @@ def bench_mixed(S, W, rank, K, Wu, flush, hbm_peak, tc_peak):
     t_star = nbytes / (hbm_peak * 1e9) + flops / (tc_peak * 1e12)
     return {"workload": WORKLOAD_TEXT["mixed_serving"], "value": ms, "unit": "ms", "higher_is_better": False,
             "t_star_ms": t_star * 1e3, "frac_of_t_star": t_star * 1e3 / ms, "decode_bytes": nbytes,
-            "prefill_flops": flops}
+            "prefill_flops": flops, "serial_ms": statistics.mean(serial_times),
+            "schedule": f"decode first with {workers} shares (two per SM), then the prefill with share_sms "
+                        "(one-head kernel) on a second stream; serial_ms = the default kernels one after the other"}
 
 
 def main():

@@ -75,7 +75,8 @@ unsigned long long next_epoch() {
 }
 
 // Which prefill kernel runs.  By default the two-head tcgen05 kernel when the query-head group
-// size is even, else the one-head tcgen05 kernel.  SINKATTN_PREFILL_KERNEL=tc forces the one-head
+// size is even and the caller does not ask to share the SMs (dims share_sms), else the one-head
+// tcgen05 kernel.  SINKATTN_PREFILL_KERNEL=tc forces the one-head
 // kernel and =mma the warp-level mma.sync kernel (kept as the measured baseline only; the paged
 // prefill has no mma.sync form and runs the one-head kernel then).
 enum class PrefillKernel { kAuto, kOneHead, kLegacy };
@@ -165,6 +166,7 @@ sinkattn_status_t check_paged_dims(const sinkattn_paged_dims_t* d, bool need_q_h
         d->max_pages < 1)
         return SINKATTN_ERR_INVALID_ARG;
     if (need_q_heads && (d->num_q_heads <= 0 || d->num_q_heads % d->num_kv_heads)) return SINKATTN_ERR_INVALID_ARG;
+    if (need_q_heads && d->share_sms != 0 && d->share_sms != 1) return SINKATTN_ERR_INVALID_ARG;
     if (d->head_dim != kHeadDim || d->page_size != kPageSize) return SINKATTN_ERR_UNSUPPORTED;
     if (d->num_seqs > 16384 || d->max_seqlen > (1 << 20)) return SINKATTN_ERR_UNSUPPORTED;
     if ((long long)d->num_pages * d->num_kv_heads * kPageSize >= (1ll << 31)) return SINKATTN_ERR_UNSUPPORTED;
@@ -456,7 +458,7 @@ sinkattn_status_t sinkattn_prefill_paged(const void* q, const void* k_pages, con
     a.num_pages = d.num_pages;
     a.max_pages = d.max_pages;
     // the two-head kernel for an even query-head group (unless the one-head kernel is forced)
-    const bool two_head = a.G % 2 == 0 && prefill_kernel_choice() == PrefillKernel::kAuto;
+    const bool two_head = a.G % 2 == 0 && !d.share_sms && prefill_kernel_choice() == PrefillKernel::kAuto;
     const cudaError_t e = two_head ? prefill_pp_paged_launch(a, tq, tk, tv, static_cast<cudaStream_t>(stream))
                                    : prefill_paged_launch(a, tq, tk, tv, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? SINKATTN_OK : SINKATTN_ERR_CUDA;
@@ -522,6 +524,7 @@ sinkattn_status_t sinkattn_prefill(const void* q, const void* k, const void* v, 
         d.num_q_heads % d.num_kv_heads)
         return SINKATTN_ERR_INVALID_ARG;
     if (d.head_dim != kHeadDim) return SINKATTN_ERR_UNSUPPORTED;
+    if (d.share_sms != 0 && d.share_sms != 1) return SINKATTN_ERR_INVALID_ARG;
     if (d.num_seqs > 16384 || d.max_seqlen > (1 << 20)) return SINKATTN_ERR_UNSUPPORTED;
     if (d.num_seqs == 0 || d.total_tokens == 0 || d.max_seqlen == 0) return SINKATTN_OK;
     if (!q || !k || !v || !cu_seqlens || !sinks || !out) return SINKATTN_ERR_INVALID_ARG;
@@ -562,7 +565,7 @@ sinkattn_status_t sinkattn_prefill(const void* q, const void* k, const void* v, 
             !encode_thd(&tk, k, d.total_tokens, d.num_kv_heads, 128) ||
             !encode_thd(&tv, v, d.total_tokens, d.num_kv_heads, 128))
             return SINKATTN_ERR_INVALID_ARG;
-        e = (which == PrefillKernel::kAuto && a.G % 2 == 0)
+        e = (which == PrefillKernel::kAuto && a.G % 2 == 0 && !d.share_sms)
                 ? prefill_pp_launch(a, tq, tk, tv, static_cast<cudaStream_t>(stream))
                 : prefill_tc_launch(a, tq, tk, tv, static_cast<cudaStream_t>(stream));
     }

@@ -43,7 +43,7 @@ class VerifyDims(ctypes.Structure):
 
 class PagedDims(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("num_seqs", "total_tokens", "max_seqlen", "num_q_heads", "num_kv_heads",
-                                              "head_dim", "page_size", "num_pages", "max_pages")]
+                                              "head_dim", "page_size", "num_pages", "max_pages", "share_sms")]
 
 
 class RopeParams(ctypes.Structure):
@@ -54,7 +54,7 @@ class RopeParams(ctypes.Structure):
 
 class PrefillDims(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("num_seqs", "total_tokens", "max_seqlen", "num_q_heads",
-                                              "num_kv_heads", "head_dim")]
+                                              "num_kv_heads", "head_dim", "share_sms")]
 
 
 class MergeDims(ctypes.Structure):
@@ -253,10 +253,10 @@ def sinkattn_verify_tree(q, k_pages, v_pages, page_table, kv_lens, tree_mask, si
     return out, lse
 
 
-def paged_dims(k_pages, page_table, cu_seqlens, total_tokens, max_seqlen, num_q_heads=0) -> PagedDims:
+def paged_dims(k_pages, page_table, cu_seqlens, total_tokens, max_seqlen, num_q_heads=0, share_sms=False) -> PagedDims:
     P, Hkv, PS, D = k_pages.shape
     return PagedDims(cu_seqlens.shape[0] - 1, total_tokens, max_seqlen, num_q_heads, Hkv, D, PS, P,
-                     page_table.shape[1])
+                     page_table.shape[1], int(bool(share_sms)))
 
 
 def sinkattn_kv_append(k, v, cu_seqlens, start_pos, page_table, k_pages, v_pages, max_seqlen=0, stream=None):
@@ -305,9 +305,10 @@ def sinkattn_qkv_prologue(qkv, bias, cu_seqlens, start_pos, page_table, k_pages,
 
 
 def sinkattn_prefill_paged(q, k_pages, v_pages, page_table, cu_seqlens, start_pos, sinks, scale, max_seqlen=None,
-                           out=None, lse=None, return_lse=True, stream=None):
+                           out=None, lse=None, return_lse=True, stream=None, share_sms=False):
     """Chunked prefill of new tokens q [T, Hq, 64] over the paged cache (their K/V already appended):
-    new token i of sequence n sees cache tokens 0 .. start_pos[n] + i.  Returns (out, lse)."""
+    new token i of sequence n sees cache tokens 0 .. start_pos[n] + i.  Returns (out, lse).
+    ``share_sms`` as in sinkattn_prefill."""
     _need(q, "q", torch.bfloat16, 3)
     _need(k_pages, "k_pages", torch.bfloat16, 4)
     _need(v_pages, "v_pages", torch.bfloat16, 4)
@@ -318,7 +319,7 @@ def sinkattn_prefill_paged(q, k_pages, v_pages, page_table, cu_seqlens, start_po
     if max_seqlen is None:
         raise ValueError("max_seqlen is required (an upper bound of the new tokens per sequence)")
     T, Hq, D = q.shape
-    dims = paged_dims(k_pages, page_table, cu_seqlens, T, max_seqlen, Hq)
+    dims = paged_dims(k_pages, page_table, cu_seqlens, T, max_seqlen, Hq, share_sms)
     if out is None:
         out = torch.empty_like(q)
     if lse is None and return_lse:
@@ -331,8 +332,10 @@ def sinkattn_prefill_paged(q, k_pages, v_pages, page_table, cu_seqlens, start_po
 
 
 def sinkattn_prefill(q, k, v, cu_seqlens, sinks, scale, causal=True, max_seqlen=None, out=None, lse=None,
-                     return_lse=True, stream=None):
-    """Packed varlen prefill.  ``max_seqlen`` (an upper bound of the lengths) is required."""
+                     return_lse=True, stream=None, share_sms=False):
+    """Packed varlen prefill.  ``max_seqlen`` (an upper bound of the lengths) is required.  ``share_sms``
+    picks the kernel that leaves room on every SM for a decode launched just before it on another
+    stream with two shares per SM."""
     _need(q, "q", torch.bfloat16, 3)
     _need(k, "k", torch.bfloat16, 3)
     _need(v, "v", torch.bfloat16, 3)
@@ -343,7 +346,7 @@ def sinkattn_prefill(q, k, v, cu_seqlens, sinks, scale, causal=True, max_seqlen=
     T, Hq, D = q.shape
     if k.shape != v.shape or k.shape[0] != T or sinks.shape[0] != Hq:
         raise ValueError("inconsistent prefill shapes")
-    dims = PrefillDims(cu_seqlens.shape[0] - 1, T, int(max_seqlen), Hq, k.shape[1], D)
+    dims = PrefillDims(cu_seqlens.shape[0] - 1, T, int(max_seqlen), Hq, k.shape[1], D, int(bool(share_sms)))
     if out is None:
         out = torch.empty_like(q)
     if lse is None and return_lse:

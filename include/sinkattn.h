@@ -72,6 +72,15 @@ typedef struct {
     int32_t num_q_heads;       /* Hq                                                     */
     int32_t num_kv_heads;      /* Hkv; Hq % Hkv == 0                                     */
     int32_t head_dim;          /* must be 64                                             */
+    int32_t share_sms;         /* 0: the fastest kernel for a prefill that has the GPU to
+                                  itself (two query heads per CTA, a whole SM each, when
+                                  Hq / Hkv is even); 1: a kernel that leaves room on every
+                                  SM for another kernel on another stream (one head per CTA,
+                                  two CTAs per SM at 32 K registers, ~100 KB of shared
+                                  memory and 256 TMEM columns each), so that a decode
+                                  launched just before it with two shares per SM
+                                  (num_workers = 2 x SMs) runs beside it; other values:
+                                  SINKATTN_ERR_INVALID_ARG                              */
 } sinkattn_prefill_dims_t;
 
 /* Sizes of a merge call. */
@@ -207,6 +216,8 @@ typedef struct {
     int32_t page_size;         /* must be 16                                              */
     int32_t num_pages;         /* P, pages in the K/V pools                               */
     int32_t max_pages;         /* row length of page_table (>= 1)                         */
+    int32_t share_sms;         /* sinkattn_prefill_paged only: as in sinkattn_prefill_dims_t
+                                  (0 or 1; the other calls ignore it)                      */
 } sinkattn_paged_dims_t;
 
 /*

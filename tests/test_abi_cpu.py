@@ -66,6 +66,9 @@ def test_host_validation_without_device(S):
     p = S.PrefillDims(-1, 10, 10, 8, 2, 64)
     assert lib.sinkattn_prefill(None, None, None, None, None, 0.1, 1, None, None, ctypes.byref(p), None) == \
         S.ERR_INVALID_ARG
+    p = S.PrefillDims(1, 10, 10, 8, 2, 64, 2)  # share_sms is 0 or 1
+    assert lib.sinkattn_prefill(None, None, None, None, None, 0.1, 1, None, None, ctypes.byref(p), None) == \
+        S.ERR_INVALID_ARG
     m = S.MergeDims(2, 4, 0, 64)
     assert lib.sinkattn_merge(None, None, None, None, None, ctypes.byref(m), None) == S.ERR_INVALID_ARG
     assert lib.sinkattn_merge(None, None, None, None, None, None, None) == S.ERR_INVALID_ARG
@@ -96,6 +99,8 @@ def test_paged_host_validation_without_device(S):
     assert lib.sinkattn_prefill_paged(*([None] * 7), 0.125, None, None, ctypes.byref(d), None) == S.ERR_INVALID_ARG
     d = S.PagedDims(2, 10, 8, 8, 2, 64, 16, 10, 0)  # max_pages 0
     assert lib.sinkattn_kv_append(*([None] * 7), ctypes.byref(d), None) == S.ERR_INVALID_ARG
+    d = S.PagedDims(2, 10, 8, 8, 2, 64, 16, 10, 4, 3)  # share_sms is 0 or 1
+    assert lib.sinkattn_prefill_paged(*([None] * 7), 0.125, None, None, ctypes.byref(d), None) == S.ERR_INVALID_ARG
     d = S.PagedDims(0, 0, 0, 8, 2, 64, 16, 10, 4)  # nothing to do
     assert lib.sinkattn_kv_append(*([None] * 7), ctypes.byref(d), None) == 0
     assert lib.sinkattn_prefill_paged(*([None] * 7), 0.125, None, None, ctypes.byref(d), None) == 0

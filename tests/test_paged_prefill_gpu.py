@@ -72,6 +72,20 @@ def test_maximum_sequence_count(S):
     assert_parity(out, lse, ro, rl, "16384 sequences")
 
 
+def test_share_sms_matches_oracle(S):
+    """The paged prefill's kernel that leaves room on every SM computes the same attention."""
+    inp = W.make_paged_prefill(64, 8, [300, 5, 1000], [40, 300, 17], seed=35)
+    g = inp.to("cuda")
+    S.sinkattn_kv_append(g.k_new, g.v_new, g.cu_seqlens, g.start_pos, g.page_table, g.k_pages, g.v_pages)
+    out, lse = S.sinkattn_prefill_paged(g.q, g.k_pages, g.v_pages, g.page_table, g.cu_seqlens, g.start_pos, g.sinks,
+                                        g.scale, max_seqlen=inp.max_seqlen, share_sms=True)
+    assert S.sinkattn_get_error() == 0
+    kb, vb = oracle.kv_append(inp.k_new, inp.v_new, inp.cu_seqlens, inp.start_pos, inp.page_table, inp.k_pages,
+                              inp.v_pages)
+    ro, rl = oracle.prefill_paged(inp.q, kb, vb, inp.page_table, inp.cu_seqlens, inp.start_pos, inp.sinks, inp.scale)
+    assert_parity(out.float().cpu().numpy(), lse.cpu().numpy(), ro, rl, "paged share_sms")
+
+
 def test_no_prefix_equals_plain_prefill(S):
     """start_pos = 0: the paged prefill is the causal prefill of the new tokens."""
     inp = W.make_paged_prefill(16, 2, [0, 0, 0], [200, 1, 129], seed=51)

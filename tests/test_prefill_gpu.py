@@ -80,6 +80,43 @@ def test_maximum_sequence_count(S):
     assert_parity(out, lse, *ref(inp), "16384 sequences")
 
 
+@pytest.mark.parametrize("causal", [True, False])
+def test_share_sms_matches_oracle(S, causal):
+    """The kernel that leaves room on every SM (share_sms) computes the same attention."""
+    inp = W.make_prefill(64, 8, [300, 5, 64, 1000, 129], seed=31, causal=causal)
+    g = inp.to("cuda")
+    out, lse = S.sinkattn_prefill(g.q, g.k, g.v, g.cu_seqlens, g.sinks, g.scale, causal, max_seqlen=inp.max_seqlen,
+                                  share_sms=True)
+    assert S.sinkattn_get_error() == 0
+    assert_parity(out.float().cpu().numpy(), lse.cpu().numpy(), *ref(inp), f"share_sms causal={causal}")
+
+
+def test_decode_and_prefill_side_by_side(S):
+    """A decode with two shares per SM and a prefill that shares the SMs, launched on two streams
+    at once (the mixed-batch schedule): both match the oracle."""
+    dec = W.make_decode(64, 64, 8, (256, 2048), seed=33)
+    pre = W.make_prefill(64, 8, [700, 1300, 90, 2048], seed=34)
+    gd, gp = dec.to("cuda"), pre.to("cuda")
+    workers = 2 * torch.cuda.get_device_properties(0).multi_processor_count
+    ws = torch.empty(S.sinkattn_decode_workspace_size(gd.q, gd.k_pages, gd.page_table, workers), dtype=torch.uint8,
+                     device="cuda")
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    main = torch.cuda.current_stream()
+    s1.wait_stream(main)
+    s2.wait_stream(main)
+    dout, dlse = S.sinkattn_decode(gd.q, gd.k_pages, gd.v_pages, gd.page_table, gd.kv_lens, gd.sinks, gd.scale,
+                                   workspace=ws, num_workers=workers, stream=s2)
+    pout, plse = S.sinkattn_prefill(gp.q, gp.k, gp.v, gp.cu_seqlens, gp.sinks, gp.scale, True,
+                                    max_seqlen=pre.max_seqlen, share_sms=True, stream=s1)
+    main.wait_stream(s1)
+    main.wait_stream(s2)
+    torch.cuda.synchronize()
+    assert S.sinkattn_get_error() == 0
+    ro, rl = oracle.decode(dec.q, dec.k_pages, dec.v_pages, dec.page_table, dec.kv_lens, dec.sinks, dec.scale)
+    assert_parity(dout.float().cpu().numpy(), dlse.cpu().numpy(), ro, rl, "decode beside the prefill")
+    assert_parity(pout.float().cpu().numpy(), plse.cpu().numpy(), *ref(pre), "prefill beside the decode")
+
+
 def sampled_rows(inp, n, seed):
     rng = np.random.default_rng(seed)
     cu = inp.cu_seqlens.tolist()
