@@ -58,7 +58,7 @@ typedef struct {
     int32_t page_size;         /* must be 16                                             */
     int32_t num_pages;         /* P, pages in the K/V pools                              */
     int32_t max_pages;         /* row length of page_table (>= 1)                        */
-    int32_t num_workers;       /* 0 = automatic (one share per resident CTA: four per SM);
+    int32_t num_workers;       /* 0 = automatic (one share per resident CTA, up to four per SM);
                                   otherwise the number of equal shares the flattened
                                   (request, KV head, page) work is cut into, one CTA each.
                                   A request whose pages span several shares is split and
