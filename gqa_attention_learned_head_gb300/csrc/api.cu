@@ -246,8 +246,7 @@ sinkattn_status_t sinkattn_decode(const void* q, const void* k_pages, const void
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     a.part_o = reinterpret_cast<float*>(ws);
     a.part_lse = a.part_o + plan.slots * G * kHeadDim;
-    a.counters = reinterpret_cast<unsigned long long*>(ws + plan.counters_offset);
-    a.epoch = next_epoch();
+    a.merge_list = reinterpret_cast<int2*>(ws + plan.merge_list_offset);
     a.err = ds->err;
     a.B = dims->batch;
     a.Hq = dims->num_q_heads;
@@ -259,8 +258,13 @@ sinkattn_status_t sinkattn_decode(const void* q, const void* k_pages, const void
     a.min_pages_per_worker = plan.min_pages;
     a.fixed_workers = dims->num_workers > 0 ? 1 : 0;
     a.scale_log2 = scale * 1.4426950408889634f;
-    return decode_launch(a, plan, tk, tv, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SINKATTN_OK
-                                                                                            : SINKATTN_ERR_CUDA;
+    // One share (a fixed single worker, or an automatic split whose largest possible work,
+    // every request at max_pages, stays under the minimum share) cuts no segment.
+    const long long max_units = (long long)dims->batch * Hkv * dims->max_pages;
+    const bool may_split = plan.workers > 1 && (a.fixed_workers || max_units > plan.min_pages);
+    return decode_launch(a, plan, tk, tv, may_split, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? SINKATTN_OK
+               : SINKATTN_ERR_CUDA;
 }
 
 size_t sinkattn_verify_workspace_size(const sinkattn_verify_dims_t* dims) {

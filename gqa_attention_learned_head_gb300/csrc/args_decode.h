@@ -15,8 +15,8 @@ struct DecodeArgs {
     float* lse;                 // [B, Hq] or null
     float* part_o;              // [slots, G, 64]
     float* part_lse;            // [slots, G], base-2 log-sum-exp
-    unsigned long long* counters;  // [B*Hkv]: (call epoch << 24) | pieces arrived
-    unsigned long long epoch;      // this call's epoch, in [1, 2^40)
+    int2* merge_list;           // [grid]: (segment, pieces) whose page 0 the CTA holds, or (-1, 0);
+                                // null when no segment can be split (no merge kernel then)
     unsigned* err;              // device error word
     int B, Hq, Hkv, G, num_pages, max_pages;
     int workers;                // number of worker warps sharing the work
@@ -30,14 +30,16 @@ struct DecodePlan {
     int workers;         // worker warps
     int min_pages;       // automatic mode: never cut shares finer than this many pages
     size_t smem;         // dynamic shared memory of the split kernel
-    size_t slots;            // partial-result slots the workspace must hold
-    size_t counters_offset;  // byte offset of the per-segment arrival counters
-    size_t ws_bytes;         // workspace bytes
+    size_t slots;              // partial-result slots the workspace must hold
+    size_t merge_list_offset;  // byte offset of the per-CTA merge list
+    size_t ws_bytes;           // workspace bytes
 };
 
 // Plan the decode launch for the current device (no device memory touched).
 cudaError_t decode_plan(int B, int Hq, int Hkv, int num_workers, DecodePlan* plan);
+// may_split = false: the host knows that no segment can be cut (one share), so the merge kernel
+// is not launched.
 cudaError_t decode_launch(const DecodeArgs& args, const DecodePlan& plan, const CUtensorMap& tmap_k,
-                          const CUtensorMap& tmap_v, cudaStream_t stream);
+                          const CUtensorMap& tmap_v, bool may_split, cudaStream_t stream);
 
 }  // namespace sinkattn

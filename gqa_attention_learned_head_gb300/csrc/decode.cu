@@ -16,18 +16,22 @@
 //    knowledge of the lengths (no host sync; graph-capturable).  CTA c takes
 //    the contiguous share [c*U/C, (c+1)*U/C) of the U units: balanced to one
 //    page.  The share is cut at segment ends into "pieces".
-//  * A piece of >= 4 pages is spread over the CTA's 4 warps page by page
-//    (warp k takes pages k, k+4, ...); the warps then combine their online-
-//    softmax states in shared memory.  A shorter piece goes whole to one warp.
-//  * A piece that is a whole segment writes the final output.  Otherwise it
-//    writes an fp32 partial (o_c, lse_c) and bumps the segment's arrival
-//    counter; the CTA that completes a segment merges its partials by
-//    log-sum-exp (all 4 warps, at the end of its share) -- one kernel, no
-//    second launch.  Only the piece holding page 0 is seeded with the sink,
-//    so the sink is counted exactly once.  The counters carry the call's epoch
-//    in their high bits, so the workspace needs no zeroing, and the CTA that
-//    completes a segment resets its counter to 0, so replaying the same
-//    launch also works.
+//  * The warps of a CTA deal the pages of their share round robin, one page
+//    each in turn, and the turn carries on across piece boundaries, so every
+//    warp streams the same number of pages (+-1) however the share is cut.  A
+//    piece shorter than the warp count goes whole to the warp whose turn it is.
+//  * Piece ends need no CTA barrier: each warp drops its online-softmax state
+//    for the piece into one of two shared-memory slots and counts itself in;
+//    the last warp to arrive combines the states and writes the result while
+//    the others carry on streaming.
+//  * A piece that is a whole segment writes the final output.  Any other piece
+//    writes an fp32 partial (o_c, lse_c) into its slot of the workspace; the
+//    CTA holding a split segment's page 0 lists the segment, and a small merge
+//    kernel, launched as a programmatic dependent of this one (its launch
+//    overlaps this kernel; it waits for this grid to finish), combines the
+//    partials by log-sum-exp.  No CTA ever waits for another, and nothing in
+//    the workspace carries over between calls.  Only the piece holding page 0
+//    is seeded with the sink, so the sink is counted exactly once.
 //  * Each warp streams its pages through a private ring of kStages shared-
 //    memory stages.  One stage = the K and V slices of one (page, KV head):
 //    2 x 2 KiB, loaded by two TMA tensor copies with 128-byte swizzle (so the
@@ -50,20 +54,23 @@
 #ifndef SINKATTN_DECODE_MIN_BLOCKS
 #define SINKATTN_DECODE_MIN_BLOCKS 4
 #endif
+#ifndef SINKATTN_DECODE_WARPS
+#define SINKATTN_DECODE_WARPS 4
+#endif
 
 namespace sinkattn {
 namespace {
 
-constexpr int kWarps = 4;                        // warps per CTA
+constexpr int kWarps = SINKATTN_DECODE_WARPS;    // warps per CTA
 constexpr int kStages = SINKATTN_DECODE_STAGES;  // ring depth per warp
 constexpr int kSliceBytes = kPageSize * kHeadDim * 2;  // 2048: one (page, KV head) of K or V
 constexpr int kStageBytes = 2 * kSliceBytes;
-constexpr int kMaxMerge = 2;  // a share completes at most its first and its last segment
+constexpr int kMergeThreads = 256;  // merge kernel: 16 half-warps, one (segment, head) each
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kNegInf = -__builtin_huge_valf();
 
-// Shared memory: ring | mbarriers | bad-page flags | combine area | merge queue | prefix[B+1].
+// Shared memory: ring | mbarriers | bad-page flags | combine slots | slot words | scan | prefix[B+1].
 template <int NT>
 struct SmemLayout {
     static constexpr int kHeads = 8 * NT;
@@ -72,10 +79,9 @@ struct SmemLayout {
     static constexpr size_t bad = bars + size_t(kWarps) * kStages * 8;
     static constexpr size_t cmb_o = bad + size_t(kWarps) * kStages * 4;                   // [2][warps][heads][64] f32
     static constexpr size_t cmb_md = cmb_o + 2 * size_t(kWarps) * kHeads * kHeadDim * 4;  // [2][warps][heads] m, d
-    static constexpr size_t misc = cmb_md + 2 * size_t(kWarps) * kHeads * 8;              // scan scratch, counts
-    static constexpr size_t pend = misc + 8 * 4;                                          // partial pieces: <= 2
-    static constexpr size_t queue = pend + 2 * 4;
-    static constexpr size_t prefix = queue + kMaxMerge * 4;
+    static constexpr size_t slot = cmb_md + 2 * size_t(kWarps) * kHeads * 8;  // [2] arrivals, [2] generation
+    static constexpr size_t scan = slot + 4 * 4;                             // [kWarps] scan scratch
+    static constexpr size_t prefix = scan + kWarps * 4;
     static constexpr size_t fixed = prefix + 1024 /* alignment slack */;
 };
 
@@ -83,77 +89,50 @@ __device__ __forceinline__ uint32_t ld_u32(const __nv_bfloat16* p) {
     return __ldg(reinterpret_cast<const unsigned int*>(p));
 }
 
-__device__ __forceinline__ void cta_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory"); }
+__device__ __forceinline__ void allow_dependent_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void wait_for_prerequisite_grids() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
 
-// A piece as the decode processes it: one of >= kWarps pages is spread over the warps page by page.
+// A piece as the decode processes it.  `rot` is the warp whose turn it is at the piece's first
+// page (the deal carries on from the previous piece of the share).  A piece of >= kWarps pages
+// is dealt page by page from warp rot on; a shorter one goes whole to warp rot.
 struct Piece : SegPiece {
+    int rot;
     __device__ bool split() const { return len() >= kWarps; }
+    __device__ int offset(int w) const { return (w - rot + kWarps) % kWarps; }
     // Units of this piece that warp w processes, and the page of its t-th one.
     __device__ int count(int w) const {
-        if (split()) return len() > w ? (len() - w + kWarps - 1) / kWarps : 0;
-        return (idx % kWarps) == w ? len() : 0;
+        if (split()) {
+            const int o = offset(w);
+            return len() > o ? (len() - o + kWarps - 1) / kWarps : 0;
+        }
+        return rot == w ? len() : 0;
     }
-    __device__ int page(int w, int t) const { return page0() + (split() ? w + t * kWarps : t); }
+    __device__ int page(int w, int t) const { return page0() + (split() ? offset(w) + t * kWarps : t); }
+    __device__ void first(const int* prefix, int B, int Hkv, long long x0, long long x1) {
+        piece_first(*this, prefix, B, Hkv, x0, x1);
+        rot = 0;
+    }
+    __device__ void next(const int* prefix, int B, int Hkv, long long x1) {
+        rot = (rot + len()) % kWarps;
+        piece_next(*this, prefix, B, Hkv, x1);
+    }
 };
 
-// Log-sum-exp merge of one head of one segment from its partials (base-2 lse), by 16 lanes:
-// lane l of the half-warp owns head-dims 4l..4l+3.  Pieces are taken 8 at a time with all loads
-// issued together and combined online.
-__device__ __forceinline__ void merge_head(const DecodeArgs& a, int b, int g, int h, long long slot0, int pieces,
-                                           int hl) {
-    constexpr int kChunk = 8;
-    const int G = a.G;
-    const float* lp = a.part_lse + slot0 * G + h;
-    const float* op = a.part_o + (slot0 * G + h) * kHeadDim + 4 * hl;
-    float M = kNegInf, sum = 0.f;
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c0 = 0; c0 < pieces; c0 += kChunk) {
-        float l[kChunk];
-        float4 v[kChunk];
-#pragma unroll
-        for (int i = 0; i < kChunk; ++i) {
-            const bool in = c0 + i < pieces;
-            l[i] = in ? __ldcg(lp + (long long)(c0 + i) * G) : kNegInf;
-            v[i] = in ? __ldcg(reinterpret_cast<const float4*>(op + (long long)(c0 + i) * G * kHeadDim))
-                      : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        float Mc = M;
-#pragma unroll
-        for (int i = 0; i < kChunk; ++i) Mc = fmaxf(Mc, l[i]);
-        if (Mc == kNegInf) continue;
-        const float r = M == kNegInf ? 0.f : exp2f(M - Mc);
-        sum *= r;
-        o.x *= r;
-        o.y *= r;
-        o.z *= r;
-        o.w *= r;
-#pragma unroll
-        for (int i = 0; i < kChunk; ++i) {
-            const float w = l[i] == kNegInf ? 0.f : exp2f(l[i] - Mc);
-            sum += w;
-            o.x += w * v[i].x;
-            o.y += w * v[i].y;
-            o.z += w * v[i].z;
-            o.w += w * v[i].w;
-        }
-        M = Mc;
-    }
-    const long long row = (long long)b * a.Hq + g * G + h;
-    uint2* dst = reinterpret_cast<uint2*>(a.out + row * kHeadDim) + hl;
-    if (M == kNegInf) {  // no live key and no finite sink in any piece
-        *dst = make_uint2(0u, 0u);
-        if (hl == 0 && a.lse) a.lse[row] = kNegInf;
-        return;
-    }
-    const float inv = 1.f / sum;
-    *dst = make_uint2(pack_bf16(o.x * inv, o.y * inv), pack_bf16(o.z * inv, o.w * inv));
-    if (hl == 0 && a.lse) a.lse[row] = (M + log2f(sum)) * kLn2;
+// Bounded spin until a shared-memory word reaches `want`; false on give-up.
+__device__ __forceinline__ bool wait_word(const int* w, int want) {
+    for (uint32_t i = 0; i < kMaxPolls; ++i)
+        if (*reinterpret_cast<const volatile int*>(w) == want) return true;
+    return false;
 }
 
 template <int NT>  // NT = ceil(G / 8) groups of 8 query heads
-__global__ void __launch_bounds__(kWarps * 32, SINKATTN_DECODE_MIN_BLOCKS) decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                                                                   const __grid_constant__ CUtensorMap tmap_v,
-                                                                   const DecodeArgs a) {
+__global__ void __launch_bounds__(kWarps * 32, SINKATTN_DECODE_MIN_BLOCKS)
+    decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                        const DecodeArgs a) {
     using L = SmemLayout<NT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -161,13 +140,20 @@ __global__ void __launch_bounds__(kWarps * 32, SINKATTN_DECODE_MIN_BLOCKS) decod
     int* bad = reinterpret_cast<int*>(sm + L::bad);
     float* cmb_o = reinterpret_cast<float*>(sm + L::cmb_o);
     float* cmb_md = reinterpret_cast<float*>(sm + L::cmb_md);
-    int* misc = reinterpret_cast<int*>(sm + L::misc);  // [0..3] scan scratch, [4] merge queue, [6] pend count
-    int* pend = reinterpret_cast<int*>(sm + L::pend);    // segments of this share's partial pieces
-    int* queue = reinterpret_cast<int*>(sm + L::queue);  // segments this CTA completes and merges
+    int* slot_arr = reinterpret_cast<int*>(sm + L::slot);  // [2] warps counted in for the slot's piece
+    int* slot_gen = slot_arr + 2;                          // [2] pieces the slot has combined
+    int* scan = reinterpret_cast<int*>(sm + L::scan);
     int* prefix = reinterpret_cast<int*>(sm + L::prefix);  // [B + 1] exclusive prefix of pages per request
+
+    // Launched as a programmatic dependent of whatever precedes it on the stream: the launch
+    // overlaps that kernel's tail, and nothing is read before it has completed.  The merge kernel
+    // may be scheduled as soon as every CTA of this grid is running.
+    wait_for_prerequisite_grids();
+    allow_dependent_launch();
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int B = a.B, Hkv = a.Hkv, G = a.G, cap = a.max_pages * kPageSize;
+    const long long cta = blockIdx.x;
 
     // ---- 1. pages per request -> exclusive prefix sum (every CTA, in shared memory)
     int running = 0;
@@ -184,12 +170,12 @@ __global__ void __launch_bounds__(kWarps * 32, SINKATTN_DECODE_MIN_BLOCKS) decod
             int y = __shfl_up_sync(0xffffffffu, incl, o);
             if (lane >= o) incl += y;
         }
-        if (lane == 31) misc[warp] = incl;
+        if (lane == 31) scan[warp] = incl;
         __syncthreads();
         int woff = 0, tot = 0;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
-            int v = misc[w];
+            int v = scan[w];
             woff += (w < warp) ? v : 0;
             tot += v;
         }
@@ -199,7 +185,8 @@ __global__ void __launch_bounds__(kWarps * 32, SINKATTN_DECODE_MIN_BLOCKS) decod
     }
     if (tid == 0) {
         prefix[B] = running;
-        misc[4] = 0;
+        slot_arr[0] = slot_arr[1] = 0;
+        slot_gen[0] = slot_gen[1] = 0;
     }
     __syncthreads();
 
@@ -217,10 +204,11 @@ __global__ void __launch_bounds__(kWarps * 32, SINKATTN_DECODE_MIN_BLOCKS) decod
     }
 
     const long long U = (long long)running * Hkv;
-    if (U == 0) return;
-    const long long C = effective_shares(a.workers, a.fixed_workers, a.min_pages_per_worker, U);
-    const long long cta = blockIdx.x;
-    if (cta >= C) return;
+    const long long C = U > 0 ? effective_shares(a.workers, a.fixed_workers, a.min_pages_per_worker, U) : 0;
+    if (cta >= C) {
+        if (tid == 0 && a.merge_list) a.merge_list[cta] = make_int2(-1, 0);
+        return;
+    }
     const long long x0 = cta * U / C, x1 = (cta + 1) * U / C;
 
     uint8_t* my_ring = sm + warp * kStages * kStageBytes;
@@ -237,11 +225,11 @@ __global__ void __launch_bounds__(kWarps * 32, SINKATTN_DECODE_MIN_BLOCKS) decod
 
     // ---- 3. producer: walks this warp's units piece by piece; lanes resolve 32 page ids at a time
     Piece pp;
-    piece_first(pp, prefix, B, Hkv, x0, x1);
+    pp.first(prefix, B, Hkv, x0, x1);
     int pt = 0, pcnt = pp.count(warp), win_base = -64, win_row = -1, issued = 0;
     auto issue = [&]() -> bool {  // warp-uniform
         while (pt >= pcnt) {
-            piece_next(pp, prefix, B, Hkv, x1);
+            pp.next(prefix, B, Hkv, x1);
             if (pp.ps >= x1) return false;
             pt = 0;
             pcnt = pp.count(warp);
@@ -284,6 +272,8 @@ __global__ void __launch_bounds__(kWarps * 32, SINKATTN_DECODE_MIN_BLOCKS) decod
     float m[NT][2], d[NT][2];
     int consumed = 0;
     bool failed = false;  // a wait gave up: skip all further work, keep the barriers
+    int nsplit = 0;       // dealt pieces met so far (they take the combine slots in turn)
+    int head_seg = -1;    // segment whose page 0 this share holds without completing it
 
     // Per-piece inputs (query fragments, sink logits, cache length), fetched one piece ahead.
     struct PieceIn {
@@ -311,20 +301,21 @@ __global__ void __launch_bounds__(kWarps * 32, SINKATTN_DECODE_MIN_BLOCKS) decod
     };
     PieceIn cur, nxt;
     Piece cp;
-    piece_first(cp, prefix, B, Hkv, x0, x1);
+    cp.first(prefix, B, Hkv, x0, x1);
     fetch(cp, cur);
-    int pend_n = 0;  // partial pieces of this share (at most its first and its last), thread 0 only
 
-    for (int pidx = 0; cp.ps < x1; ++pidx) {
+    while (cp.ps < x1) {
         Piece np = cp;
-        piece_next(np, prefix, B, Hkv, x1);
+        np.next(prefix, B, Hkv, x1);
         if (np.ps < x1) fetch(np, nxt);  // in flight while this piece is processed
 
         const int cnt = cp.count(warp);
-        const bool first = cp.page0() == 0;                       // this piece holds the segment's page 0
-        const bool seeded = first && (!cp.split() || warp == 0);  // ... and this warp carries the sink
+        const bool first = cp.page0() == 0;  // this piece holds the segment's page 0
+        // ... and this warp carries the sink (for a dealt piece, warp 0: it always has a page)
+        const bool seeded = first && (cp.split() ? warp == 0 : cnt > 0);
         const int seg = cp.b * Hkv + cp.g;
         const bool whole = first && (cp.pe == cp.seg_start + cp.n);
+        if (first && !whole) head_seg = seg;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
@@ -440,7 +431,6 @@ __global__ void __launch_bounds__(kWarps * 32, SINKATTN_DECODE_MIN_BLOCKS) decod
                 for (int o = 4; o < 32; o <<= 1) d[nt][e] += __shfl_xor_sync(0xffffffffu, d[nt][e], o);
 
         const long long slot = cta + seg;  // partial slot of this piece
-        if (!whole && tid == 0) pend[pend_n++] = seg;  // counted at the end of the share
         if (!cp.split()) {
             if (cnt > 0) {
                 // one warp holds the whole piece: normalise and write
@@ -477,10 +467,17 @@ __global__ void __launch_bounds__(kWarps * 32, SINKATTN_DECODE_MIN_BLOCKS) decod
                 }
             }
         } else {
-            // ---- a split piece: combine the four warps' states in shared memory (double buffered,
-            // so one barrier per piece suffices)
-            float* co = cmb_o + (pidx & 1) * (kWarps * L::kHeads * kHeadDim);
-            float* cmd = cmb_md + (pidx & 1) * (kWarps * L::kHeads * 2);
+            // ---- a dealt piece: drop this warp's state into the piece's combine slot; the last
+            // warp to count itself in combines the states and writes the result
+            const int sl = nsplit & 1, gen = nsplit >> 1;
+            ++nsplit;
+            if (!wait_word(&slot_gen[sl], gen)) {  // the slot's previous piece is combined
+                failed = true;
+                if (lane == 0) atomicOr(a.err, kErrTimeout);
+            }
+            __threadfence_block();
+            float* co = cmb_o + sl * (kWarps * L::kHeads * kHeadDim);
+            float* cmd = cmb_md + sl * (kWarps * L::kHeads * 2);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
@@ -500,34 +497,79 @@ __global__ void __launch_bounds__(kWarps * 32, SINKATTN_DECODE_MIN_BLOCKS) decod
                     }
                 }
             }
-            cta_bar();
-            for (int h = warp; h < G; h += kWarps) {
-                float M = kNegInf;
-#pragma unroll
-                for (int w = 0; w < kWarps; ++w) M = fmaxf(M, cmd[(w * L::kHeads + h) * 2]);
-                float dt = 0.f, ox = 0.f, oy = 0.f;
-                if (M != kNegInf) {
+            __syncwarp();
+            int before = 0;
+            if (lane == 0) {
+                __threadfence_block();  // this warp's state is written before it counts itself in
+                before = atomicAdd(&slot_arr[sl], 1);
+                __threadfence_block();  // ... and the other warps' states are read after
+            }
+            before = __shfl_sync(0xffffffffu, before, 0);
+            __syncwarp();
+            if (before == kWarps - 1) {
+                // the lanes split the G x 64 outputs: kLanesPerHead lanes per head, each with a run
+                // of kDims consecutive head-dims, all loads of a run issued together
+                constexpr int kLanesPerHead = 32 / L::kHeads;       // 4 (NT = 1) or 2 (NT = 2)
+                constexpr int kDims = kHeadDim / kLanesPerHead;     // 16 or 32
+                const int h = lane / kLanesPerHead, d0 = (lane % kLanesPerHead) * kDims;
+                if (h < G) {
+                    float sw[kWarps], M = kNegInf;
 #pragma unroll
                     for (int w = 0; w < kWarps; ++w) {
-                        const float mw = cmd[(w * L::kHeads + h) * 2];
-                        const float sw = mw == kNegInf ? 0.f : fast_exp2(mw - M);
-                        const float2 v = reinterpret_cast<const float2*>(co + (w * L::kHeads + h) * kHeadDim)[lane];
-                        dt += sw * cmd[(w * L::kHeads + h) * 2 + 1];
-                        ox += sw * v.x;
-                        oy += sw * v.y;
+                        sw[w] = cmd[(w * L::kHeads + h) * 2];
+                        M = fmaxf(M, sw[w]);
+                    }
+                    float dt = 0.f;
+#pragma unroll
+                    for (int w = 0; w < kWarps; ++w) {
+                        sw[w] = (M == kNegInf || sw[w] == kNegInf) ? 0.f : fast_exp2(sw[w] - M);
+                        dt += sw[w] * cmd[(w * L::kHeads + h) * 2 + 1];
+                    }
+                    const float inv = dt > 0.f ? 1.f / dt : 0.f;
+                    const float l2 = dt > 0.f ? M + log2f(dt) : kNegInf;
+                    const long long row = (long long)cp.b * a.Hq + cp.g * G + h;
+#pragma unroll
+                    for (int part = 0; part < kDims / 8; ++part) {  // 8 head-dims at a time
+                        float acc[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll
+                        for (int w = 0; w < kWarps; ++w) {
+                            const float4* src =
+                                reinterpret_cast<const float4*>(co + (w * L::kHeads + h) * kHeadDim + d0 + 8 * part);
+                            const float4 v0 = src[0], v1 = src[1];
+                            acc[0] += sw[w] * v0.x;
+                            acc[1] += sw[w] * v0.y;
+                            acc[2] += sw[w] * v0.z;
+                            acc[3] += sw[w] * v0.w;
+                            acc[4] += sw[w] * v1.x;
+                            acc[5] += sw[w] * v1.y;
+                            acc[6] += sw[w] * v1.z;
+                            acc[7] += sw[w] * v1.w;
+                        }
+                        if (whole) {
+                            reinterpret_cast<uint4*>(a.out + row * kHeadDim + d0)[part] =
+                                make_uint4(pack_bf16(acc[0] * inv, acc[1] * inv), pack_bf16(acc[2] * inv, acc[3] * inv),
+                                           pack_bf16(acc[4] * inv, acc[5] * inv), pack_bf16(acc[6] * inv, acc[7] * inv));
+                        } else {
+                            float4* dst = reinterpret_cast<float4*>(a.part_o + (slot * G + h) * kHeadDim + d0 + 8 * part);
+                            dst[0] = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+                            dst[1] = make_float4(acc[4] * inv, acc[5] * inv, acc[6] * inv, acc[7] * inv);
+                        }
+                    }
+                    if (d0 == 0) {
+                        if (whole) {
+                            if (a.lse) a.lse[row] = l2 * kLn2;
+                        } else {
+                            a.part_lse[slot * G + h] = l2;
+                        }
                     }
                 }
-                const float inv = dt > 0.f ? 1.f / dt : 0.f;
-                const float l2 = dt > 0.f ? M + log2f(dt) : kNegInf;
-                if (whole) {
-                    const long long row = (long long)cp.b * a.Hq + cp.g * G + h;
-                    reinterpret_cast<__nv_bfloat162*>(a.out + row * kHeadDim)[lane] =
-                        __floats2bfloat162_rn(ox * inv, oy * inv);
-                    if (lane == 0 && a.lse) a.lse[row] = l2 * kLn2;
-                } else {
-                    reinterpret_cast<float2*>(a.part_o + (slot * G + h) * kHeadDim)[lane] =
-                        make_float2(ox * inv, oy * inv);
-                    if (lane == 0) a.part_lse[slot * G + h] = l2;
+                __syncwarp();
+                if (lane == 0) {  // free the slot for the piece after next
+                    slot_arr[sl] = 0;
+                    __threadfence_block();
+                    *reinterpret_cast<volatile int*>(&slot_gen[sl]) = gen + 1;
                 }
             }
         }
@@ -535,35 +577,88 @@ __global__ void __launch_bounds__(kWarps * 32, SINKATTN_DECODE_MIN_BLOCKS) decod
         if (cp.ps < x1) cur = nxt;
     }
 
-    if (tid == 0) misc[6] = pend_n;
     if (failed) {
         // let copies already in flight land (bounded) before the CTA's shared memory is released
         for (int j = consumed; j < issued; ++j) (void)mbar_wait(&my_bars[j % kStages], (j / kStages) & 1);
     }
 
-    // ---- 5. count this share's partial pieces (at most two); merge the segments it completes
-    __syncthreads();  // every partial of this CTA is written (CTA scope) ...
-    if (tid < 2 && tid < misc[6]) {  // ... and the release CAS publishes them device-wide
-        const int seg = pend[tid];
-        const int b = seg / Hkv, g = seg - b * Hkv;
-        const int n = prefix[b + 1] - prefix[b];
-        long long c_first;
-        int pieces;
-        segment_pieces((long long)prefix[b] * Hkv + (long long)g * n, n, C, U, c_first, pieces);
-        if (arrive_last(&a.counters[seg], a.epoch, pieces)) queue[atomicAdd(&misc[4], 1)] = seg;
+    // ---- 5. list the segment whose page 0 this share holds but does not complete: the merge
+    // kernel combines its pieces (slots cta + seg .. cta + pieces - 1 + seg)
+    if (tid == 0 && a.merge_list) {
+        int2 e = make_int2(-1, 0);
+        if (head_seg >= 0) {
+            const int b = head_seg / Hkv, g = head_seg - b * Hkv;
+            const int n = prefix[b + 1] - prefix[b];
+            long long c_first;
+            int pieces;
+            segment_pieces((long long)prefix[b] * Hkv + (long long)g * n, n, C, U, c_first, pieces);
+            e = make_int2(head_seg, pieces);
+        }
+        a.merge_list[cta] = e;
     }
-    __syncthreads();
-    const int nq = misc[4];
-    // (segment, head) items over half-warps: 8 per pass of the CTA
-    for (int item = warp * 2 + (lane >> 4); item < nq * G; item += kWarps * 2) {
-        const int seg = queue[item / G], h = item % G;
-        const int b = seg / Hkv, g = seg - b * Hkv;
-        const int n = prefix[b + 1] - prefix[b];
-        long long c_first;
-        int pieces;
-        segment_pieces((long long)prefix[b] * Hkv + (long long)g * n, n, C, U, c_first, pieces);
-        merge_head(a, b, g, h, c_first + seg, pieces, lane & 15);
+}
+
+// Log-sum-exp merge of the split segments: half-warp per (listed segment, query head); lane l of
+// the half-warp owns head-dims 4l..4l+3.  Pieces are taken 8 at a time with all loads issued
+// together and combined online (base-2 partial lse).  Waits for the decode grid before reading.
+__global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecodeArgs a, int listed) {
+    wait_for_prerequisite_grids();
+    allow_dependent_launch();  // the next kernel on the stream may start launching
+    constexpr int kChunk = 8;
+    const int G = a.G, hl = threadIdx.x & 15;
+    const long long item = (long long)blockIdx.x * (kMergeThreads / 16) + (threadIdx.x >> 4);
+    if (item >= (long long)listed * G) return;
+    const int c = (int)(item / G), h = (int)(item % G);
+    const int2 e = __ldcg(&a.merge_list[c]);
+    if (e.x < 0) return;
+    const int seg = e.x, pieces = e.y;
+    const long long slot0 = (long long)c + seg;
+    const float* lp = a.part_lse + slot0 * G + h;
+    const float* op = a.part_o + (slot0 * G + h) * kHeadDim + 4 * hl;
+    float M = kNegInf, sum = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c0 = 0; c0 < pieces; c0 += kChunk) {
+        float l[kChunk];
+        float4 v[kChunk];
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i) {
+            const bool in = c0 + i < pieces;
+            l[i] = in ? __ldcg(lp + (long long)(c0 + i) * G) : kNegInf;
+            v[i] = in ? __ldcg(reinterpret_cast<const float4*>(op + (long long)(c0 + i) * G * kHeadDim))
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float Mc = M;
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i) Mc = fmaxf(Mc, l[i]);
+        if (Mc == kNegInf) continue;
+        const float r = M == kNegInf ? 0.f : exp2f(M - Mc);
+        sum *= r;
+        o.x *= r;
+        o.y *= r;
+        o.z *= r;
+        o.w *= r;
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i) {
+            const float w = l[i] == kNegInf ? 0.f : exp2f(l[i] - Mc);
+            sum += w;
+            o.x += w * v[i].x;
+            o.y += w * v[i].y;
+            o.z += w * v[i].z;
+            o.w += w * v[i].w;
+        }
+        M = Mc;
     }
+    const int b = seg / a.Hkv, g = seg - b * a.Hkv;
+    const long long row = (long long)b * a.Hq + g * G + h;
+    uint2* dst = reinterpret_cast<uint2*>(a.out + row * kHeadDim) + hl;
+    if (M == kNegInf) {  // no live key and no finite sink in any piece
+        *dst = make_uint2(0u, 0u);
+        if (hl == 0 && a.lse) a.lse[row] = kNegInf;
+        return;
+    }
+    const float inv = 1.f / sum;
+    *dst = make_uint2(pack_bf16(o.x * inv, o.y * inv), pack_bf16(o.z * inv, o.w * inv));
+    if (hl == 0 && a.lse) a.lse[row] = (M + log2f(sum)) * kLn2;
 }
 
 template <int NT>
@@ -627,19 +722,39 @@ cudaError_t decode_plan(int B, int Hq, int Hkv, int num_workers, DecodePlan* pla
     plan->slots = (size_t)shares + (size_t)B * Hkv;
     size_t bytes = plan->slots * G * kHeadDim * 4;   // partial o
     bytes += plan->slots * G * 4;                    // partial lse (base 2)
-    plan->counters_offset = (bytes + 255) & ~size_t(255);
-    plan->ws_bytes = plan->counters_offset + (size_t)B * Hkv * sizeof(unsigned long long);
+    plan->merge_list_offset = (bytes + 255) & ~size_t(255);
+    plan->ws_bytes = plan->merge_list_offset + (size_t)shares * sizeof(int2);
     return cudaSuccess;
 }
 
 cudaError_t decode_launch(const DecodeArgs& args, const DecodePlan& plan, const CUtensorMap& tk,
-                          const CUtensorMap& tv, cudaStream_t stream) {
+                          const CUtensorMap& tv, bool may_split, cudaStream_t stream) {
     if (args.B == 0) return cudaSuccess;
-    if (args.G <= 8)
-        decode_split_kernel<1><<<plan.grid, kWarps * 32, plan.smem, stream>>>(tk, tv, args);
-    else
-        decode_split_kernel<2><<<plan.grid, kWarps * 32, plan.smem, stream>>>(tk, tv, args);
-    return cudaGetLastError();
+    DecodeArgs a = args;
+    if (!may_split) a.merge_list = nullptr;
+    // Both kernels are programmatic dependents of what precedes them on the stream (each waits,
+    // griddepcontrol.wait, for its predecessor to complete before reading anything), so a launch
+    // overlaps the tail of the kernel before it instead of starting after it.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)plan.grid);
+    cfg.blockDim = dim3(kWarps * 32);
+    cfg.dynamicSmemBytes = plan.smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = a.G <= 8 ? cudaLaunchKernelEx(&cfg, decode_split_kernel<1>, tk, tv, a)
+                             : cudaLaunchKernelEx(&cfg, decode_split_kernel<2>, tk, tv, a);
+    if (e != cudaSuccess || !may_split) return e;
+    // the merge: its CTAs are scheduled while the decode runs and wait for the decode grid to
+    // complete before they read its partials
+    const long long items = (long long)plan.grid * a.G;
+    cfg.gridDim = dim3((unsigned)((items + kMergeThreads / 16 - 1) / (kMergeThreads / 16)));
+    cfg.blockDim = dim3(kMergeThreads);
+    cfg.dynamicSmemBytes = 0;
+    return cudaLaunchKernelEx(&cfg, decode_merge_kernel, a, plan.grid);
 }
 
 }  // namespace sinkattn

@@ -86,6 +86,12 @@ __device__ __forceinline__ unsigned long long cas_acq_rel(unsigned long long* p,
     return old;
 }
 
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
 // Records one more finished piece of a segment; true for the piece that completes it.  The
 // compare-and-swap has release semantics (this CTA's partials, ordered before it by the CTA
 // barrier, become visible first) and acquire semantics (the other pieces' partials are visible

@@ -31,6 +31,20 @@ def test_header_declares_the_three_calls():
         assert fn in names
 
 
+def documented_functions():
+    """Entry points listed in the design document's boundary section (the paragraph that opens with
+    "Exported entry points")."""
+    text = (ROOT / "DESIGN.md").read_text()
+    para = text[text.index("Exported entry points"):]
+    para = para[:para.index("\n\n")]
+    para = para[para.index(":\n") + 2:]
+    return sorted(set(re.findall(r"`(sinkattn_\w+)`", para)))
+
+
+def test_documented_entry_points_match_the_header():
+    assert documented_functions() == declared_functions()
+
+
 def test_library_exports_every_declared_symbol(S):
     lib = ctypes.CDLL(S.library_path)
     for fn in declared_functions():

@@ -168,3 +168,47 @@ def test_one_million_token_request(S):
     del g
     ro, rl = ref(c)
     assert_parity(out, lse, ro, rl, "2^20-token request")
+
+
+def test_workspace_needs_no_initialisation(S):
+    """The caller's workspace may hold anything: random bytes give the same result as a fresh one."""
+    inp = W.make_decode(6, 64, 8, [300, 5000, 17, 0, 2048, 777], seed=11)
+    g = inp.to("cuda")
+    n = S.sinkattn_decode_workspace_size(g.q, g.k_pages, g.page_table, 40)
+    ws = torch.randint(0, 256, (n,), dtype=torch.uint8, device="cuda")
+    out, lse = S.sinkattn_decode(g.q, g.k_pages, g.v_pages, g.page_table, g.kv_lens, g.sinks, g.scale,
+                                 workspace=ws, num_workers=40)
+    assert S.sinkattn_get_error() == 0
+    assert_parity(out.float().cpu().numpy(), lse.cpu().numpy(), *ref(inp), "random workspace")
+
+
+def test_graph_replay_with_new_inputs(S):
+    """The decode (split kernel and its dependent merge) captured once in a CUDA graph and replayed
+    after the inputs in the same buffers changed: every replay matches the oracle on its inputs."""
+    a = W.make_decode(8, 64, 8, (512, 4096), seed=12)
+    b = W.make_decode(8, 64, 8, a.kv_lens.tolist(), seed=13)
+    b.page_table = a.page_table.clone()  # same lengths and pool size, other contents and layout
+    c = W.make_decode(8, 64, 8, a.kv_lens.tolist(), seed=14)
+    c.page_table = a.page_table.clone()
+    c.kv_lens = a.kv_lens // 3 + 1  # shorter caches: the split of the work moves
+    g = a.to("cuda")
+    out = torch.empty_like(g.q)
+    lse = torch.empty(g.q.shape[:2], dtype=torch.float32, device="cuda")
+    ws = torch.empty(S.sinkattn_decode_workspace_size(g.q, g.k_pages, g.page_table), dtype=torch.uint8,
+                     device="cuda")
+    stream = torch.cuda.Stream()
+    S.sinkattn_decode(g.q, g.k_pages, g.v_pages, g.page_table, g.kv_lens, g.sinks, g.scale, out=out, lse=lse,
+                      workspace=ws, stream=stream)  # warm-up outside the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        S.sinkattn_decode(g.q, g.k_pages, g.v_pages, g.page_table, g.kv_lens, g.sinks, g.scale, out=out, lse=lse,
+                          workspace=ws, stream=stream)
+    for src in (a, b, c, a):
+        for name in ("q", "k_pages", "v_pages", "kv_lens", "sinks"):
+            getattr(g, name).copy_(getattr(src, name))
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert S.sinkattn_get_error() == 0
+        assert_parity(out.float().cpu().numpy(), lse.cpu().numpy(), *ref(src), "graph replay")
