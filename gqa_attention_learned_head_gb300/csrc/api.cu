@@ -7,7 +7,6 @@
 
 #include <atomic>
 #include <chrono>
-#include <cstdlib>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -19,12 +18,19 @@ namespace {
 
 // One word per device (each device holds its own copy of a __device__ variable).
 __device__ unsigned g_error_word = 0;
+// Where sinkattn_get_error's exchange leaves the word it took (read back by the host).
+__device__ unsigned g_error_taken = 0;
+
+// Takes the error word and clears it in one atomic step, ordered on the caller's stream: a bit
+// that a kernel on another stream sets afterwards stays in the word for the next read.
+__global__ void take_error_kernel(unsigned* err, unsigned* taken) { *taken = atomicExch(err, 0u); }
 
 constexpr int kMaxDevices = 64;
 
 struct DeviceState {
     bool ready = false;
-    unsigned* err = nullptr;  // device address of g_error_word
+    unsigned* err = nullptr;    // device address of g_error_word
+    unsigned* taken = nullptr;  // device address of g_error_taken
 };
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -43,6 +49,8 @@ sinkattn_status_t device_state(DeviceState** out) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return SINKATTN_ERR_CUDA;
         s.err = static_cast<unsigned*>(p);
+        if (cudaGetSymbolAddress(&p, g_error_taken) != cudaSuccess) return SINKATTN_ERR_CUDA;
+        s.taken = static_cast<unsigned*>(p);
         if (!g_encode) {
             cudaDriverEntryPointQueryResult q;
             void* fn = nullptr;
@@ -72,31 +80,6 @@ unsigned long long next_epoch() {
         e = counter.fetch_add(1) & ((1ull << 40) - 1);
     } while (e == 0);
     return e;
-}
-
-// Which prefill kernel runs.  By default the two-head tcgen05 kernel when the query-head group
-// size is even and the caller does not ask to share the SMs (dims share_sms), else the one-head
-// tcgen05 kernel.  SINKATTN_PREFILL_KERNEL=tc forces the one-head
-// kernel and =mma the warp-level mma.sync kernel (kept as the measured baseline only; the paged
-// prefill has no mma.sync form and runs the one-head kernel then).
-enum class PrefillKernel { kAuto, kOneHead, kLegacy };
-PrefillKernel prefill_kernel_choice() {
-    static const PrefillKernel choice = [] {
-        const char* s = std::getenv("SINKATTN_PREFILL_KERNEL");
-        if (s && std::strcmp(s, "mma") == 0) return PrefillKernel::kLegacy;
-        if (s && std::strcmp(s, "tc") == 0) return PrefillKernel::kOneHead;
-        return PrefillKernel::kAuto;
-    }();
-    return choice;
-}
-
-// Which verification kernel runs: SINKATTN_VERIFY_KERNEL=tc the tcgen05 kernel, =mma the mma.sync
-// kernel, unset the library's choice (the tcgen05 kernel).  Read at every call.
-int verify_kernel_choice() {
-    const char* s = std::getenv("SINKATTN_VERIFY_KERNEL");
-    if (s && std::strcmp(s, "tc") == 0) return 1;
-    if (s && std::strcmp(s, "mma") == 0) return 0;
-    return -1;
 }
 
 // 3-D bf16 tensor map over q [tokens, H, 64] whose box is 64 x box_heads heads x box_tokens tokens
@@ -270,8 +253,8 @@ sinkattn_status_t sinkattn_decode(const void* q, const void* k_pages, const void
 size_t sinkattn_verify_workspace_size(const sinkattn_verify_dims_t* dims) {
     if (check_verify_dims(dims) != SINKATTN_OK) return 0;
     VerifyPlan plan;
-    if (verify_plan(dims->batch, dims->q_len, dims->num_q_heads, dims->num_kv_heads, dims->num_workers, -1,
-                    &plan) != cudaSuccess)
+    if (verify_plan(dims->batch, dims->q_len, dims->num_q_heads, dims->num_kv_heads, dims->num_workers, &plan) !=
+        cudaSuccess)
         return 0;
     return plan.ws_bytes;
 }
@@ -322,21 +305,14 @@ sinkattn_status_t verify_common(const void* q, const void* k_pages, const void* 
     if (!(scale == scale)) return SINKATTN_ERR_INVALID_ARG;
     DeviceState* ds = nullptr;
     if ((st = device_state(&ds)) != SINKATTN_OK) return st;
-    // The tcgen05 kernel fetches absent pages as zero-filled copies, which need a real tensor map:
-    // with an empty pool the mma.sync kernel runs (it issues no copy for an absent page).
-    const int choice = dims->num_pages == 0 ? 0 : verify_kernel_choice();
     VerifyPlan plan;
-    if (verify_plan(dims->batch, dims->q_len, dims->num_q_heads, dims->num_kv_heads, dims->num_workers, choice,
-                    &plan) != cudaSuccess)
+    if (verify_plan(dims->batch, dims->q_len, dims->num_q_heads, dims->num_kv_heads, dims->num_workers, &plan) !=
+        cudaSuccess)
         return SINKATTN_ERR_CUDA;
     if (!workspace || workspace_bytes < plan.ws_bytes || !aligned(workspace, 256)) return SINKATTN_ERR_WORKSPACE;
 
     const int Hkv = dims->num_kv_heads, G = dims->num_q_heads / Hkv;
-    // With an empty pool every page id is out of range, so no copy is ever issued
-    // and the (zeroed) maps are never read.
     CUtensorMap tk, tv;
-    std::memset(&tk, 0, sizeof tk);
-    std::memset(&tv, 0, sizeof tv);
     const unsigned long long rows = (unsigned long long)dims->num_pages * Hkv * kPageSize;
     if (rows > 0 &&
         (!encode_rows(&tk, k_pages, rows, 128, kPageSize) || !encode_rows(&tv, v_pages, rows, 128, kPageSize)))
@@ -364,21 +340,19 @@ sinkattn_status_t verify_common(const void* q, const void* k_pages, const void* 
     a.R = dims->q_len * G;
     a.num_pages = dims->num_pages;
     a.max_pages = dims->max_pages;
-    a.workers = plan.grid;
-    a.min_pages_per_worker = 0;  // set by the launcher
     a.fixed_workers = dims->num_workers > 0 ? 1 : 0;
     a.tc_grid = plan.tc_grid;
     a.scale_log2 = scale * 1.4426950408889634f;
-    cudaError_t e;
-    if (plan.tc) {
-        CUtensorMap tq;
-        if (!encode_token_groups(&tq, q, (long long)dims->batch * dims->q_len, dims->num_q_heads, (unsigned)G,
-                                 (unsigned)dims->q_len))
-            return SINKATTN_ERR_INVALID_ARG;
-        e = verify_tc_launch(a, tq, tk, tv, static_cast<cudaStream_t>(stream));
-    } else {
-        e = verify_launch(a, plan, tk, tv, static_cast<cudaStream_t>(stream));
-    }
+    // An empty pool has no page to copy (and no memory for a tensor map to describe): every
+    // cached token is absent, so every row is the sink's alone.
+    if (rows == 0)
+        return verify_empty_pool_launch(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SINKATTN_OK
+                                                                                           : SINKATTN_ERR_CUDA;
+    CUtensorMap tq;
+    if (!encode_token_groups(&tq, q, (long long)dims->batch * dims->q_len, dims->num_q_heads, (unsigned)G,
+                             (unsigned)dims->q_len))
+        return SINKATTN_ERR_INVALID_ARG;
+    const cudaError_t e = verify_tc_launch(a, tq, tk, tv, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? SINKATTN_OK : SINKATTN_ERR_CUDA;
 }
 }  // namespace
@@ -461,8 +435,8 @@ sinkattn_status_t sinkattn_prefill_paged(const void* q, const void* k_pages, con
     a.start_pos = start_pos;
     a.num_pages = d.num_pages;
     a.max_pages = d.max_pages;
-    // the two-head kernel for an even query-head group (unless the one-head kernel is forced)
-    const bool two_head = a.G % 2 == 0 && !d.share_sms && prefill_kernel_choice() == PrefillKernel::kAuto;
+    // the two-head kernel for an even query-head group (unless the caller shares the SMs)
+    const bool two_head = a.G % 2 == 0 && !d.share_sms;
     const cudaError_t e = two_head ? prefill_pp_paged_launch(a, tq, tk, tv, static_cast<cudaStream_t>(stream))
                                    : prefill_paged_launch(a, tq, tk, tv, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? SINKATTN_OK : SINKATTN_ERR_CUDA;
@@ -559,20 +533,16 @@ sinkattn_status_t sinkattn_prefill(const void* q, const void* k, const void* v, 
     a.page_table = nullptr;
     a.start_pos = nullptr;
     a.num_pages = a.max_pages = 0;
-    cudaError_t e;
-    const PrefillKernel which = prefill_kernel_choice();
-    if (which == PrefillKernel::kLegacy) {
-        e = prefill_mma_launch(a, static_cast<cudaStream_t>(stream));
-    } else {
-        CUtensorMap tq, tk, tv;
-        if (!encode_thd(&tq, q, d.total_tokens, d.num_q_heads, 128) ||
-            !encode_thd(&tk, k, d.total_tokens, d.num_kv_heads, 128) ||
-            !encode_thd(&tv, v, d.total_tokens, d.num_kv_heads, 128))
-            return SINKATTN_ERR_INVALID_ARG;
-        e = (which == PrefillKernel::kAuto && a.G % 2 == 0 && !d.share_sms)
-                ? prefill_pp_launch(a, tq, tk, tv, static_cast<cudaStream_t>(stream))
-                : prefill_tc_launch(a, tq, tk, tv, static_cast<cudaStream_t>(stream));
-    }
+    CUtensorMap tq, tk, tv;
+    if (!encode_thd(&tq, q, d.total_tokens, d.num_q_heads, 128) ||
+        !encode_thd(&tk, k, d.total_tokens, d.num_kv_heads, 128) ||
+        !encode_thd(&tv, v, d.total_tokens, d.num_kv_heads, 128))
+        return SINKATTN_ERR_INVALID_ARG;
+    // the two-head kernel for an even query-head group (unless the caller shares the SMs), else
+    // the one-head kernel
+    const cudaError_t e = (a.G % 2 == 0 && !d.share_sms)
+                              ? prefill_pp_launch(a, tq, tk, tv, static_cast<cudaStream_t>(stream))
+                              : prefill_tc_launch(a, tq, tk, tv, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? SINKATTN_OK : SINKATTN_ERR_CUDA;
 }
 
@@ -611,11 +581,15 @@ sinkattn_status_t sinkattn_get_error(void* stream) {
     sinkattn_status_t st = device_state(&ds);
     if (st != SINKATTN_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (cudaStreamSynchronize(s) != cudaSuccess) return SINKATTN_ERR_CUDA;
+    // one reader at a time per process: the exchange's destination word is shared
+    static std::mutex take_mu;
+    std::lock_guard<std::mutex> lock(take_mu);
     unsigned word = 0;
-    if (cudaMemcpyFromSymbol(&word, g_error_word, sizeof word) != cudaSuccess) return SINKATTN_ERR_CUDA;
-    const unsigned zero = 0;
-    if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof zero) != cudaSuccess) return SINKATTN_ERR_CUDA;
+    take_error_kernel<<<1, 1, 0, s>>>(ds->err, ds->taken);
+    if (cudaGetLastError() != cudaSuccess) return SINKATTN_ERR_CUDA;
+    if (cudaMemcpyAsync(&word, ds->taken, sizeof word, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return SINKATTN_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SINKATTN_ERR_CUDA;
     for (int code = 1; code < 32; ++code)
         if (word & (1u << code)) return static_cast<sinkattn_status_t>(code);
     return SINKATTN_OK;

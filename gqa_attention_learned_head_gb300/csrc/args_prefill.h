@@ -34,7 +34,5 @@ cudaError_t prefill_paged_launch(const PrefillArgs& args, const CUtensorMap& tma
 // The same over two query heads of one KV group per CTA (group size must be even).
 cudaError_t prefill_pp_paged_launch(const PrefillArgs& args, const CUtensorMap& tmap_q, const CUtensorMap& tmap_k,
                                     const CUtensorMap& tmap_v, cudaStream_t stream);
-// Warp-level mma.sync prefill, kept as the legacy-tensor-path baseline.
-cudaError_t prefill_mma_launch(const PrefillArgs& args, cudaStream_t stream);
 
 }  // namespace sinkattn

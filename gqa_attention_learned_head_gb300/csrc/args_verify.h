@@ -21,24 +21,21 @@ struct VerifyArgs {
     unsigned long long epoch;      // this call's epoch, in [1, 2^40)
     unsigned* err;
     int B, QL, Hq, Hkv, G, R, num_pages, max_pages;  // R = QL * G rows per segment
-    int workers, min_pages_per_worker, fixed_workers;  // the mma.sync kernel's split
-    long long tc_grid;  // the tcgen05 kernel's shares (one CTA each); fixed_workers: exactly that many
+    int fixed_workers;  // 1: exactly tc_grid shares (the caller's num_workers)
+    long long tc_grid;  // shares of the (request, KV head, 128-key tile) units, one CTA each
     float scale_log2;
 };
 struct VerifyPlan {
-    bool tc;  // the tcgen05 kernel runs (else the mma.sync kernel)
-    int grid, warps, stages;  // mma.sync kernel
-    long long tc_grid;  // tcgen05 kernel: shares
-    size_t smem, slots, counters_offset, ws_bytes;  // workspace: enough for either kernel
+    long long tc_grid;                       // shares (CTAs)
+    size_t slots, counters_offset, ws_bytes;  // workspace: partials per slot, then a counter per segment
 };
-// use_tc: -1 = the library's choice, 0 = the mma.sync kernel, 1 = the tcgen05 kernel
-cudaError_t verify_plan(int B, int QL, int Hq, int Hkv, int num_workers, int use_tc, VerifyPlan* plan);
-cudaError_t verify_launch(const VerifyArgs& args, const VerifyPlan& plan, const CUtensorMap& tmap_k,
-                          const CUtensorMap& tmap_v, cudaStream_t stream);
-// tcgen05 kernel (verify_tc.cu); tmap_q covers q as [B * q_len tokens, Hq, 64] with a box of
-// 64 x G heads x q_len tokens.
+cudaError_t verify_plan(int B, int QL, int Hq, int Hkv, int num_workers, VerifyPlan* plan);
+// tmap_q covers q as [B * q_len tokens, Hq, 64] with a box of 64 x G heads x q_len tokens.
 cudaError_t verify_tc_occupancy(int* per_sm);
 cudaError_t verify_tc_launch(const VerifyArgs& args, const CUtensorMap& tmap_q, const CUtensorMap& tmap_k,
                              const CUtensorMap& tmap_v, cudaStream_t stream);
+// An empty page pool: every request's cached tokens are absent (out = 0, lse = sink); a request
+// with kv_len > 0 raises the bad-page error, one outside [0, max_pages * 16] the bad-length one.
+cudaError_t verify_empty_pool_launch(const VerifyArgs& args, cudaStream_t stream);
 
 }  // namespace sinkattn

@@ -662,7 +662,31 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 }
 
+// An empty pool: one thread per (request, drafted token, query head) row writes out = 0 and
+// lse = sink (every cached token is absent); the first row of a request checks its length.
+__global__ void __launch_bounds__(256) verify_empty_pool_kernel(const VerifyArgs a) {
+    const long long rows = (long long)a.B * a.QL * a.Hq;
+    const long long r = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= rows) return;
+    uint4* dst = reinterpret_cast<uint4*>(a.out + r * kHeadDim);
+#pragma unroll
+    for (int c = 0; c < kHeadDim / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+    if (a.lse) a.lse[r] = __ldg(&a.sinks[r % a.Hq]);
+    if (r % ((long long)a.QL * a.Hq) == 0) {
+        const int L = __ldg(&a.kv_lens[r / ((long long)a.QL * a.Hq)]);
+        if (L < 0 || L > a.max_pages * kPageSize) atomicOr(a.err, kErrBadLength);
+        else if (L > 0) atomicOr(a.err, kErrBadPage);
+    }
+}
+
 }  // namespace
+
+cudaError_t verify_empty_pool_launch(const VerifyArgs& a, cudaStream_t stream) {
+    const long long rows = (long long)a.B * a.QL * a.Hq;
+    if (rows == 0) return cudaSuccess;
+    verify_empty_pool_kernel<<<(unsigned)((rows + 255) / 256), 256, 0, stream>>>(a);
+    return cudaGetLastError();
+}
 
 size_t verify_tc_smem() { return 1024 + sizeof(Smem); }
 
@@ -696,6 +720,25 @@ cudaError_t verify_tc_occupancy(int* per_sm) {
     if (n < 1) return cudaErrorInvalidConfiguration;
     if (dev < 64) cached[dev] = n;
     *per_sm = n;
+    return cudaSuccess;
+}
+
+cudaError_t verify_plan(int B, int QL, int Hq, int Hkv, int num_workers, VerifyPlan* plan) {
+    const int G = Hq / Hkv, R = QL * G;
+    // one share of the (request, KV head, 128-key tile) units per resident slot (num_workers > 0:
+    // that many shares)
+    int per_sm = 0, sms = 0, dev = 0;
+    cudaError_t e;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = verify_tc_occupancy(&per_sm)) != cudaSuccess) return e;
+    const long long segs = (long long)B * Hkv;
+    plan->tc_grid = num_workers > 0 ? num_workers : (long long)sms * (per_sm > 0 ? per_sm : 1);
+    plan->slots = (size_t)plan->tc_grid + (size_t)segs;  // partial slot = share + segment
+    size_t bytes = plan->slots * R * kHeadDim * 4;       // partial o
+    bytes += plan->slots * R * 4;                        // partial lse (base 2)
+    plan->counters_offset = (bytes + 255) & ~size_t(255);
+    plan->ws_bytes = plan->counters_offset + (size_t)segs * sizeof(unsigned long long);
     return cudaSuccess;
 }
 

@@ -390,9 +390,12 @@ sinkattn_status_t sinkattn_decode_noalloc(const void *q, const void *k_pages, co
                                           const sinkattn_decode_dims_t *dims, void *stream);
 
 /*
- * Synchronises `stream`, then returns and clears the current device's error
- * word (SINKATTN_OK when no kernel reported a problem).  If several problems
- * were recorded, the one with the lowest status code is returned.
+ * Takes and clears the current device's error word in one atomic step ordered
+ * on `stream` (after everything enqueued on it before), synchronises `stream`
+ * and returns what it took (SINKATTN_OK when no kernel reported a problem).
+ * If several problems were recorded, the one with the lowest status code is
+ * returned.  A problem raised by a kernel on another stream after the step
+ * stays in the word for the next call.
  */
 sinkattn_status_t sinkattn_get_error(void *stream);
 

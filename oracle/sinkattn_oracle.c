@@ -25,7 +25,7 @@
  * space.  With J empty, out = 0 and lse = sig; with J empty and sig = -inf,
  * out = 0 and lse = -inf.
  *
- * Readings taken where the page is silent (each is repeated in the design doc):
+ * Readings taken where the page is silent:
  *   - query head h reads key/value head h / (Hq / Hkv) (contiguous groups);
  *   - causal prefill: row i of a sequence sees keys 0..i of that sequence;
  *   - a paged cache of page size PS stores token t of request b in page

@@ -212,3 +212,13 @@ def test_graph_replay_with_new_inputs(S):
         torch.cuda.synchronize()
         assert S.sinkattn_get_error() == 0
         assert_parity(out.float().cpu().numpy(), lse.cpu().numpy(), *ref(src), "graph replay")
+
+
+def test_benchmark_draw_of_the_batched_workload(S):
+    """The exact bytes the benchmark times: the batched paged decode drawn on the device (seed 0,
+    the draw of rank 0), checked against the oracle on a host copy of the same inputs."""
+    g = W.batched_paged_decode(device="cuda", seed=0)
+    out, lse = S.sinkattn_decode(g.q, g.k_pages, g.v_pages, g.page_table, g.kv_lens, g.sinks, g.scale)
+    assert S.sinkattn_get_error() == 0
+    c = g.to("cpu")
+    assert_parity(out.float().cpu().numpy(), lse.cpu().numpy(), *ref(c), "benchmark draw")

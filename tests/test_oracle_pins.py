@@ -573,6 +573,25 @@ def test_yarn_ramp_orientation():
     assert abs(oracle.yarn_mscale(32.0) - (0.1 * math.log(32.0) + 1.0)) < 1e-15
 
 
+def test_yarn_ramp_interior_value():
+    """One dimension inside the ramp, worked by hand from the YaRN method's definition (the ramp is
+    a linear function of r, the number of turns a pair makes over the original context).
+
+    theta = 150000, s = 32, L = 4096, beta_fast = 32, beta_slow = 1, pair d = 16 of 32:
+      theta_16 = 150000^(-32/64) = 1 / 387.2983...          = 2.5819888974716e-3
+      r_16     = 4096 * theta_16 / (2 pi)                    = 1.6831950685839
+      gamma    = (r_16 - 1) / (32 - 1)                       = 0.022038550599482
+      angle    = ((1 - gamma) / 32 + gamma) * theta_16      = 1.3581221810508e-4 per position
+    A ramp that is linear in the pair index between the (fractional) pairs where r = 32 and r = 1
+    (8.0928 and 17.3980) would give gamma = 0.150240 and 4.5648e-4 instead."""
+    inv = oracle.yarn_inv_freq(64, 150000.0, 32.0, 4096, 32.0, 1.0)
+    assert abs(inv[16] - 1.3581221810508e-4) <= 1e-15
+    assert abs(inv[16] - 4.5648e-4) > 1e-4  # the pair-index ramp is a different reading
+    # the two ramp ends bracket it: pair 14 is inside too, pair 18 already fully slowed
+    assert abs(inv[14] - 6.0249056412024e-4) <= 1e-15
+    assert abs(inv[18] - 1.2258819959601083e-3 / 32.0) <= 1e-18
+
+
 @pytest.mark.parametrize("interleaved", [False, True])
 def test_rope_invariants(interleaved):
     rng = np.random.default_rng(81)

@@ -18,14 +18,6 @@ def S():
     return sinkattn
 
 
-@pytest.fixture(autouse=True, params=["mma", "tc"])
-def kernel(request, monkeypatch):
-    """Every case runs on both verification kernels: the mma.sync one and the tcgen05 one (the
-    library reads SINKATTN_VERIFY_KERNEL at every call)."""
-    monkeypatch.setenv("SINKATTN_VERIFY_KERNEL", request.param)
-    return request.param
-
-
 def run(S, inp, **kw):
     g = inp.to("cuda")
     out, lse = S.sinkattn_verify(g.q, g.k_pages, g.v_pages, g.page_table, g.kv_lens, g.sinks, g.scale, **kw)
@@ -81,7 +73,7 @@ def test_short_caches_put_early_tokens_on_the_sink(S):
 
 
 def test_q_len_one_matches_decode(S):
-    """q_len = 1 is decode: both kernels against the same oracle rows."""
+    """q_len = 1 is decode: both calls against the same oracle rows."""
     inp = W.make_decode(5, 64, 8, (1, 900), seed=34, q_len=1)
     out, lse, err = run(S, inp)
     assert err == 0
@@ -210,7 +202,7 @@ def test_tree_verify_full_size_sampled(S):
 
 
 def test_bad_page_tokens_count_as_absent(S):
-    """A page id outside the pool: its tokens count as absent on both kernels -- the request's rows equal
+    """A page id outside the pool: its tokens count as absent -- the request's rows equal
     the oracle's on the same cache with that page's 16 tokens left out (the page lies before the draft,
     and visibility depends only on positions relative to the draft)."""
     inp = W.make_decode(2, 8, 2, [40, 40], seed=37, q_len=2)
@@ -225,3 +217,22 @@ def test_bad_page_tokens_count_as_absent(S):
     rows = np.array([[1, i, h] for i in range(2) for h in range(8)], dtype=np.int32)
     ro, rl = ref(ok, rows)
     assert_parity(out[1].reshape(-1, 64), lse[1].reshape(-1), ro, rl, "request with an absent page")
+
+
+def test_empty_pool(S):
+    """No page in the pool: every cached token is absent, so each row is the sink's alone (out = 0,
+    lse = sink); a request that claims cached tokens is reported as pointing outside the pool."""
+    Hq, Hkv, QL = 16, 2, 3
+    q = torch.randn(3, QL, Hq, 64, device="cuda").to(torch.bfloat16)
+    pages = torch.empty(0, Hkv, 16, 64, dtype=torch.bfloat16, device="cuda")
+    pt = torch.full((3, 2), -1, dtype=torch.int32, device="cuda")
+    sinks = torch.randn(Hq, device="cuda")
+    lens = torch.zeros(3, dtype=torch.int32, device="cuda")
+    out, lse = S.sinkattn_verify(q, pages, pages, pt, lens, sinks, 0.125)
+    assert S.sinkattn_get_error() == 0
+    assert bool((out == 0).all())
+    assert torch.equal(lse, sinks.expand(3, QL, Hq))
+    lens[1] = 20  # two pages' worth of tokens, none of them in the pool
+    out, lse = S.sinkattn_verify(q, pages, pages, pt, lens, sinks, 0.125)
+    assert S.sinkattn_get_error() == S.ERR_BAD_PAGE
+    assert bool((out == 0).all()) and torch.equal(lse, sinks.expand(3, QL, Hq))

@@ -45,6 +45,28 @@ def test_noalloc_decode_matches_regular_decode_on_two_calls_in_a_row():
                       "no-alloc decode vs sinkattn_decode")
 
 
+def test_noalloc_decode_allocates_nothing():
+    """After a warm-up call (which loads the kernels and looks up the scratch array), a call through
+    the binding and the C ABI changes neither the caching allocator's count of allocations nor the
+    device's free memory."""
+    from gqa_attention_learned_head_gb300 import sinkattn as S
+
+    g = W.make_decode(16, 64, 8, (300, 3000), seed=24).to("cuda")
+    out = torch.empty_like(g.q)
+    lse = torch.empty(g.q.shape[:2], dtype=torch.float32, device="cuda")
+    S.sinkattn_decode_noalloc(g.q, g.k_pages, g.v_pages, g.page_table, g.kv_lens, g.sinks, g.scale, out, lse)
+    torch.cuda.synchronize()
+    allocs = torch.cuda.memory_stats()["allocation.all.allocated"]
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(3):
+        S.sinkattn_decode_noalloc(g.q, g.k_pages, g.v_pages, g.page_table, g.kv_lens, g.sinks, g.scale, out, lse)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert torch.cuda.memory_stats()["allocation.all.allocated"] == allocs
+    assert free1 == free0
+    assert S.sinkattn_get_error() == 0
+
+
 def test_noalloc_decode_rejects_problems_above_the_scratch_limit():
     from gqa_attention_learned_head_gb300 import sinkattn as S
 
