@@ -3,10 +3,7 @@
 // error word that kernels report into instead of trapping.
 #include <sinkattn.h>
 
-#include <unistd.h>
 
-#include <atomic>
-#include <chrono>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -67,20 +64,6 @@ sinkattn_status_t device_state(DeviceState** out) {
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
-// Epoch of a decode call: unique within the process, never 0, below 2^40.  The start
-// is salted with the clock and the process id so that counters left in reused device
-// memory by another process are unlikely to carry a matching epoch.
-unsigned long long next_epoch() {
-    static std::atomic<unsigned long long> counter{
-        (static_cast<unsigned long long>(std::chrono::steady_clock::now().time_since_epoch().count()) ^
-         (static_cast<unsigned long long>(getpid()) << 20)) & ((1ull << 39) - 1)};
-    unsigned long long e;
-    do {
-        e = counter.fetch_add(1) & ((1ull << 40) - 1);
-    } while (e == 0);
-    return e;
-}
 
 // 3-D bf16 tensor map over q [tokens, H, 64] whose box is 64 x box_heads heads x box_tokens tokens
 // (the rows of one query-head group of several consecutive tokens), 128-byte swizzle.
@@ -329,8 +312,7 @@ sinkattn_status_t verify_common(const void* q, const void* k_pages, const void* 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     a.part_o = reinterpret_cast<float*>(ws);
     a.part_lse = a.part_o + plan.slots * (size_t)dims->q_len * G * kHeadDim;
-    a.counters = reinterpret_cast<unsigned long long*>(ws + plan.counters_offset);
-    a.epoch = next_epoch();
+    a.merge_list = reinterpret_cast<int2*>(ws + plan.merge_list_offset);
     a.err = ds->err;
     a.B = dims->batch;
     a.QL = dims->q_len;
@@ -352,7 +334,11 @@ sinkattn_status_t verify_common(const void* q, const void* k_pages, const void* 
     if (!encode_token_groups(&tq, q, (long long)dims->batch * dims->q_len, dims->num_q_heads, (unsigned)G,
                              (unsigned)dims->q_len))
         return SINKATTN_ERR_INVALID_ARG;
-    const cudaError_t e = verify_tc_launch(a, tq, tk, tv, static_cast<cudaStream_t>(stream));
+    // one share (a fixed single worker, or an automatic split whose largest possible work stays
+    // under the minimum share) cuts no segment
+    const long long max_tiles = (long long)dims->batch * Hkv * (((long long)dims->max_pages * kPageSize + 127) / 128);
+    const bool may_split = plan.tc_grid > 1 && (a.fixed_workers || max_tiles > kVerifyMinTiles);
+    const cudaError_t e = verify_tc_launch(a, tq, tk, tv, may_split, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? SINKATTN_OK : SINKATTN_ERR_CUDA;
 }
 }  // namespace

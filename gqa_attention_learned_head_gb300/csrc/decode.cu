@@ -42,6 +42,7 @@
 //    head is a 3-step shuffle; P^T is re-laid out for the next MMA with
 //    movmatrix; O^T[64 x 8] += V^T * P^T.  Everything stays in registers.
 #include "args_decode.h"
+#include "args_merge.h"
 #include "ptx.cuh"
 #include "split_kv.cuh"
 
@@ -65,7 +66,6 @@ constexpr int kWarps = SINKATTN_DECODE_WARPS;    // warps per CTA
 constexpr int kStages = SINKATTN_DECODE_STAGES;  // ring depth per warp
 constexpr int kSliceBytes = kPageSize * kHeadDim * 2;  // 2048: one (page, KV head) of K or V
 constexpr int kStageBytes = 2 * kSliceBytes;
-constexpr int kMergeThreads = 256;  // merge kernel: 16 half-warps, one (segment, head) each
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kNegInf = -__builtin_huge_valf();
@@ -598,69 +598,6 @@ __global__ void __launch_bounds__(kWarps * 32, SINKATTN_DECODE_MIN_BLOCKS)
     }
 }
 
-// Log-sum-exp merge of the split segments: half-warp per (listed segment, query head); lane l of
-// the half-warp owns head-dims 4l..4l+3.  Pieces are taken 8 at a time with all loads issued
-// together and combined online (base-2 partial lse).  Waits for the decode grid before reading.
-__global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecodeArgs a, int listed) {
-    wait_for_prerequisite_grids();
-    allow_dependent_launch();  // the next kernel on the stream may start launching
-    constexpr int kChunk = 8;
-    const int G = a.G, hl = threadIdx.x & 15;
-    const long long item = (long long)blockIdx.x * (kMergeThreads / 16) + (threadIdx.x >> 4);
-    if (item >= (long long)listed * G) return;
-    const int c = (int)(item / G), h = (int)(item % G);
-    const int2 e = __ldcg(&a.merge_list[c]);
-    if (e.x < 0) return;
-    const int seg = e.x, pieces = e.y;
-    const long long slot0 = (long long)c + seg;
-    const float* lp = a.part_lse + slot0 * G + h;
-    const float* op = a.part_o + (slot0 * G + h) * kHeadDim + 4 * hl;
-    float M = kNegInf, sum = 0.f;
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c0 = 0; c0 < pieces; c0 += kChunk) {
-        float l[kChunk];
-        float4 v[kChunk];
-#pragma unroll
-        for (int i = 0; i < kChunk; ++i) {
-            const bool in = c0 + i < pieces;
-            l[i] = in ? __ldcg(lp + (long long)(c0 + i) * G) : kNegInf;
-            v[i] = in ? __ldcg(reinterpret_cast<const float4*>(op + (long long)(c0 + i) * G * kHeadDim))
-                      : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        float Mc = M;
-#pragma unroll
-        for (int i = 0; i < kChunk; ++i) Mc = fmaxf(Mc, l[i]);
-        if (Mc == kNegInf) continue;
-        const float r = M == kNegInf ? 0.f : exp2f(M - Mc);
-        sum *= r;
-        o.x *= r;
-        o.y *= r;
-        o.z *= r;
-        o.w *= r;
-#pragma unroll
-        for (int i = 0; i < kChunk; ++i) {
-            const float w = l[i] == kNegInf ? 0.f : exp2f(l[i] - Mc);
-            sum += w;
-            o.x += w * v[i].x;
-            o.y += w * v[i].y;
-            o.z += w * v[i].z;
-            o.w += w * v[i].w;
-        }
-        M = Mc;
-    }
-    const int b = seg / a.Hkv, g = seg - b * a.Hkv;
-    const long long row = (long long)b * a.Hq + g * G + h;
-    uint2* dst = reinterpret_cast<uint2*>(a.out + row * kHeadDim) + hl;
-    if (M == kNegInf) {  // no live key and no finite sink in any piece
-        *dst = make_uint2(0u, 0u);
-        if (hl == 0 && a.lse) a.lse[row] = kNegInf;
-        return;
-    }
-    const float inv = 1.f / sum;
-    *dst = make_uint2(pack_bf16(o.x * inv, o.y * inv), pack_bf16(o.z * inv, o.w * inv));
-    if (hl == 0 && a.lse) a.lse[row] = (M + log2f(sum)) * kLn2;
-}
-
 template <int NT>
 cudaError_t ensure_smem_attr(size_t smem) {
     static thread_local size_t set_to[64] = {};
@@ -750,11 +687,19 @@ cudaError_t decode_launch(const DecodeArgs& args, const DecodePlan& plan, const 
     if (e != cudaSuccess || !may_split) return e;
     // the merge: its CTAs are scheduled while the decode runs and wait for the decode grid to
     // complete before they read its partials
-    const long long items = (long long)plan.grid * a.G;
-    cfg.gridDim = dim3((unsigned)((items + kMergeThreads / 16 - 1) / (kMergeThreads / 16)));
-    cfg.blockDim = dim3(kMergeThreads);
-    cfg.dynamicSmemBytes = 0;
-    return cudaLaunchKernelEx(&cfg, decode_merge_kernel, a, plan.grid);
+    SplitMergeArgs m;
+    m.part_o = a.part_o;
+    m.part_lse = a.part_lse;
+    m.list = a.merge_list;
+    m.out = a.out;
+    m.lse = a.lse;
+    m.listed = plan.grid;
+    m.R = a.G;
+    m.G = a.G;
+    m.QL = 1;
+    m.Hq = a.Hq;
+    m.Hkv = a.Hkv;
+    return split_merge_launch(m, stream);
 }
 
 }  // namespace sinkattn

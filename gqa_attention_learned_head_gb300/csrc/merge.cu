@@ -6,10 +6,12 @@
 // put it in one split (sinks == null) or hands it to the merge, which adds
 // exp(sink) exactly once.
 //
-// One warp per (row, head); lane l owns head-dims 2l and 2l+1, so the 64-wide
-// fp32 partial rows are read with coalesced 8-byte loads and the bf16 output
-// row is written as one 128-byte line.  HBM-bound and tiny next to the decode
-// pass that produces the partials.
+// sinkattn_merge: one warp per (row, head); lane l owns head-dims 2l and 2l+1,
+// so the 64-wide fp32 partial rows are read with coalesced 8-byte loads and
+// the bf16 output row is written as one 128-byte line.  HBM-bound and tiny next
+// to the pass that produces the partials.  The decode and verification kernels'
+// own split segments are merged by split_merge_kernel, launched right behind
+// them.
 #include "args_merge.h"
 #include "ptx.cuh"
 
@@ -50,7 +52,89 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeArgs a) {
     if (lane == 0 && a.lse) a.lse[row] = M + logf(sum);
 }
 
+constexpr int kSplitThreads = 256;  // 16 half-warps, one (listed segment, row) each
+
+// Log-sum-exp merge of the split segments: half-warp per (listed segment, row); lane l of the
+// half-warp owns head-dims 4l..4l+3.  Pieces are taken 8 at a time with all loads issued together
+// and combined online (base-2 partial lse).  Waits for the kernel that wrote the partials first,
+// then lets the next kernel on the stream start launching.
+__global__ void __launch_bounds__(kSplitThreads) split_merge_kernel(const SplitMergeArgs a) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    constexpr int kChunk = 8;
+    const int R = a.R, hl = threadIdx.x & 15;
+    const long long item = (long long)blockIdx.x * (kSplitThreads / 16) + (threadIdx.x >> 4);
+    if (item >= (long long)a.listed * R) return;
+    const int c = (int)(item / R), r = (int)(item % R);
+    const int2 e = __ldcg(&a.list[c]);
+    if (e.x < 0) return;
+    const int seg = e.x, pieces = e.y;
+    const long long slot0 = (long long)c + seg;
+    const float* lp = a.part_lse + slot0 * R + r;
+    const float* op = a.part_o + (slot0 * R + r) * kHeadDim + 4 * hl;
+    float M = kNegInf, sum = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c0 = 0; c0 < pieces; c0 += kChunk) {
+        float l[kChunk];
+        float4 v[kChunk];
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i) {
+            const bool in = c0 + i < pieces;
+            l[i] = in ? __ldcg(lp + (long long)(c0 + i) * R) : kNegInf;
+            v[i] = in ? __ldcg(reinterpret_cast<const float4*>(op + (long long)(c0 + i) * R * kHeadDim))
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float Mc = M;
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i) Mc = fmaxf(Mc, l[i]);
+        if (Mc == kNegInf) continue;
+        const float rs = M == kNegInf ? 0.f : exp2f(M - Mc);
+        sum *= rs;
+        o.x *= rs;
+        o.y *= rs;
+        o.z *= rs;
+        o.w *= rs;
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i) {
+            const float w = l[i] == kNegInf ? 0.f : exp2f(l[i] - Mc);
+            sum += w;
+            o.x += w * v[i].x;
+            o.y += w * v[i].y;
+            o.z += w * v[i].z;
+            o.w += w * v[i].w;
+        }
+        M = Mc;
+    }
+    const int b = seg / a.Hkv, g = seg - b * a.Hkv;
+    const long long row = ((long long)b * a.QL + r / a.G) * a.Hq + g * a.G + r % a.G;
+    uint2* dst = reinterpret_cast<uint2*>(a.out + row * kHeadDim) + hl;
+    if (M == kNegInf) {  // no live key and no finite sink in any piece
+        *dst = make_uint2(0u, 0u);
+        if (hl == 0 && a.lse) a.lse[row] = kNegInf;
+        return;
+    }
+    const float inv = 1.f / sum;
+    *dst = make_uint2(pack_bf16(o.x * inv, o.y * inv), pack_bf16(o.z * inv, o.w * inv));
+    if (hl == 0 && a.lse) a.lse[row] = (M + log2f(sum)) * 0.6931471805599453f;
+}
+
 }  // namespace
+
+cudaError_t split_merge_launch(const SplitMergeArgs& a, cudaStream_t stream) {
+    const long long items = (long long)a.listed * a.R;
+    if (items == 0) return cudaSuccess;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((items + kSplitThreads / 16 - 1) / (kSplitThreads / 16)));
+    cfg.blockDim = dim3(kSplitThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, split_merge_kernel, a);
+}
 
 cudaError_t merge_launch(const MergeArgs& a, cudaStream_t stream) {
     const long long rows = (long long)a.R * a.H;

@@ -1,8 +1,8 @@
 // split_kv.cuh -- the work split shared by the paged kernels (decode and draft
 // verification): the flattened list of (request b, KV head g, page) units, cut
 // into contiguous per-CTA shares; a share is cut at segment ends into pieces;
-// pieces of a segment held by several CTAs are merged by the CTA whose arrival
-// on the segment's counter completes it.
+// the pieces of a segment held by several CTAs are merged after the kernel by
+// the split-merge kernel (slot of CTA c's piece of segment seg: c + seg).
 //
 // Source of the split: "GPT-OSS on day 0" (Perplexity), section "Kernels for
 // GPT-OSS / Sink Attention": attention runs in parallel along the KV length as
@@ -74,43 +74,6 @@ __device__ __forceinline__ void segment_pieces(long long seg_start, int n, long 
     c_first = ((seg_start + 1) * C - 1) / U;
     const long long c_last = ((seg_start + n) * C - 1) / U;
     pieces = (int)(c_last - c_first + 1);
-}
-
-constexpr int kCountBits = 24;  // low bits of a segment counter: arrivals; high bits: call epoch
-
-__device__ __forceinline__ unsigned long long cas_acq_rel(unsigned long long* p, unsigned long long cmp,
-                                                          unsigned long long val) {
-    unsigned long long old;
-    asm volatile("atom.acq_rel.gpu.global.cas.b64 %0, [%1], %2, %3;" : "=l"(old) : "l"(p), "l"(cmp), "l"(val)
-                 : "memory");
-    return old;
-}
-
-__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
-    unsigned long long v;
-    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-
-// Records one more finished piece of a segment; true for the piece that completes it.  The
-// compare-and-swap has release semantics (this CTA's partials, ordered before it by the CTA
-// barrier, become visible first) and acquire semantics (the other pieces' partials are visible
-// to the merge that follows).  The first attempt guesses that this is the last arrival, so the
-// arrival that completes a segment -- the one on the critical path -- needs one round trip.
-// The counter carries the call's epoch in its high bits (a word from another call restarts the
-// count, so the workspace needs no zeroing) and the completing arrival resets it to 0.
-__device__ __forceinline__ bool arrive_last(unsigned long long* ctr, unsigned long long epoch, int pieces) {
-    unsigned long long old = (epoch << kCountBits) | (unsigned long long)(pieces - 1), nw;
-    while (true) {
-        nw = ((old >> kCountBits) == epoch) ? old + 1 : ((epoch << kCountBits) | 1ull);
-        const unsigned long long prev = cas_acq_rel(ctr, old, nw);
-        if (prev == old) break;
-        old = prev;
-    }
-    const bool last = (int)(nw & ((1ull << kCountBits) - 1)) == pieces;
-    // epoch 0 is never used: the next call starts afresh (no arrival can follow the last one)
-    if (last) *reinterpret_cast<volatile unsigned long long*>(ctr) = 0ull;
-    return last;
 }
 
 }  // namespace sinkattn

@@ -29,9 +29,13 @@
 //   warps 4-7   softmax, thread r = row r (only the warps that hold rows work),
 //               each row masked at its own causal limit or by its tree mask; at
 //               a piece's end they read O and write the rows (or fp32 partials).
-// A piece holding token 0 is seeded with the sink; the pieces of a segment
-// split between CTAs are merged by the CTA whose arrival completes it.  Every
-// wait is bounded.
+// A piece holding token 0 is seeded with the sink.  The pieces of a segment
+// split between CTAs write fp32 partials; the CTA holding the segment's first
+// piece lists it, and the split-merge kernel, launched right behind this one as
+// a programmatic dependent, combines them (no CTA waits for another).  The
+// kernel itself is a programmatic dependent of what precedes it on the stream.
+// Every wait is bounded.
+#include "args_merge.h"
 #include "args_verify.h"
 #include "ptx.cuh"
 #include "split_kv.cuh"
@@ -47,7 +51,7 @@ constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColS = 0, kColO = 128, kColP = 192;
 constexpr int kKStages = 2, kVStages = 2;
 constexpr int kPagesPerTile = kBN / kPageSize;  // 8
-constexpr int kMinTiles = 4;  // automatic mode: never cut shares finer than this
+constexpr int kMinTiles = kVerifyMinTiles;  // automatic mode: never cut shares finer than this
 
 
 __device__ __forceinline__ int kv_len_of(const VerifyArgs& a, int i) {
@@ -102,75 +106,11 @@ struct __align__(1024) Smem {
     uint64_t q_full[2], q_empty[2], k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
     uint64_t s_full, s_free, p_full, o_done, mma_done;
     uint32_t tmem_base;
-    int pend[2];         // segments of this share's partial pieces ...
-    int pend_tiles[2];   // ... their tiles ...
-    long long pend_start[2];  // ... and their first units
-    int last;            // this CTA completes the segment being merged
     long long red[8];    // block reductions
     long long found[4];  // share start: request, its first unit, its tiles, flag
     Walk walk[4];        // the softmax warps' walkers (kept out of their registers)
     Piece piece[4];      // ... and their current pieces
 };
-
-__device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-
-// Log-sum-exp merge of segment seg from its pieces' partials (base-2 lse), by the 128 softmax threads:
-// DIMS head-dims of one row per thread (64 / DIMS threads per row), pieces taken four at a time
-// with all their loads issued together and combined online.
-template <int DIMS>
-__device__ void merge_rows(const VerifyArgs& a, int seg, long long slot0, int pieces, int t) {
-    constexpr int kTpr = kHeadDim / DIMS, kChunk = 4;
-    const int R = a.R, G = a.G, b = seg / a.Hkv, g = seg - b * a.Hkv;
-    const int r = t / kTpr, d0 = (t % kTpr) * DIMS;
-    if (r >= R) return;
-    const float* lp = a.part_lse + slot0 * R + r;
-    const float* op = a.part_o + (slot0 * R + r) * kHeadDim + d0;
-    float M = kNegInf, sum = 0.f, o[DIMS];
-#pragma unroll
-    for (int e = 0; e < DIMS; ++e) o[e] = 0.f;
-    for (int c0 = 0; c0 < pieces; c0 += kChunk) {
-        float l[kChunk];
-        float4 v[kChunk][DIMS / 4];
-#pragma unroll
-        for (int k = 0; k < kChunk; ++k) {
-            const bool in = c0 + k < pieces;
-            l[k] = in ? __ldcg(lp + (long long)(c0 + k) * R) : kNegInf;
-            const float4* src = reinterpret_cast<const float4*>(op + (long long)(c0 + k) * R * kHeadDim);
-#pragma unroll
-            for (int e = 0; e < DIMS / 4; ++e) v[k][e] = in ? __ldcg(src + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        float Mc = M;
-#pragma unroll
-        for (int k = 0; k < kChunk; ++k) Mc = fmaxf(Mc, l[k]);
-        if (Mc == kNegInf) continue;
-        const float rs = M == kNegInf ? 0.f : exp2f(M - Mc);
-        sum *= rs;
-#pragma unroll
-        for (int e = 0; e < DIMS; ++e) o[e] *= rs;
-#pragma unroll
-        for (int k = 0; k < kChunk; ++k) {
-            const float w = l[k] == kNegInf ? 0.f : exp2f(l[k] - Mc);
-            sum += w;
-#pragma unroll
-            for (int e = 0; e < DIMS / 4; ++e) {
-                o[4 * e + 0] += w * v[k][e].x;
-                o[4 * e + 1] += w * v[k][e].y;
-                o[4 * e + 2] += w * v[k][e].z;
-                o[4 * e + 3] += w * v[k][e].w;
-            }
-        }
-        M = Mc;
-    }
-    const int i = r / G, h = r % G;
-    const long long row = ((long long)b * a.QL + i) * a.Hq + g * G + h;
-    uint4* dst = reinterpret_cast<uint4*>(a.out + row * kHeadDim + d0);
-    const float inv = M == kNegInf ? 0.f : 1.f / sum;  // no live key and no finite sink: zeros
-#pragma unroll
-    for (int e = 0; e < DIMS / 8; ++e)
-        dst[e] = make_uint4(pack_bf16(o[8 * e + 0] * inv, o[8 * e + 1] * inv), pack_bf16(o[8 * e + 2] * inv, o[8 * e + 3] * inv),
-                            pack_bf16(o[8 * e + 4] * inv, o[8 * e + 5] * inv), pack_bf16(o[8 * e + 6] * inv, o[8 * e + 7] * inv));
-    if (d0 == 0 && a.lse) a.lse[row] = M == kNegInf ? kNegInf : (M + log2f(sum)) * kLn2;
-}
 
 __global__ void __launch_bounds__(kThreads, 2)
     verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
@@ -179,6 +119,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = a.B, Hkv = a.Hkv, R = a.R, QL = a.QL, G = a.G;
+    // a programmatic dependent of what precedes it on the stream: nothing is read before that has
+    // completed; the split merge behind this kernel may be scheduled once every CTA runs
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // ---- 1. units (Hkv x tiles) per request: their total U and, by a running block-wide scan, the
     // request holding this share's first unit (one pass when the batch fits the CTA's threads)
@@ -226,10 +170,12 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (a.lse) a.lse[r] = __ldg(&a.sinks[r % a.Hq]);
         }
     }
-    if (U == 0) return;
-    const long long C = effective_shares(a.tc_grid, a.fixed_workers, kMinTiles, U);
+    const long long C = U > 0 ? effective_shares(a.tc_grid, a.fixed_workers, kMinTiles, U) : 0;
     const long long cta = blockIdx.x;
-    if (cta >= C) return;
+    if (cta >= C) {
+        if (tid == 0 && a.merge_list) a.merge_list[cta] = make_int2(-1, 0);
+        return;
+    }
     const long long x0 = cta * U / C, x1 = (cta + 1) * U / C;
     if (B <= kThreads) {
         if (cnt > 0 && x0 >= lo && x0 < lo + cnt) {
@@ -446,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int r = tid - 128;
         const bool live = r < R;
         const int i = live ? r / G : 0, h = live ? r % G : 0;
-        int pend_n = 0;  // partial pieces of this share (at most its first and its last)
+        int2 head = make_int2(-1, 0);  // the share's last piece, if it starts a segment it does not end
         if (warp - 4 < active) {
             // ---------------------------------------------------------------- softmax
             const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
@@ -593,12 +539,12 @@ __global__ void __launch_bounds__(kThreads, 2)
                 tc_fence_before();
                 const bool whole = seeded && tb == pc.tiles;
                 const int seg = pc.b * Hkv + pc.g;
-                if (!whole && tid == 128) {
-                    sm.pend[pend_n] = seg;
-                    sm.pend_tiles[pend_n] = pc.tiles;
-                    sm.pend_start[pend_n] = pc.seg_start;
+                if (seeded && !whole) {
+                    long long c_first = 0;
+                    int pieces = 0;
+                    segment_pieces(pc.seg_start, pc.tiles, C, U, c_first, pieces);
+                    head = make_int2(seg, pieces);
                 }
-                pend_n += whole ? 0 : 1;
                 if (live) {
                     const float inv = d > 0.f ? 1.f / d : 0.f;
                     const float l2 = d > 0.f ? m + log2f(d) : kNegInf;
@@ -627,32 +573,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
             }
             if (!ok && lane == 0) atomicOr(a.err, kErrTimeout);
-        } else {
-            // a softmax warp without rows counts the share's partial pieces too
-            Piece pc;
-            while (walk.next(a, pc)) pend_n += (pc.ta == 0 && pc.tb == pc.tiles) ? 0 : 1;
         }
-        // ---- the share's partial pieces (at most its first and its last): arrive on their segments'
-        // counters together; the CTA completing a segment merges it
-        pend_n = __shfl_sync(0xffffffffu, pend_n, 0);
-        softmax_bar();  // the partials of this CTA are written (CTA scope) and pend[] is set
-        if (tid - 128 < pend_n) {
-            const int k = tid - 128;
-            const int seg = sm.pend[k];
-            long long c_first = 0;
-            int pieces = 0;
-            segment_pieces(sm.pend_start[k], sm.pend_tiles[k], C, U, c_first, pieces);
-            const bool last = arrive_last(&a.counters[seg], a.epoch, pieces);  // release + acquire
-            sm.red[2 * k] = last ? c_first + seg : -1;  // merge job: the segment's first partial slot ...
-            sm.red[2 * k + 1] = pieces;                  // ... and its pieces
-        }
-        softmax_bar();
-        for (int k = 0; k < pend_n; ++k) {
-            const long long slot0 = sm.red[2 * k];
-            if (slot0 < 0) continue;
-            if (R <= 32) merge_rows<16>(a, sm.pend[k], slot0, (int)sm.red[2 * k + 1], r);
-            else merge_rows<32>(a, sm.pend[k], slot0, (int)sm.red[2 * k + 1], r);
-        }
+        // ---- list the segment whose first piece this share holds without completing it (the
+        // split merge combines its partials once every CTA has finished)
+        if (tid == 128 && a.merge_list) a.merge_list[cta] = head;
     }
     tc_fence_before();
     __syncthreads();
@@ -737,20 +661,45 @@ cudaError_t verify_plan(int B, int QL, int Hq, int Hkv, int num_workers, VerifyP
     plan->slots = (size_t)plan->tc_grid + (size_t)segs;  // partial slot = share + segment
     size_t bytes = plan->slots * R * kHeadDim * 4;       // partial o
     bytes += plan->slots * R * 4;                        // partial lse (base 2)
-    plan->counters_offset = (bytes + 255) & ~size_t(255);
-    plan->ws_bytes = plan->counters_offset + (size_t)segs * sizeof(unsigned long long);
+    plan->merge_list_offset = (bytes + 255) & ~size_t(255);
+    plan->ws_bytes = plan->merge_list_offset + (size_t)plan->tc_grid * sizeof(int2);
     return cudaSuccess;
 }
 
-cudaError_t verify_tc_launch(const VerifyArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                             cudaStream_t stream) {
-    if (a.B == 0) return cudaSuccess;
-    if (a.tc_grid > 0x7fffffffll || a.tc_grid < 1) return cudaErrorInvalidConfiguration;
+cudaError_t verify_tc_launch(const VerifyArgs& args, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                             bool may_split, cudaStream_t stream) {
+    if (args.B == 0) return cudaSuccess;
+    if (args.tc_grid > 0x7fffffffll || args.tc_grid < 1) return cudaErrorInvalidConfiguration;
     int per_sm = 0;  // also sets the kernel's shared-memory limit
     cudaError_t e = verify_tc_occupancy(&per_sm);
     if (e != cudaSuccess) return e;
-    verify_tc_kernel<<<(unsigned)a.tc_grid, kThreads, verify_tc_smem(), stream>>>(tq, tk, tv, a);
-    return cudaGetLastError();
+    VerifyArgs a = args;
+    if (!may_split) a.merge_list = nullptr;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.tc_grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = verify_tc_smem();
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, verify_tc_kernel, tq, tk, tv, a);
+    if (e != cudaSuccess || !may_split) return e;
+    SplitMergeArgs m;
+    m.part_o = a.part_o;
+    m.part_lse = a.part_lse;
+    m.list = a.merge_list;
+    m.out = a.out;
+    m.lse = a.lse;
+    m.listed = (int)a.tc_grid;
+    m.R = a.R;
+    m.G = a.G;
+    m.QL = a.QL;
+    m.Hq = a.Hq;
+    m.Hkv = a.Hkv;
+    return split_merge_launch(m, stream);
 }
 
 }  // namespace sinkattn
