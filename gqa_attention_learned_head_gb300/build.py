@@ -75,11 +75,45 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> Path:
     return LIB
 
 
+# Host code with the most validation logic: the C ABI layer and the no-allocation entry point.
+SANITIZED_SOURCES = ("api.cu", "decode_noalloc.cu")
+SAN_BUILD = PKG / "_build_san"
+SAN_LIB = SAN_BUILD / "libsinkattn.so"
+SAN_FLAGS = ["-Xcompiler", "-fsanitize=address", "-Xcompiler", "-fsanitize=undefined", "-Xcompiler", "-fno-omit-frame-pointer",
+             "-Xcompiler", "-fno-sanitize-recover=undefined"]
+
+
+def build_sanitized() -> Path:
+    """A copy of the library whose host code in SANITIZED_SOURCES is compiled with AddressSanitizer
+    and UndefinedBehaviorSanitizer (the other objects are the regular ones), for tests of the host
+    validation paths.  A process loading it must load the ASan runtime first (LD_PRELOAD)."""
+    build()
+    nvcc = nvcc_path()
+    SAN_BUILD.mkdir(exist_ok=True)
+    objs = [str(BUILD / (src.stem + ".o")) for src in sources() if src.name not in SANITIZED_SOURCES]
+    for name in SANITIZED_SOURCES:
+        obj = SAN_BUILD / (Path(name).stem + ".o")
+        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *SAN_FLAGS, "-c", str(CSRC / name), "-o", str(obj)]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed on {name}:\n{r.stdout}\n{r.stderr}")
+        objs.append(str(obj))
+    cmd = [nvcc, *ARCH, "-shared", "-Xcompiler", "-fPIC", *SAN_FLAGS, *objs, "-o", str(SAN_LIB)]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    return SAN_LIB
+
+
 if __name__ == "__main__":
     ap = argparse.ArgumentParser()
     ap.add_argument("--force", action="store_true")
     ap.add_argument("--verbose", action="store_true")
     ap.add_argument("--ptxas-info", action="store_true", help="print register / shared memory use")
+    ap.add_argument("--sanitize", action="store_true",
+                    help="also build _build_san/libsinkattn.so, its host validation code under ASan + UBSan")
     args = ap.parse_args()
+    if args.sanitize:
+        print(build_sanitized())
     extra = ["-Xptxas", "-v"] if args.ptxas_info else []
     print(build(force=args.force or args.ptxas_info, verbose=args.verbose or args.ptxas_info, extra_flags=extra))

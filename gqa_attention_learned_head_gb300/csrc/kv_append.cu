@@ -21,6 +21,11 @@ constexpr int kWarpsPerBlock = 8;
 
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) kv_append_kernel(const AppendArgs a) {
     const int lane = threadIdx.x & 31;
+    // a packing that is not 0 <= cu_seqlens[n] <= cu_seqlens[n+1] <= T is reported (one grid-stride pass)
+    for (long long n = (long long)blockIdx.x * blockDim.x + threadIdx.x; n < a.N; n += (long long)gridDim.x * blockDim.x) {
+        const int c0 = __ldg(&a.cu_seqlens[n]), c1 = __ldg(&a.cu_seqlens[n + 1]);
+        if (c0 < 0 || c1 < c0 || c1 > a.T) atomicOr(a.err, kErrBadLength);
+    }
     const long long t = (long long)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
     if (t >= a.T) return;
     // sequence holding token t: largest n with cu_seqlens[n] <= t (all lanes, same addresses)
@@ -31,6 +36,11 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) kv_append_kernel(const Ap
         else hi = mid - 1;
     }
     const int n = lo;
+    // with a corrupted packing the search can land on a sequence that does not hold t: skip it
+    if (t < __ldg(&a.cu_seqlens[n]) || t >= __ldg(&a.cu_seqlens[n + 1])) {
+        if (lane == 0) atomicOr(a.err, kErrBadLength);
+        return;
+    }
     const long long pos = (long long)__ldg(&a.start_pos[n]) + (t - __ldg(&a.cu_seqlens[n]));
     if (pos < 0 || pos >= (long long)a.max_pages * kPageSize) {
         if (lane == 0) atomicOr(a.err, kErrBadLength);

@@ -44,6 +44,11 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
 
 __global__ void __launch_bounds__(kWarps * 32) qkv_prologue_kernel(const PrologueArgs a) {
     const int lane = threadIdx.x & 31;
+    // a packing that is not 0 <= cu_seqlens[n] <= cu_seqlens[n+1] <= T is reported (one grid-stride pass)
+    for (long long n = (long long)blockIdx.x * blockDim.x + threadIdx.x; n < a.N; n += (long long)gridDim.x * blockDim.x) {
+        const int c0 = __ldg(&a.cu_seqlens[n]), c1 = __ldg(&a.cu_seqlens[n + 1]);
+        if (c0 < 0 || c1 < c0 || c1 > a.T) atomicOr(a.err, kErrBadLength);
+    }
     const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
     if (t >= a.T) return;
     int lo = 0, hi = a.N - 1;  // sequence holding token t: largest n with cu_seqlens[n] <= t
@@ -52,9 +57,12 @@ __global__ void __launch_bounds__(kWarps * 32) qkv_prologue_kernel(const Prologu
         if (__ldg(&a.cu_seqlens[mid]) <= t) lo = mid;
         else hi = mid - 1;
     }
+    // with a corrupted packing the search can land on a sequence that does not hold t: its k / v
+    // are not written (q_out still is)
+    const bool held = t >= __ldg(&a.cu_seqlens[lo]) && t < __ldg(&a.cu_seqlens[lo + 1]);
     const long long pos = (long long)__ldg(&a.start_pos[lo]) + (t - __ldg(&a.cu_seqlens[lo]));
     int page = -1;
-    if (pos < 0 || pos >= (long long)a.max_pages * kPageSize) {
+    if (!held || pos < 0 || pos >= (long long)a.max_pages * kPageSize) {
         if (lane == 0) atomicOr(a.err, kErrBadLength);
     } else {
         page = __ldg(&a.page_table[(long long)lo * a.max_pages + pos / kPageSize]);

@@ -131,3 +131,63 @@ def test_prologue_host_validation_without_device(S):
     assert call(S.RopeParams(150000.0, 32.0, 4096, 1.0, 32.0, 0.0, 0)) == S.ERR_INVALID_ARG  # beta_fast <= beta_slow
     assert call(ok) == S.ERR_INVALID_ARG  # null buffers
     assert call(ok, S.PagedDims(0, 0, 0, 8, 2, 64, 16, 10, 4)) == 0  # nothing to do
+
+
+SANITIZED_CHILD = r"""
+import ctypes, sys
+sys.path.insert(0, sys.argv[1])
+from gqa_attention_learned_head_gb300 import abi
+lib = abi.declare(ctypes.CDLL(sys.argv[2]))
+nul = [None] * 7
+codes = []
+for d in (abi.DecodeDims(2, 8, 2, 32, 16, 10, 4, 0), abi.DecodeDims(2, 8, 3, 64, 16, 10, 4, 0),
+          abi.DecodeDims(2, 64, 2, 64, 16, 10, 4, 0), abi.DecodeDims(-1, 8, 2, 64, 16, 10, 4, 0),
+          abi.DecodeDims(2, 8, 2, 64, 16, 10, 0, 0)):
+    codes.append(lib.sinkattn_decode(*nul[:6], 0.125, None, None, ctypes.byref(d), None, 0, None))
+    codes.append(lib.sinkattn_decode_noalloc(*nul[:6], 0.125, None, None, ctypes.byref(d), None))
+    codes.append(int(lib.sinkattn_decode_workspace_size(ctypes.byref(d)) == 0))
+codes.append(lib.sinkattn_decode(*nul[:6], 0.125, None, None, None, None, 0, None))
+for d in (abi.VerifyDims(2, 0, 8, 2, 64, 16, 10, 4, 0), abi.VerifyDims(2, 17, 8, 8, 64, 16, 10, 4, 0),
+          abi.VerifyDims(2, 9, 64, 8, 64, 16, 10, 4, 0), abi.VerifyDims(2, 4, 8, 3, 64, 16, 10, 4, 0)):
+    codes.append(lib.sinkattn_verify(*nul[:6], 0.125, None, None, ctypes.byref(d), None, 0, None))
+    codes.append(lib.sinkattn_verify_tree(*nul[:7], 0.125, None, None, ctypes.byref(d), None, 0, None))
+for d in (abi.PrefillDims(1, 10, 10, 8, 2, 128), abi.PrefillDims(-1, 10, 10, 8, 2, 64),
+          abi.PrefillDims(1, 10, 10, 8, 2, 64, 2), abi.PrefillDims(1, 10, 10, 8, 3, 64)):
+    codes.append(lib.sinkattn_prefill(*nul[:5], 0.1, 1, None, None, ctypes.byref(d), None))
+for d in (abi.PagedDims(2, 10, 8, 8, 2, 32, 16, 10, 4), abi.PagedDims(2, 10, 8, 8, 3, 64, 16, 10, 4),
+          abi.PagedDims(2, 10, 8, 8, 2, 64, 16, 10, 0), abi.PagedDims(2, 10, 8, 8, 2, 64, 16, 10, 4, 3),
+          abi.PagedDims(20000, 10, 8, 8, 2, 64, 16, 10, 4)):
+    codes.append(lib.sinkattn_kv_append(*nul[:7], ctypes.byref(d), None))
+    codes.append(lib.sinkattn_prefill_paged(*nul[:7], 0.125, None, None, ctypes.byref(d), None))
+    r = abi.RopeParams(150000.0, 0.5, 4096, 32.0, 1.0, 0.0, 0)
+    codes.append(lib.sinkattn_qkv_prologue(*nul[:5], ctypes.byref(r), None, None, None, ctypes.byref(d), None))
+for d in (abi.MergeDims(2, 4, 0, 64), abi.MergeDims(2, 4, 8, 32), abi.MergeDims(-1, 4, 8, 64)):
+    codes.append(lib.sinkattn_merge(*nul[:5], ctypes.byref(d), None))
+codes.append(lib.sinkattn_merge(*nul[:5], None, None))
+for st in list(range(-3, 12)) + [1 << 30]:
+    lib.sinkattn_status_string(st)
+assert all(c != 0 for c in codes), codes
+print("ok", len(codes))
+"""
+
+
+def test_host_validation_under_sanitizers():
+    """The host code of the C ABI layer and the no-allocation entry point, built with AddressSanitizer
+    and UndefinedBehaviorSanitizer, rejects every malformed call of the validation tests (and status
+    strings out of range) without a sanitizer report."""
+    import os
+    import subprocess
+    import sys
+
+    from gqa_attention_learned_head_gb300 import build
+
+    asan = subprocess.run(["gcc", "-print-file-name=libasan.so"], capture_output=True, text=True).stdout.strip()
+    if not asan or not os.path.isabs(asan) or not os.path.exists(asan):
+        pytest.skip("the AddressSanitizer runtime is not installed")
+    lib = build.build_sanitized()
+    env = dict(os.environ, LD_PRELOAD=asan, ASAN_OPTIONS="detect_leaks=0:abort_on_error=1",
+               UBSAN_OPTIONS="halt_on_error=1:print_stacktrace=1")
+    r = subprocess.run([sys.executable, "-c", SANITIZED_CHILD, str(ROOT), str(lib)], env=env, capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode == 0 and r.stdout.startswith("ok"), r.stdout[-2000:] + r.stderr[-4000:]
+    assert "AddressSanitizer" not in r.stderr and "runtime error" not in r.stderr, r.stderr[-4000:]
