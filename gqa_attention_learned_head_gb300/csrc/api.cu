@@ -65,40 +65,78 @@ sinkattn_status_t device_state(DeviceState** out) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// 3-D bf16 tensor map over q [tokens, H, 64] whose box is 64 x box_heads heads x box_tokens tokens
-// (the rows of one query-head group of several consecutive tokens), 128-byte swizzle.
+// A bf16, 128-byte-swizzled tensor map of `rank` dimensions (the innermost one 64 elements of
+// 128 B), encoded once per distinct (base, dims, strides, box) in each host thread: a serving loop
+// calling with the same buffers every step skips the encoder after its first call.
+bool encode_cached(CUtensorMap* map, int rank, const void* base, const cuuint64_t* dims, const cuuint64_t* strides,
+                   const cuuint32_t* box) {
+    struct Entry {
+        const void* base;
+        int rank;
+        cuuint64_t dims[3], strides[2];
+        cuuint32_t box[3];
+        CUtensorMap map;
+    };
+    constexpr int kEntries = 16;
+    static thread_local Entry cache[kEntries];
+    static thread_local int used = 0, next = 0;
+    auto same = [&](const Entry& e) {
+        if (e.base != base || e.rank != rank) return false;
+        for (int i = 0; i < rank; ++i)
+            if (e.dims[i] != dims[i] || e.box[i] != box[i]) return false;
+        for (int i = 0; i < rank - 1; ++i)
+            if (e.strides[i] != strides[i]) return false;
+        return true;
+    };
+    for (int i = 0; i < used; ++i)
+        if (same(cache[i])) {
+            *map = cache[i].map;
+            return true;
+        }
+    const cuuint32_t estride[3] = {1, 1, 1};
+    if (g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box,
+                 estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    Entry& e = cache[next];
+    e.base = base;
+    e.rank = rank;
+    for (int i = 0; i < rank; ++i) {
+        e.dims[i] = dims[i];
+        e.box[i] = box[i];
+    }
+    for (int i = 0; i < rank - 1; ++i) e.strides[i] = strides[i];
+    e.map = *map;
+    next = (next + 1) % kEntries;
+    if (used < kEntries) ++used;
+    return true;
+}
+
+// 3-D map over q [tokens, H, 64] whose box is 64 x box_heads heads x box_tokens tokens (the rows of
+// one query-head group of several consecutive tokens).
 bool encode_token_groups(CUtensorMap* map, const void* base, long long tokens, int H, unsigned box_heads,
                          unsigned box_tokens) {
-    cuuint64_t dims[3] = {64, (cuuint64_t)H, (cuuint64_t)tokens};
-    cuuint64_t strides[2] = {128, (cuuint64_t)H * 128};
-    cuuint32_t box[3] = {64, box_heads, box_tokens};
-    cuuint32_t estride[3] = {1, 1, 1};
-    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estride,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    const cuuint64_t dims[3] = {64, (cuuint64_t)H, (cuuint64_t)tokens};
+    const cuuint64_t strides[2] = {128, (cuuint64_t)H * 128};
+    const cuuint32_t box[3] = {64, box_heads, box_tokens};
+    return encode_cached(map, 3, base, dims, strides, box);
 }
 
-// 2-D bf16 tensor map over rows of 64 elements (128 B), box = box_rows x 64, 128-byte swizzle.
+// 2-D map over rows of 64 elements (128 B), box = box_rows x 64.
 bool encode_rows(CUtensorMap* map, const void* base, unsigned long long rows, unsigned long long row_stride_bytes,
                  unsigned box_rows) {
-    cuuint64_t dims[2] = {64, rows};
-    cuuint64_t strides[1] = {row_stride_bytes};
-    cuuint32_t box[2] = {64, box_rows};
-    cuuint32_t estride[2] = {1, 1};
-    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estride,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    const cuuint64_t dims[2] = {64, rows};
+    const cuuint64_t strides[1] = {row_stride_bytes};
+    const cuuint32_t box[2] = {64, box_rows};
+    return encode_cached(map, 2, base, dims, strides, box);
 }
 
-// 3-D bf16 tensor map over [T, H, 64] (token-major), box = box_rows tokens x 1 head x 64.
+// 3-D map over [T, H, 64] (token-major), box = box_rows tokens x 1 head x 64.
 bool encode_thd(CUtensorMap* map, const void* base, int T, int H, unsigned box_rows) {
-    cuuint64_t dims[3] = {64, (cuuint64_t)H, (cuuint64_t)T};
-    cuuint64_t strides[2] = {128, (cuuint64_t)H * 128};
-    cuuint32_t box[3] = {64, 1, box_rows};
-    cuuint32_t estride[3] = {1, 1, 1};
-    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estride,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    const cuuint64_t dims[3] = {64, (cuuint64_t)H, (cuuint64_t)T};
+    const cuuint64_t strides[2] = {128, (cuuint64_t)H * 128};
+    const cuuint32_t box[3] = {64, 1, box_rows};
+    return encode_cached(map, 3, base, dims, strides, box);
 }
 
 sinkattn_status_t check_decode_dims(const sinkattn_decode_dims_t* d) {

@@ -11,8 +11,9 @@
 // compete for the MUFU, then both wait for the tensor core.  Here one CTA per
 // SM owns the same 128 query rows of two heads h0, h0 + 1 of one KV group, so
 // K_j and V_j are loaded once for both, and the two softmax warpgroups hand an
-// "exp turn" back and forth through mbarriers: while warpgroup 0 exponentiates
-// tile j, the tensor core runs warpgroup 1's products, and the other way round.
+// "exp turn" back and forth through mbarriers, warp by warp on each SM
+// sub-partition (whose exp unit warps k and k + 4 of the two groups share): while
+// one group exponentiates tile j, the tensor core runs the other's products.
 //
 //   warp 0      TMA: both Q tiles once, then K_j into a 3-stage ring.
 //   warp 3      TMA: V_j into a 2-stage ring.
@@ -50,7 +51,9 @@ struct __align__(1024) Smem {
     uint8_t v[kVStages][kTileBytes];
     uint64_t q_full, k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
     uint64_t s_full[2], s_free[2], p_full[2], o_done[2];
-    uint64_t turn[2];  // turn[w] completes a phase when the other warpgroup has finished an exp phase
+    // turn[w][k]: warp k of warpgroup w may exponentiate; completed by warp k of the other warpgroup (the
+    // same SM sub-partition, whose exp unit the two share) when it has finished its exp phase
+    uint64_t turn[2][4];
     uint64_t mma_done;
     uint64_t v_fixed;  // paged: the last V tile with its rows past the cache end zeroed
     uint32_t tmem_base;
@@ -116,7 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sm.s_free[w], 128);
             mbar_init(&sm.p_full[w], 128);
             mbar_init(&sm.o_done[w], 1);
-            mbar_init(&sm.turn[w], 4);  // one arrival per warp of the other warpgroup
+            for (int k = 0; k < 4; ++k) mbar_init(&sm.turn[w][k], 1);
         }
         mbar_init(&sm.mma_done, 2);
         mbar_init(&sm.v_fixed, 1);
@@ -339,9 +342,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float neg_m = (m == kNegInf) ? 0.f : -m;
 
-            // The exp turn: warpgroup 0 goes first at every tile, warpgroup 1 after it.
+            // The exp turn, per SM sub-partition: warp k of warpgroup 0 goes first at every tile, warp k
+            // of warpgroup 1 (on the same sub-partition) after it.
             if (w == 0 ? j > 0 : true) {
-                if (!(ok = warp_wait(&sm.turn[w], (w == 0 ? j - 1 : j) & 1))) break;
+                if (!(ok = warp_wait(&sm.turn[w][warp & 3], (w == 0 ? j - 1 : j) & 1))) break;
             }
             const float2 mul2 = make_float2(mul, mul), negm2 = make_float2(neg_m, neg_m);
             float2 sums[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
@@ -365,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Hand the turn over once this row's exponentials are summed: d >= 0 always holds, but the
             // test makes the arrival wait for every exp2 of the tile.
             __syncwarp();
-            if (lane == 0 && !(d < 0.f)) mbar_arrive(&sm.turn[w ^ 1]);  // the other warpgroup's turn
+            if (lane == 0 && !(d < 0.f)) mbar_arrive(&sm.turn[w ^ 1][warp & 3]);  // the partner warp's turn
             if (j > 0) {  // P_{j-1} consumed and O_{j-1} final before P and O are touched
                 if (!(ok = warp_wait(&sm.o_done[w], (j - 1) & 1))) break;
                 tc_fence_after();
