@@ -214,48 +214,51 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
             for (int j = issued - kVStages < 0 ? 0 : issued - kVStages; j < issued; ++j)
                 (void)mbar_wait(&sm.v_full[j % kVStages], (j / kVStages) & 1);
-        } else if (warp == 1 && lane == 0) {
+        } else if (warp == 1) {
             // ------------------------------------------------------------ S issuer: S_j = Q K_j^T
             // Needs only K_j and the S columns released by the softmax, so S_{j+1} is computed
-            // while the softmax still works on tile j.
+            // while the softmax still works on tile j.  (The whole warp walks the loop, one elected
+            // lane issues.)
             const uint32_t tS = tbase + kColS;
             const uint32_t qaddr = smem_u32(sm.q);
-            bool ok = mbar_wait(&sm.q_full, 0);
+            bool ok = warp_wait(&sm.q_full, 0);
             for (int j = 0; ok && j < ntile; ++j) {
                 const int st = j % kKStages;
-                ok = mbar_wait(&sm.k_full[st], (j / kKStages) & 1) && (j == 0 || mbar_wait(&sm.s_free, (j - 1) & 1));
+                ok = warp_wait(&sm.k_full[st], (j / kKStages) & 1) && (j == 0 || warp_wait(&sm.s_free, (j - 1) & 1));
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t kaddr = smem_u32(sm.k[st]);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    tc_mma_ss(tS, sw128_desc(qaddr + kk * 32), sw128_desc(kaddr + kk * 32), kIdescQK, kk > 0);
-                tc_commit(&sm.s_full);
-                tc_commit(&sm.k_empty[st]);  // K_j read
+                    tc_mma_ss_warp(tS, sw128_desc(qaddr + kk * 32), sw128_desc(kaddr + kk * 32), kIdescQK, kk > 0);
+                tc_commit_warp(&sm.s_full);
+                tc_commit_warp(&sm.k_empty[st]);  // K_j read
             }
-            if (!ok) atomicOr(a.err, kErrTimeout);
-            tc_commit(&sm.mma_done);  // every MMA of both issuers has finished before TMEM is released
-            (void)mbar_wait(&sm.mma_done, 0);
-        } else if (warp == 2 && lane == 0) {
+            if (!ok && lane == 0) atomicOr(a.err, kErrTimeout);
+            tc_commit_warp(&sm.mma_done);  // every MMA of both issuers has finished before TMEM is released
+            (void)warp_wait(&sm.mma_done, 0);
+        } else if (warp == 2) {
             // ------------------------------------------------------------ PV issuer: O += P_j V_j
+            // (the whole warp walks the loop, one elected lane issues)
             const uint32_t tO = tbase + kColO, tP = tbase + kColP;
             bool ok = true;
             for (int j = 0; ok && j < ntile; ++j) {
-                ok = ((fix_last_v && j == ntile - 1) ? mbar_wait(&sm.v_fixed, 0)
-                                                     : mbar_wait(&sm.v_full[j % kVStages], (j / kVStages) & 1)) &&
-                     mbar_wait(&sm.p_full, j & 1);
+                ok = ((fix_last_v && j == ntile - 1) ? warp_wait(&sm.v_fixed, 0)
+                                                     : warp_wait(&sm.v_full[j % kVStages], (j / kVStages) & 1)) &&
+                     warp_wait(&sm.p_full, j & 1);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t vaddr = smem_u32(sm.v[j % kVStages]);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
-                    tc_mma_ts(tO, tP + ks * 8, sw128_desc(vaddr + ks * 2048), kIdescPV, (j > 0 || ks > 0) ? 1u : 0u);
-                tc_commit(&sm.v_empty[j % kVStages]);  // V_j read
-                tc_commit(&sm.o_done);
+                    tc_mma_ts_warp(tO, tP + ks * 8, sw128_desc(vaddr + ks * 2048), kIdescPV,
+                                   (j > 0 || ks > 0) ? 1u : 0u);
+                tc_commit_warp(&sm.v_empty[j % kVStages]);  // V_j read
+                tc_commit_warp(&sm.o_done);
             }
-            if (!ok) atomicOr(a.err, kErrTimeout);
-            tc_commit(&sm.mma_done);
-            (void)mbar_wait(&sm.mma_done, 0);
+            if (!ok && lane == 0) atomicOr(a.err, kErrTimeout);
+            tc_commit_warp(&sm.mma_done);
+            (void)warp_wait(&sm.mma_done, 0);
         }
     } else {
         // 128 x 40 + 128 x 216 = 128 x 56 + 128 x 200 = 256 x 128, the launch's registers

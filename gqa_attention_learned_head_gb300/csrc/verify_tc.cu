@@ -318,37 +318,38 @@ __global__ void __launch_bounds__(kThreads, 2)
                 if (is_k)
                     for (int q = p - 2 < 0 ? 0 : p - 2; q < p; ++q) (void)mbar_wait(&sm.q_full[q & 1], (q >> 1) & 1);
             }
-        } else if (warp == 1 && lane == 0) {
+        } else if (warp == 1) {
             // ------------------------------------------------------------ S issuer: S_j = Q K_j^T
+            // (the whole warp walks the loop, one elected lane issues)
             const uint32_t tS = tbase + kColS;
             int J = 0, p = 0;
             bool ok = true;
             Piece pc;
             while (ok && walk.next(a, pc)) {
-                if (!(ok = mbar_wait(&sm.q_full[p & 1], (p >> 1) & 1))) break;
+                if (!(ok = warp_wait(&sm.q_full[p & 1], (p >> 1) & 1))) break;
                 const uint32_t qaddr = smem_u32(sm.q[p & 1]);
                 for (int t = pc.ta; t < pc.tb; ++t, ++J) {
                     const int st = J % kKStages;
-                    ok = mbar_wait(&sm.k_full[st], (J / kKStages) & 1) && (J == 0 || mbar_wait(&sm.s_free, (J - 1) & 1));
+                    ok = warp_wait(&sm.k_full[st], (J / kKStages) & 1) && (J == 0 || warp_wait(&sm.s_free, (J - 1) & 1));
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t kaddr = smem_u32(sm.k[st]);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        tc_mma_ss(tS, sw128_desc(qaddr + kk * 32), sw128_desc(kaddr + kk * 32), kIdescQK, kk > 0);
-                    tc_commit(&sm.s_full);
-                    tc_commit(&sm.k_empty[st]);
+                        tc_mma_ss_warp(tS, sw128_desc(qaddr + kk * 32), sw128_desc(kaddr + kk * 32), kIdescQK, kk > 0);
+                    tc_commit_warp(&sm.s_full);
+                    tc_commit_warp(&sm.k_empty[st]);
                 }
-                tc_commit(&sm.q_empty[p & 1]);  // this piece's Q slot is free once its products end
+                tc_commit_warp(&sm.q_empty[p & 1]);  // this piece's Q slot is free once its products end
                 ++p;
             }
-            if (!ok) atomicOr(a.err, kErrTimeout);
-            tc_commit(&sm.mma_done);  // every MMA of both issuers has finished before TMEM is released
-            (void)mbar_wait(&sm.mma_done, 0);
+            if (!ok && lane == 0) atomicOr(a.err, kErrTimeout);
+            tc_commit_warp(&sm.mma_done);  // every MMA of both issuers has finished before TMEM is released
+            (void)warp_wait(&sm.mma_done, 0);
         } else if (warp == 2) {
             // ------------------------------------------------------------ PV issuer: O += P_j V_j
-            // Lane 0 issues; the whole warp zeroes the rows past the cache end of a segment's last V tile
-            // (they may hold anything, and a 0 weight times NaN is NaN) before its product.
+            // One elected lane issues; the whole warp zeroes the rows past the cache end of a segment's last V
+            // tile (they may hold anything, and a 0 weight times NaN is NaN) before its product.
             const uint32_t tO = tbase + kColO, tP = tbase + kColP;
             int J = 0;
             bool ok = true;
@@ -365,26 +366,21 @@ __global__ void __launch_bounds__(kThreads, 2)
                         __syncwarp();
                     }
                     if (!(ok = warp_wait(&sm.p_full, J & 1))) break;
-                    if (lane == 0) {
-                        tc_fence_after();
-                        const uint32_t vaddr = smem_u32(sm.v[st]);
-                        // P_j is written only after the softmax has read the previous piece's O, so the
-                        // first tile of a piece may start O afresh
+                    tc_fence_after();
+                    const uint32_t vaddr = smem_u32(sm.v[st]);
+                    // P_j is written only after the softmax has read the previous piece's O, so the first tile of
+                    // a piece may start O afresh
 #pragma unroll
-                        for (int ks = 0; ks < 8; ++ks)
-                            tc_mma_ts(tO, tP + ks * 8, sw128_desc(vaddr + ks * 2048), kIdescPV,
-                                      (t > pc.ta || ks > 0) ? 1u : 0u);
-                        tc_commit(&sm.v_empty[st]);
-                        tc_commit(&sm.o_done);
-                    }
-                    __syncwarp();
+                    for (int ks = 0; ks < 8; ++ks)
+                        tc_mma_ts_warp(tO, tP + ks * 8, sw128_desc(vaddr + ks * 2048), kIdescPV,
+                                       (t > pc.ta || ks > 0) ? 1u : 0u);
+                    tc_commit_warp(&sm.v_empty[st]);
+                    tc_commit_warp(&sm.o_done);
                 }
             }
-            if (lane == 0) {
-                if (!ok) atomicOr(a.err, kErrTimeout);
-                tc_commit(&sm.mma_done);
-                (void)mbar_wait(&sm.mma_done, 0);
-            }
+            if (!ok && lane == 0) atomicOr(a.err, kErrTimeout);
+            tc_commit_warp(&sm.mma_done);
+            (void)warp_wait(&sm.mma_done, 0);
         }
     } else {
         // 128 x 56 + 128 x 200 = 256 x 128, the launch's registers
