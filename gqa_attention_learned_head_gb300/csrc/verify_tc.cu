@@ -119,7 +119,43 @@ __global__ void __launch_bounds__(kThreads, 2)
     Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = a.B, Hkv = a.Hkv, R = a.R, QL = a.QL, G = a.G;
-    // a programmatic dependent of what precedes it on the stream: nothing is read before that has
+    const int active = (R + 31) / 32;  // softmax warps that hold rows
+
+    // ---- 0. set-up that reads no input (barriers, tensor memory, the Q padding): done before the wait
+    // below, so it overlaps the preceding kernel's tail
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm.q_full[i], 1);
+            mbar_init(&sm.q_empty[i], 1);
+        }
+        for (int i = 0; i < kKStages; ++i) {
+            mbar_init(&sm.k_full[i], 1);
+            mbar_init(&sm.k_empty[i], 1);
+        }
+        for (int i = 0; i < kVStages; ++i) {
+            mbar_init(&sm.v_full[i], 1);
+            mbar_init(&sm.v_empty[i], 1);
+        }
+        mbar_init(&sm.s_full, 1);
+        mbar_init(&sm.s_free, 32 * active);
+        mbar_init(&sm.p_full, 32 * active);
+        mbar_init(&sm.o_done, 1);
+        mbar_init(&sm.mma_done, 2);
+        fence_mbar_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 1) {
+        tmem_alloc(&sm.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    // Q rows R..127 (no query) are zeros, so their scores stay finite; the TMA writes rows 0..R-1
+    for (int e = R * 8 + tid; e < kBM * 8; e += kThreads) {
+        reinterpret_cast<uint4*>(sm.q[0])[e] = make_uint4(0u, 0u, 0u, 0u);
+        reinterpret_cast<uint4*>(sm.q[1])[e] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async_smem();
+
+    // a programmatic dependent of what precedes it on the stream: no input is read before that has
     // completed; the split merge behind this kernel may be scheduled once every CTA runs
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -172,8 +208,14 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     const long long C = U > 0 ? effective_shares(a.tc_grid, a.fixed_workers, kMinTiles, U) : 0;
     const long long cta = blockIdx.x;
-    if (cta >= C) {
+    if (cta >= C) {  // no share: release the tensor memory taken above (the whole CTA is here)
         if (tid == 0 && a.merge_list) a.merge_list[cta] = make_int2(-1, 0);
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 1) {
+            tc_fence_after();
+            tmem_dealloc(sm.tmem_base, kTmemCols);
+        }
         return;
     }
     const long long x0 = cta * U / C, x1 = (cta + 1) * U / C;
@@ -228,39 +270,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     walk.seg_start = sm.found[1] + (long long)walk.g * walk.tiles;
     walk.x = x0;
     walk.x1 = x1;
-    const int active = (R + 31) / 32;  // softmax warps that hold rows
-
-    if (tid == 0) {
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&sm.q_full[i], 1);
-            mbar_init(&sm.q_empty[i], 1);
-        }
-        for (int i = 0; i < kKStages; ++i) {
-            mbar_init(&sm.k_full[i], 1);
-            mbar_init(&sm.k_empty[i], 1);
-        }
-        for (int i = 0; i < kVStages; ++i) {
-            mbar_init(&sm.v_full[i], 1);
-            mbar_init(&sm.v_empty[i], 1);
-        }
-        mbar_init(&sm.s_full, 1);
-        mbar_init(&sm.s_free, 32 * active);
-        mbar_init(&sm.p_full, 32 * active);
-        mbar_init(&sm.o_done, 1);
-        mbar_init(&sm.mma_done, 2);
-        fence_mbar_init();
-        fence_proxy_async_smem();
-    }
-    if (warp == 1) {
-        tmem_alloc(&sm.tmem_base, kTmemCols);
-        tmem_relinquish();
-    }
-    // Q rows R..127 (no query) are zeros, so their scores stay finite; the TMA writes rows 0..R-1
-    for (int e = R * 8 + tid; e < kBM * 8; e += kThreads) {
-        reinterpret_cast<uint4*>(sm.q[0])[e] = make_uint4(0u, 0u, 0u, 0u);
-        reinterpret_cast<uint4*>(sm.q[1])[e] = make_uint4(0u, 0u, 0u, 0u);
-    }
-    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
