@@ -7,7 +7,7 @@ import torch
 
 import oracle
 from gqa_attention_learned_head_gb300 import workloads as W
-from parity_utils import assert_parity
+from parity_utils import assert_parity, growing_scores
 
 pytestmark = pytest.mark.gpu
 
@@ -222,3 +222,12 @@ def test_benchmark_draw_of_the_batched_workload(S):
     assert S.sinkattn_get_error() == 0
     c = g.to("cpu")
     assert_parity(out.float().cpu().numpy(), lse.cpu().numpy(), *ref(c), "benchmark draw")
+
+
+@pytest.mark.parametrize("workers", [0, 13])
+def test_growing_scores(S, workers):
+    """Scores that rise along the cache (the running max moves on every page), whole and split."""
+    inp = growing_scores(W.make_decode(4, 64, 8, [700, 300, 2000, 129], seed=83), seed=84)
+    out, lse, err = run(S, inp, num_workers=workers)
+    assert err == 0
+    assert_parity(out, lse, *ref(inp), f"workers={workers}")

@@ -6,7 +6,7 @@ import torch
 
 import oracle
 from gqa_attention_learned_head_gb300 import workloads as W
-from parity_utils import assert_parity
+from parity_utils import assert_parity, growing_scores
 
 pytestmark = pytest.mark.gpu
 
@@ -236,3 +236,20 @@ def test_empty_pool(S):
     out, lse = S.sinkattn_verify(q, pages, pages, pt, lens, sinks, 0.125)
     assert S.sinkattn_get_error() == S.ERR_BAD_PAGE
     assert bool((out == 0).all()) and torch.equal(lse, sinks.expand(3, QL, Hq))
+
+
+def test_growing_scores_rescale_o(S):
+    """Scores that rise along the cache by ~10 (log2 units) per 128-key tile at kv_len 700: each row's
+    running max passes the lazy-rescale threshold tile after tile, so O is rescaled in tensor memory
+    again and again; linear drafts and a tree, with and without split segments."""
+    inp = growing_scores(W.make_decode(4, 64, 8, [700, 300, 2000, 129], seed=81, q_len=4), seed=82)
+    _, rl = ref(inp)
+    assert float(rl[0].max()) > 35.0  # the first request's last row sees scores from ~0 to ~40
+    masks = [W.tree_masks([-1, 0, 0, 1])] * 4
+    for workers in (0, 9):
+        out, lse, err = run(S, inp, num_workers=workers)
+        assert err == 0
+        assert_parity(out, lse, *ref(inp), f"linear workers={workers}")
+        out, lse, err = run_tree(S, inp, masks, num_workers=workers)
+        assert err == 0
+        assert_parity(out, lse, *ref_tree(inp, masks), f"tree workers={workers}")
