@@ -17,17 +17,15 @@
 //
 //   warp 0      TMA: both Q tiles once, then K_j into a 3-stage ring.
 //   warp 3      TMA: V_j into a 3-stage ring.
-//   warp 1      allocates all 512 TMEM columns; one lane issues S_w = Q_w K_j^T
-//               for w = 0, 1 into the next free score buffer.
-//   warp 2      one lane issues O_w += P_w V_j as soon as P_w is written.
+//   warp 1      allocates all 512 TMEM columns; issues S_w = Q_w K_j^T for
+//               w = 0, 1 as soon as warpgroup w has read its previous S.
+//   warp 2      issues O_w += P_w V_j as soon as P_w is written.
+// The two issuer warps walk their loops warp-wide and one elected lane issues
+// each product (operands computed warp-uniformly: the products go out at the
+// tensor pipe's rate, which a lone lane in a divergent branch does not reach).
 //   warps 4-7   softmax of head h0 (warpgroup 0), thread r owns query row r.
 //   warps 8-11  softmax of head h0 + 1 (warpgroup 1).
-// TMEM columns: three 128-column score buffers at 0, 128, 256, taken in turn by the
-// products S_0(0), S_1(0), S_0(1), ... (tile j, head w -> buffer (2j + w) mod 3);
-// P_w (bf16 pairs) overwrites the first 64 columns of its own scores, and the
-// buffer is free again once O_w += P_w V_j has read it.  O_w at 384 + 64 w.  So
-// a softmax writes P as soon as its exps are done, and the scores of the next
-// tile are already waiting in another buffer.
+// TMEM columns: S_w at 128 w, O_w at 256 + 64 w, P_w (bf16 pairs) at 384 + 64 w.
 // Every wait is bounded; a wait that gives up sets the device error word and
 // the kernel winds down (the other waits then give up too).
 #include "args_prefill.h"
@@ -42,7 +40,7 @@ using namespace tc;
 
 constexpr int kThreads = 384;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColO = 384;  // score buffers at kColS + 128 b, b < 3; O_w at kColO + 64 w
+constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
 constexpr int kKStages = 3, kVStages = 3;
 constexpr uint32_t kProducerRegs = 72, kSoftmaxRegs = 208;  // 128 x 72 + 256 x 208 <= 384 x 168
 
@@ -55,8 +53,7 @@ struct __align__(1024) Smem {
     uint8_t k[kKStages][kTileBytes];
     uint8_t v[kVStages][kTileBytes];
     uint64_t q_full, k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
-    uint64_t s_full[2], p_full[2], o_done[2];
-    uint64_t buf_free[3];  // score buffer b: the P it held has been read by its PV product
+    uint64_t s_full[2], s_free[2], p_full[2], o_done[2];
     // turn[w][k]: warp k of warpgroup w may exponentiate; completed by warp k of the other warpgroup (the
     // same SM sub-partition, whose exp unit the two share) when it has finished its exp phase
     uint64_t turn[2][4];
@@ -122,11 +119,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int w = 0; w < 2; ++w) {
             mbar_init(&sm.s_full[w], 1);
+            mbar_init(&sm.s_free[w], 128);
             mbar_init(&sm.p_full[w], 128);
             mbar_init(&sm.o_done[w], 1);
             for (int k = 0; k < 4; ++k) mbar_init(&sm.turn[w][k], 1);
         }
-        for (int b = 0; b < 3; ++b) mbar_init(&sm.buf_free[b], 1);
         mbar_init(&sm.mma_done, 2);
         mbar_init(&sm.v_fixed, 1);
         fence_mbar_init();
@@ -237,7 +234,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 (void)mbar_wait(&sm.v_full[j % kVStages], (j / kVStages) & 1);
         } else if (warp == 1) {
             // ------------------------------------------------------------ S issuer: S_w = Q_w K_j^T
-            // (the whole warp walks the loop, one elected lane issues)
             bool ok = warp_wait(&sm.q_full, 0);
             for (int j = 0; ok && j < ntile; ++j) {
                 const int st = j % kKStages;
@@ -245,15 +241,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t kaddr = smem_u32(sm.k[st]);
 #pragma unroll
                 for (int w = 0; w < 2; ++w) {
-                    // product i = 2j + w takes buffer i mod 3 once the P of product i - 3 in it has been consumed
-                    const int i = 2 * j + w, buf = i % 3;
-                    if (i >= 3 && !(ok = warp_wait(&sm.buf_free[buf], ((i / 3) - 1) & 1))) break;
+                    if (j > 0 && !(ok = warp_wait(&sm.s_free[w], (j - 1) & 1))) break;
                     tc_fence_after();
                     const uint32_t qaddr = smem_u32(sm.q[w]);
-                    const uint32_t tS = tbase + kColS + 128u * (uint32_t)buf;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        tc_mma_ss_warp(tS, sw128_desc(qaddr + kk * 32), sw128_desc(kaddr + kk * 32), kIdescQK, kk > 0);
+                        tc_mma_ss_warp(tbase + kColS + 128u * w, sw128_desc(qaddr + kk * 32),
+                                       sw128_desc(kaddr + kk * 32), kIdescQK, kk > 0);
                     tc_commit_warp(&sm.s_full[w]);
                 }
                 if (!ok) break;
@@ -264,7 +258,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             (void)warp_wait(&sm.mma_done, 0);
         } else if (warp == 2) {
             // ------------------------------------------------------------ PV issuer: O_w += P_w V_j
-            // (the whole warp walks the loop, one elected lane issues)
             bool ok = true;
             for (int j = 0; ok && j < ntile; ++j) {
                 const int st = j % kVStages;
@@ -276,14 +269,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int w = 0; w < 2; ++w) {
                     if (!(ok = warp_wait(&sm.p_full[w], j & 1))) break;
                     tc_fence_after();
-                    const int buf = (2 * j + w) % 3;
-                    const uint32_t tO = tbase + kColO + 64u * w, tP = tbase + kColS + 128u * (uint32_t)buf;
+                    const uint32_t tO = tbase + kColO + 64u * w, tP = tbase + kColP + 64u * w;
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks)
                         tc_mma_ts_warp(tO, tP + ks * 8, sw128_desc(vaddr + ks * 2048), kIdescPV,
                                        (j > 0 || ks > 0) ? 1u : 0u);
                     tc_commit_warp(&sm.o_done[w]);
-                    tc_commit_warp(&sm.buf_free[buf]);
                 }
                 if (!ok) break;
                 tc_commit_warp(&sm.v_empty[st]);  // V_j read by both products
@@ -299,21 +290,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int h = h0 + w;
         const int r = threadIdx.x - 128 - 128 * w;
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t tS = tbase + lane_off + kColS + 128u * w;
         const uint32_t tO = tbase + lane_off + kColO + 64u * w;
+        const uint32_t tP = tbase + lane_off + kColP + 64u * w;
         const int qrow = row0 + r;
         const float scale_log2 = a.scale_log2;
         float m = __ldg(&a.sinks[h]) * kLog2e;  // running max, seeded with the sink
         float d = 1.f;                          // e^(sink - m) = 1
         bool ok = true;
         for (int j = 0; j < ntile; ++j) {
-            // this tile's scores, and later its P, in buffer (2j + w) mod 3
-            const uint32_t tS = tbase + lane_off + kColS + 128u * (uint32_t)((2 * j + w) % 3);
             if (!(ok = warp_wait(&sm.s_full[w], j & 1))) break;
             tc_fence_after();
             float s[128];
 #pragma unroll
             for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
             tc_wait_ld();
+            tc_fence_before();
+            mbar_arrive(&sm.s_free[w]);
 
             const int kb = j * kBN;
             const bool masked = (kb + kBN > kv_total) || (a.causal && kb + kBN - 1 > start + row0);
@@ -380,27 +373,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             // test makes the arrival wait for every exp2 of the tile.
             __syncwarp();
             if (lane == 0 && !(d < 0.f)) mbar_arrive(&sm.turn[w ^ 1][warp & 3]);  // the partner warp's turn
-            // O_{j-1} must be final before O is rescaled, and is waited for at every tile before P_j is handed
-            // over (so the barrier never runs two phases ahead of this wait); P_j itself goes into this tile's
-            // own buffer and needs no wait.
-            const bool rescale_any = __any_sync(0xffffffffu, rescale_o);  // rescale_o implies j > 0
-            if (rescale_any) {
+            if (j > 0) {  // P_{j-1} consumed and O_{j-1} final before P and O are touched
                 if (!(ok = warp_wait(&sm.o_done[w], (j - 1) & 1))) break;
                 tc_fence_after();
+                if (__any_sync(0xffffffffu, rescale_o)) {
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    uint32_t o[32];
-                    tmem_ld32(tO + c * 32, o);
-                    tc_wait_ld();
+                    for (int c = 0; c < 2; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + c * 32, o);
+                        tc_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * factor);
-                    tmem_st32(tO + c * 32, o);
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * factor);
+                        tmem_st32(tO + c * 32, o);
+                    }
                 }
             }
-            tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-            tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+            tmem_st32(tP, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+            tmem_st32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
             tc_wait_st();
-            if (j > 0 && !rescale_any && !(ok = warp_wait(&sm.o_done[w], (j - 1) & 1))) break;
             tc_fence_before();
             mbar_arrive(&sm.p_full[w]);
         }
