@@ -62,6 +62,9 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) kv_append_kernel(const Ap
         reinterpret_cast<uint4*>(a.k_pages + row * kHeadDim)[part] = kx;
         reinterpret_cast<uint4*>(a.v_pages + row * kHeadDim)[part] = vx;
     }
+    // this warp's stores are issued: a prefill launched behind this kernel as a programmatic dependent may
+    // start its CTAs once every CTA gets here or exits (they wait for this grid to complete before reading)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 }  // namespace

@@ -65,6 +65,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     int* order_ints = reinterpret_cast<int*>(&sm + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+    // A programmatic dependent of what precedes it on the stream (its CTAs may start while that kernel's
+    // tail runs): nothing is read before that kernel has completed.  It lets no dependent of its own start
+    // early, since their waiting CTAs would hold SMs that its later CTAs need.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
     SeqOrder order;
     order.build_warp0(order_ints, a.cu_seqlens, kPaged ? a.start_pos : nullptr, a.N, a.T, a.max_seqlen, kBM, a.err);
     __syncthreads();
@@ -416,8 +421,17 @@ cudaError_t launch(const PrefillArgs& a, const CUtensorMap& tq, const CUtensorMa
         if (e != cudaSuccess) return e;
         if (dev < 64) set_to[dev] = smem;
     }
-    prefill_tc_kernel<kPaged><<<(unsigned)grid, kThreads, smem, stream>>>(tq, tk, tv, a);
-    return cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<kPaged>, tq, tk, tv, a);
 }
 
 }  // namespace

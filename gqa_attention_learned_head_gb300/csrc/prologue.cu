@@ -151,6 +151,9 @@ __global__ void __launch_bounds__(kWarps * 32) qkv_prologue_kernel(const Prologu
         unpack8(__ldg(row + hd * 8 + o1 / 8), w);
         finish(hd, u, w);
     }
+    // this warp's stores are issued: a prefill launched behind this kernel as a programmatic dependent may
+    // start its CTAs once every CTA gets here or exits (they wait for this grid to complete before reading)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 }  // namespace
