@@ -83,10 +83,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     int* order_ints = reinterpret_cast<int*>(&sm + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // A programmatic dependent of what precedes it on the stream (its CTAs may start while that kernel's
-    // tail runs): nothing is read before that kernel has completed.  It lets no dependent of its own start
-    // early, since their waiting CTAs would hold SMs that its later CTAs need.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // Paged: a programmatic dependent of what precedes it on the stream (the append or the prologue that
+    // wrote its K / V, whose last CTAs it may overlap): nothing is read before that kernel has completed.
+    // It lets no dependent of its own start early, since their waiting CTAs would hold SMs that its later
+    // CTAs need.  (The contiguous form follows kernels that do not let it start early: it waits for
+    // nothing and launches as a plain kernel, since the wait costs its many short CTAs ~0.3%.)
+    if constexpr (kPaged) asm volatile("griddepcontrol.wait;" ::: "memory");
 
     SeqOrder order;
     order.build_warp0(order_ints, a.cu_seqlens, kPaged ? a.start_pos : nullptr, a.N, a.T, a.max_seqlen, kBM, a.err);
@@ -479,7 +481,7 @@ cudaError_t launch_pp(const PrefillArgs& a, const CUtensorMap& tq, const CUtenso
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = kPaged ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, prefill_pp_kernel<kPaged>, tq, tk, tv, a);
 }
 
