@@ -10,12 +10,13 @@
 //   warps 0, 3  TMA producers: Q once and K_j tiles into a 3-stage ring
 //               (warp 0), V_j tiles into a 2-stage ring (warp 3); 128 keys x 64,
 //               128-byte swizzle.
-//   warp 1      allocates 256 TMEM columns; one lane issues S_j = Q K_j^T
-//               (M=128, N=128, K=64; SMEM x SMEM -> TMEM) as soon as the softmax
-//               has read S_{j-1}.
-//   warp 2      one lane issues O += P_j V_j (M=128, N=64, K=128; P read from
-//               TMEM) as soon as P_j is written.  Two issuers, so that neither
-//               chain waits on the other's wake-up.
+//   warp 1      allocates 256 TMEM columns; issues S_j = Q K_j^T (M=128,
+//               N=128, K=64; SMEM x SMEM -> TMEM) as soon as the softmax has
+//               read S_{j-1}.
+//   warp 2      issues O += P_j V_j (M=128, N=64, K=128; P read from TMEM) as
+//               soon as P_j is written.  Two issuers, so that neither chain
+//               waits on the other's wake-up; each walks its loop warp-wide and
+//               one elected lane issues the products.
 //   warps 4-7   softmax: thread r owns query row r (TMEM lane r).  It reads
 //               S_j, releases the S columns at once (so S_{j+1} can start),
 //               masks the diagonal tile, takes exp2 against a running max that

@@ -23,9 +23,10 @@
 //               i * G + h) into a 2-slot Q ring and the K tiles, warp 3 the V
 //               tiles; a tile is 8 page copies of 2 KB (lanes 0-7), 128-byte
 //               swizzle.
-//   warp 1      allocates 256 TMEM columns; one lane issues S_j = Q K_j^T.
-//   warp 2      one lane issues O += P_j V_j (P read from TMEM; the first tile
-//               of a piece starts O afresh).
+//   warp 1      allocates 256 TMEM columns; issues S_j = Q K_j^T.
+//   warp 2      issues O += P_j V_j (P read from TMEM; the first tile of a
+//               piece starts O afresh).  Both issuers walk their loops
+//               warp-wide and one elected lane issues the products.
 //   warps 4-7   softmax, thread r = row r (only the warps that hold rows work),
 //               each row masked at its own causal limit or by its tree mask; at
 //               a piece's end they read O and write the rows (or fp32 partials).
