@@ -158,3 +158,42 @@ def test_paged_prefill_reports_bad_length(S):
                                         max_seqlen=inp.max_seqlen)
     assert S.sinkattn_get_error() == S.ERR_BAD_LENGTH
     assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+
+
+def test_graph_replay_append_and_prefill(S):
+    """The chunked step (append, then the paged prefill, a programmatic dependent of the append) captured
+    once in a CUDA graph and replayed after the inputs in the same buffers changed (other tokens, pool
+    contents and page layout): every replay matches the oracle on its inputs."""
+    prefix, new = [0, 300, 1000, 17], [129, 40, 300, 1]
+    srcs = [W.make_paged_prefill(8, 2, prefix, new, seed=s) for s in (61, 62, 63)]
+    for s in srcs[1:]:
+        assert s.k_pages.shape == srcs[0].k_pages.shape and s.page_table.shape == srcs[0].page_table.shape
+    g = srcs[0].to("cuda")
+    out = torch.empty_like(g.q)
+    lse = torch.empty(g.q.shape[:2], dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream()
+
+    def step():
+        S.sinkattn_kv_append(g.k_new, g.v_new, g.cu_seqlens, g.start_pos, g.page_table, g.k_pages, g.v_pages,
+                             stream=stream)
+        S.sinkattn_prefill_paged(g.q, g.k_pages, g.v_pages, g.page_table, g.cu_seqlens, g.start_pos, g.sinks,
+                                 g.scale, max_seqlen=srcs[0].max_seqlen, out=out, lse=lse, stream=stream)
+
+    with torch.cuda.stream(stream):
+        step()  # warm-up outside the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    for src in srcs + srcs[:1]:
+        for name in ("q", "k_new", "v_new", "k_pages", "v_pages", "page_table", "sinks"):
+            getattr(g, name).copy_(getattr(src, name))
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert S.sinkattn_get_error() == 0
+        kb, vb = oracle.kv_append(src.k_new, src.v_new, src.cu_seqlens, src.start_pos, src.page_table, src.k_pages,
+                                  src.v_pages)
+        ro, rl = oracle.prefill_paged(src.q, kb, vb, src.page_table, src.cu_seqlens, src.start_pos, src.sinks,
+                                      src.scale)
+        assert_parity(out.float().cpu().numpy(), lse.cpu().numpy(), ro, rl, "graph replay")
