@@ -8,6 +8,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "call_range.h"
 #include "kernels.h"
 
 namespace sinkattn {
@@ -213,6 +214,7 @@ sinkattn_status_t sinkattn_decode(const void* q, const void* k_pages, const void
                                   const int32_t* kv_lens, const float* sinks, float scale, void* out, float* lse,
                                   const sinkattn_decode_dims_t* dims, void* workspace, size_t workspace_bytes,
                                   void* stream) {
+    CallRange range("sinkattn_decode");
     sinkattn_status_t st = check_decode_dims(dims);
     if (st != SINKATTN_OK) return st;
     if (dims->batch == 0) return SINKATTN_OK;
@@ -293,6 +295,7 @@ sinkattn_status_t sinkattn_verify(const void* q, const void* k_pages, const void
                                   const int32_t* kv_lens, const float* sinks, float scale, void* out, float* lse,
                                   const sinkattn_verify_dims_t* dims, void* workspace, size_t workspace_bytes,
                                   void* stream) {
+    CallRange range("sinkattn_verify");
     return verify_common(q, k_pages, v_pages, page_table, kv_lens, nullptr, sinks, scale, out, lse, dims, workspace,
                          workspace_bytes, stream);
 }
@@ -302,6 +305,7 @@ sinkattn_status_t sinkattn_verify_tree(const void* q, const void* k_pages, const
                                        const float* sinks, float scale, void* out, float* lse,
                                        const sinkattn_verify_dims_t* dims, void* workspace, size_t workspace_bytes,
                                        void* stream) {
+    CallRange range("sinkattn_verify_tree");
     if (!tree_mask) return SINKATTN_ERR_INVALID_ARG;
     if (dims && dims->q_len > 64) return SINKATTN_ERR_UNSUPPORTED;
     return verify_common(q, k_pages, v_pages, page_table, kv_lens, tree_mask, sinks, scale, out, lse, dims, workspace,
@@ -385,6 +389,7 @@ sinkattn_status_t verify_common(const void* q, const void* k_pages, const void* 
 sinkattn_status_t sinkattn_kv_append(const void* k, const void* v, const int32_t* cu_seqlens, const int32_t* start_pos,
                                      const int32_t* page_table, void* k_pages, void* v_pages,
                                      const sinkattn_paged_dims_t* dims, void* stream) {
+    CallRange range("sinkattn_kv_append");
     sinkattn_status_t st = check_paged_dims(dims, false);
     if (st != SINKATTN_OK) return st;
     if (dims->num_seqs == 0 || dims->total_tokens == 0) return SINKATTN_OK;
@@ -415,6 +420,7 @@ sinkattn_status_t sinkattn_prefill_paged(const void* q, const void* k_pages, con
                                          const int32_t* page_table, const int32_t* cu_seqlens, const int32_t* start_pos,
                                          const float* sinks, float scale, void* out, float* lse,
                                          const sinkattn_paged_dims_t* dims, void* stream) {
+    CallRange range("sinkattn_prefill_paged");
     sinkattn_status_t st = check_paged_dims(dims, true);
     if (st != SINKATTN_OK) return st;
     const sinkattn_paged_dims_t& d = *dims;
@@ -470,6 +476,7 @@ sinkattn_status_t sinkattn_qkv_prologue(const void* qkv, const void* bias, const
                                         const int32_t* start_pos, const int32_t* page_table, const sinkattn_rope_t* rope,
                                         void* q_out, void* k_pages, void* v_pages, const sinkattn_paged_dims_t* dims,
                                         void* stream) {
+    CallRange range("sinkattn_qkv_prologue");
     sinkattn_status_t st = check_paged_dims(dims, true);
     if (st != SINKATTN_OK) return st;
     if (!rope) return SINKATTN_ERR_INVALID_ARG;
@@ -520,6 +527,7 @@ sinkattn_status_t sinkattn_qkv_prologue(const void* qkv, const void* bias, const
 sinkattn_status_t sinkattn_prefill(const void* q, const void* k, const void* v, const int32_t* cu_seqlens,
                                    const float* sinks, float scale, int32_t causal, void* out, float* lse,
                                    const sinkattn_prefill_dims_t* dims, void* stream) {
+    CallRange range("sinkattn_prefill");
     if (!dims) return SINKATTN_ERR_INVALID_ARG;
     const sinkattn_prefill_dims_t& d = *dims;
     if (d.num_seqs < 0 || d.total_tokens < 0 || d.max_seqlen < 0 || d.num_q_heads <= 0 || d.num_kv_heads <= 0 ||
@@ -572,6 +580,7 @@ sinkattn_status_t sinkattn_prefill(const void* q, const void* k, const void* v, 
 
 sinkattn_status_t sinkattn_merge(const float* partial_o, const float* partial_lse, const float* sinks, void* out,
                                  float* lse, const sinkattn_merge_dims_t* dims, void* stream) {
+    CallRange range("sinkattn_merge");
     if (!dims) return SINKATTN_ERR_INVALID_ARG;
     if (dims->num_splits < 0 || dims->num_rows < 0 || dims->num_heads <= 0) return SINKATTN_ERR_INVALID_ARG;
     if (dims->head_dim != kHeadDim) return SINKATTN_ERR_UNSUPPORTED;
@@ -601,6 +610,7 @@ sinkattn_status_t sinkattn_selftest_wait_timeout(void* stream) {
 }
 
 sinkattn_status_t sinkattn_get_error(void* stream) {
+    CallRange range("sinkattn_get_error");
     DeviceState* ds = nullptr;
     sinkattn_status_t st = device_state(&ds);
     if (st != SINKATTN_OK) return st;

@@ -29,6 +29,8 @@
 //   * No cudaMalloc, cudaFree or allocating library routine is called.
 #include <sinkattn.h>
 
+#include "call_range.h"
+
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -63,6 +65,7 @@ extern "C" sinkattn_status_t sinkattn_decode_noalloc(const void* q, const void* 
                                                      const int32_t* page_table, const int32_t* kv_lens,
                                                      const float* sinks, float scale, void* out, float* lse,
                                                      const sinkattn_decode_dims_t* dims, void* stream) {
+    sinkattn::CallRange range("sinkattn_decode_noalloc");
     const size_t need = sinkattn_decode_workspace_size(dims);
     if (need == 0)  // invalid sizes: let the regular entry point report which check failed
         return sinkattn_decode(q, k_pages, v_pages, page_table, kv_lens, sinks, scale, out, lse, dims, nullptr, 0,
